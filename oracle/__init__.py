@@ -1,0 +1,248 @@
+"""CPU oracle for the MXFP4 / NVFP4 block-scaled GEMM and BF16 quantizer.
+
+TEST INFRASTRUCTURE ONLY.  The product path (the CUDA library and its Python
+binding) never imports, links or runs anything in this package.  Only the
+tests, the smoke check in the entry module and the CPU-baseline leg of the
+benchmark use it.
+
+The arithmetic lives in ``mx_oracle.c`` (plain C99, binary64 accumulation,
+built with ``-ffp-contract=off``); this module builds it with gcc and wraps it
+with ctypes + numpy.  It shares no code with the CUDA library.  Every
+function's definition and the page passage it follows are stated in the C
+file's header comment and at each function.
+
+Pinned by the ``-m "not gpu"`` tests (``tests/test_oracle_*.py``): exhaustive
+E2M1/E4M3/BF16 codec checks against brute-force nearest-value searches and
+library routines, the exhaustive BF16 quantize sweep, GEMM brute force against
+a dequantize-then-fp64 matmul, and the closed-form invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mx_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+
+FMT_MXFP4 = 0
+FMT_NVFP4 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile mx_oracle.c into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        c_u8p = ctypes.POINTER(ctypes.c_uint8)
+        c_u16p = ctypes.POINTER(ctypes.c_uint16)
+        c_i64 = ctypes.c_int64
+        c_i64p = ctypes.POINTER(ctypes.c_int64)
+        c_f64p = ctypes.POINTER(ctypes.c_double)
+        lib.oracle_e2m1_decode.restype = ctypes.c_double
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint32]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint32
+        lib.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_to_float.restype = ctypes.c_float
+        lib.oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_floor_log2.restype = ctypes.c_int
+        lib.oracle_bf16_floor_log2.argtypes = [ctypes.c_uint16]
+        lib.oracle_ue8m0_decode.restype = ctypes.c_double
+        lib.oracle_ue8m0_decode.argtypes = [ctypes.c_uint32]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint32]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint32
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_mx_quantize.restype = None
+        lib.oracle_mx_quantize.argtypes = [c_u16p, c_i64, c_i64, c_i64, c_u8p, c_u8p]
+        lib.oracle_bf16_amax.restype = ctypes.c_float
+        lib.oracle_bf16_amax.argtypes = [c_u16p, c_i64, c_i64, c_i64]
+        lib.oracle_nvfp4_quantize.restype = None
+        lib.oracle_nvfp4_quantize.argtypes = [c_u16p, c_i64, c_i64, c_i64, c_u8p, c_u8p,
+                                              ctypes.POINTER(ctypes.c_float)]
+        lib.oracle_block_gemm.restype = None
+        lib.oracle_block_gemm.argtypes = [ctypes.c_int, c_u8p, c_u8p, c_u8p, c_u8p,
+                                          c_i64, c_i64, c_i64, ctypes.c_float, ctypes.c_float,
+                                          c_i64p, c_i64, c_i64p, c_i64, c_f64p, c_f64p]
+        lib.oracle_scale_tile.restype = None
+        lib.oracle_scale_tile.argtypes = [c_u8p, c_i64, c_i64, c_u8p]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+# ----------------------------------------------------------------- codecs
+
+def e2m1_decode(code: int) -> float:
+    return _load().oracle_e2m1_decode(int(code))
+
+
+def e2m1_encode(y: float) -> int:
+    return _load().oracle_e2m1_encode(float(y))
+
+
+def bf16_to_float(bits: int) -> float:
+    return _load().oracle_bf16_to_float(int(bits))
+
+
+def bf16_floor_log2(bits: int) -> int:
+    return _load().oracle_bf16_floor_log2(int(bits))
+
+
+def ue8m0_decode(e: int) -> float:
+    return _load().oracle_ue8m0_decode(int(e))
+
+
+def e4m3_decode(b: int) -> float:
+    return _load().oracle_e4m3_decode(int(b))
+
+
+def e4m3_encode(v: float) -> int:
+    return _load().oracle_e4m3_encode(float(v))
+
+
+def round_bf16(d: np.ndarray) -> np.ndarray:
+    """Round binary64 values to BF16 (ties to even), returned as uint16 bits."""
+    lib = _load()
+    flat = np.ascontiguousarray(d, dtype=np.float64).ravel()
+    out = np.empty(flat.shape, dtype=np.uint16)
+    f = lib.oracle_round_bf16
+    for i, v in enumerate(flat.tolist()):
+        out[i] = f(v)
+    return out.reshape(np.shape(d))
+
+
+# ----------------------------------------------------------------- quantizers
+
+def mx_quantize(x_bits: np.ndarray):
+    """BF16 bits [rows, cols] -> (codes [rows, cols/2] u8, scales [rows, cols/32] u8)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    _load().oracle_mx_quantize(_ptr(x, ctypes.c_uint16), rows, cols, cols,
+                               _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def bf16_amax(x_bits: np.ndarray) -> float:
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    return _load().oracle_bf16_amax(_ptr(x, ctypes.c_uint16), rows, cols, cols)
+
+
+def nvfp4_quantize(x_bits: np.ndarray):
+    """BF16 bits [rows, cols] -> (codes [rows, cols/2], E4M3 scales [rows, cols/16], s_t)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 16), dtype=np.uint8)
+    s_t = ctypes.c_float(0.0)
+    _load().oracle_nvfp4_quantize(_ptr(x, ctypes.c_uint16), rows, cols, cols,
+                                  _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                  ctypes.byref(s_t))
+    return codes, scales, np.float32(s_t.value)
+
+
+# ----------------------------------------------------------------- GEMM
+
+def block_gemm(fmt: int, a_codes, a_scales, b_codes, b_scales, m: int, n: int, k: int,
+               a_tensor_scale: float = 1.0, b_tensor_scale: float = 1.0,
+               rows=None, cols=None):
+    """D = A * B^T in binary64 for block-scaled FP4 operands (TN).
+
+    Returns (d, s_abs), both [len(rows), len(cols)] float64, where s_abs is
+    sum_k |a||b| (the scale of the rounding-error bounds).
+    """
+    lib = _load()
+    a_codes = np.ascontiguousarray(a_codes, dtype=np.uint8)
+    b_codes = np.ascontiguousarray(b_codes, dtype=np.uint8)
+    a_scales = np.ascontiguousarray(a_scales, dtype=np.uint8)
+    b_scales = np.ascontiguousarray(b_scales, dtype=np.uint8)
+    blk = 32 if fmt == FMT_MXFP4 else 16
+    assert a_codes.size == m * k // 2 and b_codes.size == n * k // 2
+    assert a_scales.size == m * k // blk and b_scales.size == n * k // blk
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = m if r is None else r.size
+    nc = n if c is None else c.size
+    d = np.zeros((nr, nc), dtype=np.float64)
+    s_abs = np.zeros((nr, nc), dtype=np.float64)
+    lib.oracle_block_gemm(fmt, _ptr(a_codes, ctypes.c_uint8), _ptr(a_scales, ctypes.c_uint8),
+                          _ptr(b_codes, ctypes.c_uint8), _ptr(b_scales, ctypes.c_uint8),
+                          m, n, k, float(a_tensor_scale), float(b_tensor_scale),
+                          None if r is None else _ptr(r, ctypes.c_int64), nr,
+                          None if c is None else _ptr(c, ctypes.c_int64), nc,
+                          _ptr(d, ctypes.c_double), _ptr(s_abs, ctypes.c_double))
+    return d, s_abs
+
+
+def mx_gemm(a_codes, a_scales, b_codes, b_scales, m, n, k, rows=None, cols=None):
+    return block_gemm(FMT_MXFP4, a_codes, a_scales, b_codes, b_scales, m, n, k,
+                      rows=rows, cols=cols)
+
+
+def nvfp4_gemm(a_codes, a_scales, b_codes, b_scales, m, n, k, a_tensor_scale,
+               b_tensor_scale, rows=None, cols=None):
+    return block_gemm(FMT_NVFP4, a_codes, a_scales, b_codes, b_scales, m, n, k,
+                      a_tensor_scale, b_tensor_scale, rows=rows, cols=cols)
+
+
+# ----------------------------------------------------------------- scale order
+
+def scale_tile(plain: np.ndarray) -> np.ndarray:
+    """Plain scales [rows, kb] -> the 128x4 tiled order (flat uint8 array)."""
+    p = np.ascontiguousarray(plain, dtype=np.uint8)
+    rows, kb = p.shape
+    rows_pad = (rows + 127) // 128 * 128
+    kb_pad = (kb + 3) // 4 * 4
+    out = np.zeros(rows_pad * kb_pad, dtype=np.uint8)
+    _load().oracle_scale_tile(_ptr(p, ctypes.c_uint8), rows, kb, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+# ----------------------------------------------------------------- helpers
+
+def e2m1_decode_array(codes: np.ndarray, k: int) -> np.ndarray:
+    """Unpack codes [rows, k/2] to float64 element values [rows, k] (no scales).
+
+    Element 2t is the low nibble of byte t, element 2t+1 the high nibble.
+    """
+    table = np.array([e2m1_decode(c) for c in range(16)], dtype=np.float64)
+    c = np.asarray(codes, dtype=np.uint8)
+    lo = table[c & 0xF]
+    hi = table[c >> 4]
+    out = np.empty(c.shape[:-1] + (k,), dtype=np.float64)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
