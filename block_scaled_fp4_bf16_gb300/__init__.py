@@ -1,1 +1,14 @@
-"""GB300 (sm_103a) MXFP4 / NVFP4 block-scaled GEMM and BF16 quantizer."""
+"""GB300 (sm_103a) MXFP4 / NVFP4 block-scaled GEMM and BF16 quantizer.
+
+The compute path is the C-ABI library libmxfp4.so (include/mxfp4.h), built
+from the CUDA sources in csrc/ by build.py; ``_binding`` exposes each entry
+point under its C name.  Importing this package loads nothing: the library
+is opened on the first call, and a call without it raises.
+"""
+from ._binding import (  # noqa: F401
+    MX_ERR_ALIGNMENT, MX_ERR_CUDA, MX_ERR_DEVICE_TIMEOUT, MX_ERR_INVALID_ARG, MX_ERR_NOT_COMPILED,
+    MX_ERR_UNSUPPORTED_ARCH, MX_ERR_UNSUPPORTED_FEATURE, MX_ERR_UNSUPPORTED_SHAPE,
+    MX_ERR_WORKSPACE, MX_FMT_MXFP4, MX_FMT_NVFP4, MX_LAYOUT_TN, MX_OK, MX_OUT_BF16, MX_OUT_FP32,
+    MX_SCALE_PLAIN, MX_SCALE_TCGEN05, MXError, lib, mx_available, mx_device_status,
+    mx_error_string, mx_gemm_workspace_bytes, mx_quantize_bf16, mx_quantize_workspace_bytes,
+    mx_scale_bytes, mx_scale_relayout, mx_selftest_wait_timeout, mxfp4_gemm, nvfp4_gemm)

@@ -1,0 +1,178 @@
+"""ctypes binding of the C ABI in include/mxfp4.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: pointers are taken from torch tensors (or plain
+integer device addresses), the stream defaults to torch's current CUDA
+stream, and a non-zero status raises MXError.  The shared library is loaded
+on first use; if it is missing the call raises (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmxfp4.so")
+
+MX_OK = 0
+MX_ERR_INVALID_ARG = -1
+MX_ERR_NOT_COMPILED = -2
+MX_ERR_UNSUPPORTED_ARCH = -3
+MX_ERR_UNSUPPORTED_SHAPE = -4
+MX_ERR_UNSUPPORTED_FEATURE = -5
+MX_ERR_ALIGNMENT = -6
+MX_ERR_WORKSPACE = -7
+MX_ERR_CUDA = -8
+MX_ERR_DEVICE_TIMEOUT = -9
+
+MX_FMT_MXFP4 = 0
+MX_FMT_NVFP4 = 1
+MX_SCALE_PLAIN = 0
+MX_SCALE_TCGEN05 = 1
+MX_LAYOUT_TN = 0
+MX_OUT_BF16 = 0
+MX_OUT_FP32 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MXError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({mx_error_string(code)})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmxfp4.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, vp, sz, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.mx_error_string.restype = ctypes.c_char_p
+        L.mx_error_string.argtypes = [i32]
+        L.mx_available.restype = i32
+        L.mx_available.argtypes = []
+        L.mx_scale_bytes.restype = sz
+        L.mx_scale_bytes.argtypes = [i64, i64, i32, i32]
+        L.mx_quantize_workspace_bytes.restype = sz
+        L.mx_quantize_workspace_bytes.argtypes = [i64, i64, i32]
+        L.mx_quantize_bf16.restype = i32
+        L.mx_quantize_bf16.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.mx_scale_relayout.restype = i32
+        L.mx_scale_relayout.argtypes = [vp, i64, i64, i32, vp, vp]
+        L.mx_gemm_workspace_bytes.restype = sz
+        L.mx_gemm_workspace_bytes.argtypes = [i64, i64, i64, i32]
+        L.mxfp4_gemm.restype = i32
+        L.mxfp4_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp, sz, vp]
+        L.nvfp4_gemm.restype = i32
+        L.nvfp4_gemm.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp, sz,
+                                 vp]
+        L.mx_device_status.restype = i32
+        L.mx_device_status.argtypes = [vp]
+        L.mx_selftest_wait_timeout.restype = i32
+        L.mx_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        _lib = L
+        return L
+
+
+def _ptr(x):
+    """Device address of a tensor / int / None (NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _nbytes(x) -> int:
+    if x is None:
+        return 0
+    return x.numel() * x.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int) -> int:
+    if rc != MX_OK:
+        raise MXError(fn, rc)
+    return rc
+
+
+def mx_error_string(code: int) -> str:
+    return lib().mx_error_string(code).decode()
+
+
+def mx_available() -> bool:
+    return bool(lib().mx_available())
+
+
+def mx_scale_bytes(rows: int, cols: int, fmt: int, scale_layout: int) -> int:
+    return lib().mx_scale_bytes(rows, cols, fmt, scale_layout)
+
+
+def mx_quantize_workspace_bytes(rows: int, cols: int, fmt: int) -> int:
+    return lib().mx_quantize_workspace_bytes(rows, cols, fmt)
+
+
+def mx_gemm_workspace_bytes(m: int, n: int, k: int, split_k: int = 0) -> int:
+    return lib().mx_gemm_workspace_bytes(m, n, k, split_k)
+
+
+def mx_quantize_bf16(x, rows, cols, ld_x, fmt, scale_layout, codes, scales, tensor_scale=None,
+                     workspace=None, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("mx_quantize_bf16", lib().mx_quantize_bf16(
+        _ptr(x), rows, cols, ld_x, fmt, scale_layout, _ptr(codes), _ptr(scales),
+        _ptr(tensor_scale), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def mx_scale_relayout(plain, rows, cols, fmt, tiled, stream=None):
+    return _check("mx_scale_relayout", lib().mx_scale_relayout(
+        _ptr(plain), rows, cols, fmt, _ptr(tiled), _stream(stream)))
+
+
+def mxfp4_gemm(a_codes, a_scales, b_codes, b_scales, d, m, n, k, layout=MX_LAYOUT_TN,
+               out_dtype=MX_OUT_BF16, split_k=0, workspace=None, workspace_bytes=None,
+               stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("mxfp4_gemm", lib().mxfp4_gemm(
+        _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(d), m, n, k, layout,
+        out_dtype, split_k, _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def nvfp4_gemm(a_codes, a_scales, b_codes, b_scales, a_tensor_scale, b_tensor_scale, d, m, n, k,
+               layout=MX_LAYOUT_TN, out_dtype=MX_OUT_FP32, split_k=0, workspace=None,
+               workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("nvfp4_gemm", lib().nvfp4_gemm(
+        _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(a_tensor_scale),
+        _ptr(b_tensor_scale), _ptr(d), m, n, k, layout, out_dtype, split_k, _ptr(workspace),
+        workspace_bytes, _stream(stream)))
+
+
+def mx_device_status(stream=None) -> int:
+    """Synchronise the stream and return (not raise) the device status code."""
+    return lib().mx_device_status(_stream(stream))
+
+
+def mx_selftest_wait_timeout(timeout_ns: int, stream=None):
+    return _check("mx_selftest_wait_timeout",
+                  lib().mx_selftest_wait_timeout(timeout_ns, _stream(stream)))

@@ -1,0 +1,324 @@
+// C ABI of the library (declarations and contracts: include/mxfp4.h).
+//
+// Conventions follow the C-API review on "Initial integration of a4w4 GEMM"
+// (ROCm/TransformerEngine #663): an int status per call with distinct
+// negative codes and an availability probe; and the stride/arch contract of
+// "feat(ck-tile): aquant GEMM TE to dispatcher bridge" (ROCm/rocm-libraries
+// #9980): packed strides only, the architecture checked at run time, every
+// argument validated before anything is launched.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mx_internal.h"
+#include "mxfp4.h"
+
+#define MX_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+// Device status word (bit 0: a bounded wait ran out).  One copy per device
+// that loads the library; kernels get its device address as an argument.
+__device__ uint32_t g_status_word;
+
+__global__ void probe_kernel() {}
+
+struct DeviceInfo {
+  bool checked = false;
+  int rc = MX_OK;
+  int num_sms = 0;
+  uint32_t *status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+int device_info(DeviceInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MX_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo &d = g_devices[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return MX_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) {
+      d.rc = MX_ERR_UNSUPPORTED_ARCH;
+    } else {
+      cudaFuncAttributes attr;
+      if (cudaFuncGetAttributes(&attr, probe_kernel) != cudaSuccess) {
+        cudaGetLastError();
+        d.rc = MX_ERR_NOT_COMPILED;
+      } else {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MX_ERR_CUDA;
+        d.status = static_cast<uint32_t *>(p);
+        d.rc = MX_OK;
+      }
+    }
+    d.checked = true;
+  }
+  if (d.rc != MX_OK) return d.rc;
+  *out = &d;
+  return MX_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int block_of(int format) { return format == MX_FMT_MXFP4 ? 32 : 16; }
+
+bool valid_format(int f) { return f == MX_FMT_MXFP4 || f == MX_FMT_NVFP4; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+  });
+  return fn;
+}
+
+// Tensor map over packed FP4 codes [rows, k/2] bytes: boxes of 128 bytes
+// (256 codes along K) x box_rows rows, 128-byte swizzle, zero fill past the
+// last row.
+int encode_codes_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t k, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MX_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
+  const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+int launch_rc(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+int num_sms_or_default() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+    return sms;
+  cudaGetLastError();
+  return 152;
+}
+
+int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *b_codes,
+                const void *b_scales, const float *a_ts, const float *b_ts, void *d, int64_t m,
+                int64_t n, int64_t k, int layout, int out_dtype, int split_k, void *workspace,
+                size_t workspace_bytes, void *stream) {
+  if (!a_codes || !a_scales || !b_codes || !b_scales || !d) return MX_ERR_INVALID_ARG;
+  if (fmt == MX_FMT_NVFP4 && (!a_ts || !b_ts)) return MX_ERR_INVALID_ARG;
+  if (split_k < 0) return MX_ERR_INVALID_ARG;
+  if (layout != MX_LAYOUT_TN) return MX_ERR_UNSUPPORTED_FEATURE;
+  if (out_dtype != MX_OUT_BF16 && out_dtype != MX_OUT_FP32) return MX_ERR_UNSUPPORTED_FEATURE;
+  if (m <= 0 || n <= 0 || k <= 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (k % 256 != 0 || m % 32 != 0 || n % 32 != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (m >= (int64_t(1) << 31) || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31))
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a_codes) || !aligned16(b_codes) || !aligned16(a_scales) || !aligned16(b_scales) ||
+      !aligned16(d))
+    return MX_ERR_ALIGNMENT;
+  if (fmt == MX_FMT_NVFP4 &&
+      ((reinterpret_cast<uintptr_t>(a_ts) & 3u) || (reinterpret_cast<uintptr_t>(b_ts) & 3u)))
+    return MX_ERR_ALIGNMENT;
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  int bn = 128, splits = 1;
+  mx::gemm_plan(m, n, k, split_k, dev->num_sms, &bn, &splits);
+  if (splits > 1) {
+    const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(m) *
+                        static_cast<size_t>(n) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return MX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+  }
+  CUtensorMap tma, tmb;
+  if (encode_codes_map(&tma, a_codes, m, k, 128) != MX_OK) return MX_ERR_CUDA;
+  if (encode_codes_map(&tmb, b_codes, n, k, bn) != MX_OK) return MX_ERR_CUDA;
+  mx::GemmArgs g{};
+  g.fmt = fmt;
+  g.tmap_a = &tma;
+  g.tmap_b = &tmb;
+  g.a_scales = a_scales;
+  g.b_scales = b_scales;
+  g.a_ts = a_ts;
+  g.b_ts = b_ts;
+  g.d = d;
+  g.out_fp32 = out_dtype == MX_OUT_FP32;
+  g.m = m;
+  g.n = n;
+  g.k = k;
+  g.split_k = splits;
+  g.bn = bn;
+  g.workspace = static_cast<float *>(workspace);
+  g.status = dev->status;
+  g.num_sms = dev->num_sms;
+  return launch_rc(mx::launch_gemm(g, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+MX_API const char *mx_error_string(int code) {
+  switch (code) {
+    case MX_OK: return "success";
+    case MX_ERR_INVALID_ARG: return "invalid argument (null pointer, bad enum or leading dim)";
+    case MX_ERR_NOT_COMPILED: return "library built without sm_103a kernels";
+    case MX_ERR_UNSUPPORTED_ARCH: return "current device is not an sm_103 GPU";
+    case MX_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K % 256, M % 32, N % 32, block size)";
+    case MX_ERR_UNSUPPORTED_FEATURE: return "unsupported feature (layout or output dtype)";
+    case MX_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
+    case MX_ERR_WORKSPACE: return "workspace missing or too small";
+    case MX_ERR_CUDA: return "CUDA runtime, driver or launch error";
+    case MX_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    default: return "unknown status code";
+  }
+}
+
+MX_API int mx_available(void) {
+  DeviceInfo *d = nullptr;
+  const int rc = device_info(&d);
+  if (rc == MX_ERR_CUDA) cudaGetLastError();
+  return rc == MX_OK ? 1 : 0;
+}
+
+MX_API size_t mx_scale_bytes(int64_t rows, int64_t cols, int format, int scale_layout) {
+  if (rows <= 0 || cols <= 0 || !valid_format(format)) return 0;
+  const int blk = block_of(format);
+  if (cols % blk != 0) return 0;
+  const int64_t kb = cols / blk;
+  if (scale_layout == MX_SCALE_PLAIN) return static_cast<size_t>(rows * kb);
+  if (scale_layout == MX_SCALE_TCGEN05)
+    return static_cast<size_t>((rows + 127) / 128 * 128 * ((kb + 3) / 4 * 4));
+  return 0;
+}
+
+MX_API size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, int format) {
+  (void)rows;
+  (void)cols;
+  return format == MX_FMT_NVFP4 ? static_cast<size_t>(mx::kAmaxPartials) * sizeof(uint32_t) : 0;
+}
+
+MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
+                            int scale_layout, void *codes, void *scales, float *tensor_scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  if (!x || !codes || !scales) return MX_ERR_INVALID_ARG;
+  if (!valid_format(format)) return MX_ERR_INVALID_ARG;
+  if (scale_layout != MX_SCALE_PLAIN && scale_layout != MX_SCALE_TCGEN05) return MX_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld_x < cols) return MX_ERR_INVALID_ARG;
+  if (format == MX_FMT_MXFP4 && tensor_scale != nullptr) return MX_ERR_INVALID_ARG;
+  if (format == MX_FMT_NVFP4 && tensor_scale == nullptr) return MX_ERR_INVALID_ARG;
+  if (cols % block_of(format) != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || (ld_x % 8) != 0 || !aligned16(codes) || !aligned16(scales))
+    return MX_ERR_ALIGNMENT;
+  if (format == MX_FMT_NVFP4) {
+    if ((reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0) return MX_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < mx_quantize_workspace_bytes(rows, cols, format))
+      return MX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+  }
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  mx::QuantizeArgs a{};
+  a.x = x;
+  a.rows = rows;
+  a.cols = cols;
+  a.ld = ld_x;
+  a.tiled = scale_layout == MX_SCALE_TCGEN05;
+  a.codes = codes;
+  a.scales = scales;
+  a.tensor_scale = tensor_scale;
+  a.partials = static_cast<uint32_t *>(workspace);
+  a.num_sms = dev->num_sms;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return launch_rc(format == MX_FMT_MXFP4 ? mx::launch_mx_quantize(a, s)
+                                          : mx::launch_nvfp4_quantize(a, s));
+}
+
+MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format,
+                             void *tiled, void *stream) {
+  if (!plain || !tiled || !valid_format(format)) return MX_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0) return MX_ERR_INVALID_ARG;
+  if (cols % block_of(format) != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED_SHAPE;
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  return launch_rc(mx::launch_scale_relayout(plain, rows, cols / block_of(format), tiled,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+MX_API size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k) {
+  if (m <= 0 || n <= 0 || k <= 0 || k % 256 != 0 || split_k < 0) return 0;
+  int bn = 128, splits = 1;
+  mx::gemm_plan(m, n, k, split_k, num_sms_or_default(), &bn, &splits);
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(splits) * static_cast<size_t>(m) * static_cast<size_t>(n) *
+         sizeof(float);
+}
+
+MX_API int mxfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
+                      const void *b_scales, void *d, int64_t m, int64_t n, int64_t k, int layout,
+                      int out_dtype, int split_k, void *workspace, size_t workspace_bytes,
+                      void *stream) {
+  return gemm_common(MX_FMT_MXFP4, a_codes, a_scales, b_codes, b_scales, nullptr, nullptr, d, m, n,
+                     k, layout, out_dtype, split_k, workspace, workspace_bytes, stream);
+}
+
+MX_API int nvfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
+                      const void *b_scales, const float *a_tensor_scale,
+                      const float *b_tensor_scale, void *d, int64_t m, int64_t n, int64_t k,
+                      int layout, int out_dtype, int split_k, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+  return gemm_common(MX_FMT_NVFP4, a_codes, a_scales, b_codes, b_scales, a_tensor_scale,
+                     b_tensor_scale, d, m, n, k, layout, out_dtype, split_k, workspace,
+                     workspace_bytes, stream);
+}
+
+MX_API int mx_device_status(void *stream) {
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MX_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MX_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return MX_ERR_CUDA;
+  }
+  return (word & mx::kStatusTimeoutBit) ? MX_ERR_DEVICE_TIMEOUT : MX_OK;
+}
+
+MX_API int mx_selftest_wait_timeout(uint64_t timeout_ns, void *stream) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MX_ERR_INVALID_ARG;
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  return launch_rc(mx::launch_wait_selftest(dev->status, timeout_ns,
+                                            static_cast<cudaStream_t>(stream)));
+}

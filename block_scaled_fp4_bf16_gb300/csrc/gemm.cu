@@ -1,0 +1,448 @@
+// Block-scaled FP4 GEMM for sm_103a: D[M, N] = sum_k A[m, k] B[n, k] with
+// A, B packed E2M1 codes (TN, K-contiguous) and per-block scales.
+//   MXFP4: tcgen05.mma kind::mxf4, UE8M0 scale per 32 elements
+//          ("Integrate MXFP4 hipblaslt GEMM support", ROCm/TransformerEngine
+//          #697: FP4 x FP4 + UE8M0 block-32, K % 256, M/N % 32, BF16/FP32
+//          out, beta == 0, no bias/GELU).
+//   NVFP4: tcgen05.mma kind::mxf4nvf4, E4M3 scale per 16 elements, result
+//          times s_tA * s_tB (NVIDIA/TransformerEngine #3809).
+// Split-K with a separate fixed-order reduction follows the linear split
+// count of "Initial integration of a4w4 GEMM" (ROCm/TransformerEngine #663).
+//
+// Structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A tile (128 x 256 codes), B tile (BN x 256),
+//               and the scale atoms of the stage, into an S-stage ring of
+//               shared memory, completion tracked by mbarriers.
+//   warp 1      allocates tensor memory; one lane issues, per stage,
+//               tcgen05.cp of the scale atoms into tensor memory and four
+//               K=64 block-scaled MMAs into the tile's accumulator, then
+//               commits the stage back to the producer.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (lane = row),
+//               conversion to BF16 / FP32 (times alpha for NVFP4), stores.
+// With BN = 128 there are two accumulators in tensor memory so the
+// epilogue of one tile overlaps the main loop of the next.
+// Every wait is bounded; a wait that runs out records a status bit, makes
+// the other roles stop, drains what is in flight and frees tensor memory.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "mx_device.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kStageK = 256;         // FP4 elements of K per stage
+constexpr int kStageKBytes = 128;    // = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr int kEpilogueWarps = 4;
+
+template <int FMT, int BN>
+struct Cfg {
+  static constexpr int kAtomsK = FMT == 0 ? 2 : 4;   // 4-scale atoms per stage along K
+  static constexpr int kRowAtomsB = BN / 128;
+  static constexpr int kNumAcc = BN == 128 ? 2 : 1;
+  static constexpr int kStages = BN == 128 ? 6 : 4;
+  static constexpr int kABytes = kBM * kStageKBytes;
+  static constexpr int kBBytes = BN * kStageKBytes;
+  static constexpr int kSfaBytes = kAtomsK * 512;
+  static constexpr int kSfbBytes = kRowAtomsB * kAtomsK * 512;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kAccCol = 0;
+  static constexpr int kSfaCol = kNumAcc * BN;
+  static constexpr int kSfaCols = kAtomsK * 4;
+  static constexpr int kSfbCol = kSfaCol + kSfaCols;
+  static constexpr int kSfbCols = kAtomsK * (BN / 32);
+  static constexpr int kTmemCols = 512;
+  static_assert(kSfbCol + kSfbCols <= kTmemCols, "tensor memory budget");
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+  // barriers: full[S], empty[S], tfull[A], tempty[A]; then tmem slot, abort
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNumAcc) + 16;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+};
+
+struct Params {
+  const uint8_t *sfa;
+  const uint8_t *sfb;
+  void *d;
+  float *partial;        // split-K workspace [splits, M, N] or null
+  const float *a_ts;     // NVFP4 tensor scales or null
+  const float *b_ts;
+  uint32_t *status;
+  int m, n;
+  int m_tiles, n_tiles, splits;
+  int k_stages, stages_per_split;
+  int sfa_katoms, sfb_katoms;  // scale atoms along K per 128-row tile
+  int n_row_atoms;             // ceil(N / 128)
+  int out_fp32;
+  int num_units;
+};
+
+// Unit -> (m tile, n tile, split); tiles are walked in groups of 8 M tiles
+// so that concurrently running CTAs share A and B panels in L2.
+__device__ __forceinline__ void decode_unit(const Params &p, int u, int &mt, int &nt, int &sp) {
+  const int tiles = p.m_tiles * p.n_tiles;
+  sp = u / tiles;
+  const int t = u - sp * tiles;
+  constexpr int kGroup = 8;
+  const int per_group = kGroup * p.n_tiles;
+  const int g = t / per_group;
+  const int first_m = g * kGroup;
+  const int gsize = min(kGroup, p.m_tiles - first_m);
+  const int r = t - g * per_group;
+  mt = first_m + r % gsize;
+  nt = r / gsize;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+template <int FMT, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+  using C = Cfg<FMT, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::kStages;
+  uint64_t *tfull = bars + 2 * C::kStages;
+  uint64_t *tempty = tfull + C::kNumAcc;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + C::kNumAcc);
+  volatile uint32_t *abort = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < C::kNumAcc; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), kEpilogueWarps);
+    }
+    *abort = 0u;
+    fence_barrier_init();
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_b);
+  }
+  // B scale atoms past the end of N are never loaded: make them 0 (2^-127
+  // or 0.0, both finite) once, for every stage.
+  for (int s = 0; s < C::kStages; ++s) {
+    uint32_t *sfb = reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + C::kABytes +
+                                                 C::kBBytes + C::kSfaBytes);
+    for (int i = threadIdx.x; i < C::kSfbBytes / 4; i += kThreads) sfb[i] = 0u;
+  }
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      int mt, nt, sp;
+      decode_unit(p, u, mt, nt, sp);
+      const int k0 = sp * p.stages_per_split;
+      const int k1 = min(k0 + p.stages_per_split, p.k_stages);
+      const int rb0 = nt * C::kRowAtomsB;
+      const int rb_valid = min(C::kRowAtomsB, p.n_row_atoms - rb0);
+      const uint32_t bytes = C::kABytes + C::kBBytes + C::kSfaBytes + rb_valid * C::kAtomsK * 512;
+      for (int ks = k0; ks < k1; ++ks, ++it) {
+        const uint32_t s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1u;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t *st = smem + s * C::kStageBytes;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, bytes);
+        tma_load_2d(smem_u32(st), &tmap_a, ks * kStageKBytes, mt * kBM, fb);
+        tma_load_2d(smem_u32(st + C::kABytes), &tmap_b, ks * kStageKBytes, nt * BN, fb);
+        bulk_load(smem_u32(st + C::kABytes + C::kBBytes),
+                  p.sfa + (static_cast<size_t>(mt) * p.sfa_katoms + ks * C::kAtomsK) * 512,
+                  C::kSfaBytes, fb);
+        for (int ra = 0; ra < rb_valid; ++ra)
+          bulk_load(smem_u32(st + C::kABytes + C::kBBytes + C::kSfaBytes + ra * C::kAtomsK * 512),
+                    p.sfb + (static_cast<size_t>(rb0 + ra) * p.sfb_katoms + ks * C::kAtomsK) * 512,
+                    C::kAtomsK * 512, fb);
+      }
+    }
+    if (!ok) {
+      // Wait (bounded) for the copies still in flight before leaving.
+      const uint32_t first = it > static_cast<uint32_t>(C::kStages) ? it - C::kStages : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_drain(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t it = 0, tile = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tile) {
+      int mt, nt, sp;
+      decode_unit(p, u, mt, nt, sp);
+      const int k0 = sp * p.stages_per_split;
+      const int k1 = min(k0 + p.stages_per_split, p.k_stages);
+      const uint32_t acc = tile % C::kNumAcc;
+      const uint32_t aph = (tile / C::kNumAcc) & 1u;
+      if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + C::kAccCol + acc * BN;
+      for (int ks = k0; ks < k1; ++ks, ++it) {
+        const uint32_t s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1u;
+        if (!mbar_wait(smem_u32(&full[s]), ph, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+        const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
+        const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+#pragma unroll
+        for (int a = 0; a < C::kAtomsK; ++a)
+          tc_cp_32x128b_warpx4(tmem + C::kSfaCol + a * 4, smem_desc_scale_block(sfa_s + a * 512));
+#pragma unroll
+        for (int ra = 0; ra < C::kRowAtomsB; ++ra)
+#pragma unroll
+          for (int a = 0; a < C::kAtomsK; ++a)
+            tc_cp_32x128b_warpx4(tmem + C::kSfbCol + a * (BN / 32) + ra * 4,
+                                 smem_desc_scale_block(sfb_s + (ra * C::kAtomsK + a) * 512));
+        const uint64_t a_desc = smem_desc_sw128_kmajor(st);
+        const uint64_t b_desc = smem_desc_sw128_kmajor(st + C::kABytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // K = 64 per MMA = 32 bytes along the swizzled row (>> 4 = 2).
+          const int ka = FMT == 0 ? (kk >> 1) : kk;
+          const uint32_t sf_id = FMT == 0 ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
+          tc_mma_block_scaled<FMT>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk,
+                                   mma_idesc<FMT>(kBM, BN, sf_id), tmem + C::kSfaCol + ka * 4,
+                                   tmem + C::kSfbCol + ka * (BN / 32),
+                                   (ks > k0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&empty[s]));
+      }
+      if (!ok) break;
+      tc_commit(smem_u32(&tfull[acc]));
+    }
+    if (!ok) {
+      // Let the MMAs already issued finish before tensor memory is freed.
+      tc_commit(smem_u32(&tfull[0]));
+      mbar_drain(smem_u32(&tfull[0]), 0u);
+      mbar_drain(smem_u32(&tfull[0]), 1u);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // this warp may access tensor-memory lanes 32q..32q+31
+    const int row_in_tile = q * 32 + lane;
+    float alpha = 1.0f;
+    if (FMT == 1) alpha = __fmul_rn(*p.a_ts, *p.b_ts);
+    uint32_t tile = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tile) {
+      int mt, nt, sp;
+      decode_unit(p, u, mt, nt, sp);
+      const uint32_t acc = tile % C::kNumAcc;
+      const uint32_t aph = (tile / C::kNumAcc) & 1u;
+      // The warp leaves together (tcgen05.ld is warp-collective).
+      const bool ready = mbar_wait(smem_u32(&tfull[acc]), aph, abort, p.status);
+      if (!__all_sync(0xFFFFFFFFu, ready)) break;
+      tc_fence_after();
+      const int row = mt * kBM + row_in_tile;
+      const bool row_ok = row < p.m;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kAccCol + acc * BN + c * 32,
+                         r);
+        tc_wait_ld();
+        const int col = nt * BN + c * 32;
+        if (!row_ok || col >= p.n) continue;
+        if (p.partial != nullptr) {
+          float4 *dst = reinterpret_cast<float4 *>(
+              p.partial + (static_cast<size_t>(sp) * p.m + row) * p.n + col);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        } else if (p.out_fp32) {
+          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) +
+                                                   static_cast<size_t>(row) * p.n + col);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.d) +
+                                                 static_cast<size_t>(row) * p.n + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(__uint_as_float(r[8 * i + j]), alpha);
+            dst[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Split-K reduction: out[m, n] = alpha * sum_{s = 0..S-1} ws[s, m, n], summed
+// in split order (deterministic), then rounded once to BF16 or FP32.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws,
+                                                            int splits, int64_t mn, void *out,
+                                                            int out_fp32, const float *a_ts,
+                                                            const float *b_ts) {
+  float alpha = 1.0f;
+  if (a_ts != nullptr) alpha = __fmul_rn(*a_ts, *b_ts);
+  const int64_t n4 = mn >> 2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4 *>(ws)[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(s) * mn)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    acc.x = __fmul_rn(acc.x, alpha);
+    acc.y = __fmul_rn(acc.y, alpha);
+    acc.z = __fmul_rn(acc.z, alpha);
+    acc.w = __fmul_rn(acc.w, alpha);
+    if (out_fp32) {
+      reinterpret_cast<float4 *>(out)[i] = acc;
+    } else {
+      reinterpret_cast<uint2 *>(out)[i] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+  }
+}
+
+// One CTA waits on a barrier that nothing completes: exercises the bounded
+// wait and the status report without faulting or hanging the device.
+__global__ void wait_selftest_kernel(uint32_t *status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0u, &abort_flag, status, timeout_ns);
+}
+
+template <int FMT, int BN>
+cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
+  using C = Cfg<FMT, BN>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  Params p{};
+  p.sfa = static_cast<const uint8_t *>(g.a_scales);
+  p.sfb = static_cast<const uint8_t *>(g.b_scales);
+  p.d = g.d;
+  p.partial = g.split_k > 1 ? g.workspace : nullptr;
+  p.a_ts = g.a_ts;
+  p.b_ts = g.b_ts;
+  p.status = g.status;
+  p.m = static_cast<int>(g.m);
+  p.n = static_cast<int>(g.n);
+  p.m_tiles = static_cast<int>((g.m + kBM - 1) / kBM);
+  p.n_tiles = static_cast<int>((g.n + BN - 1) / BN);
+  p.k_stages = static_cast<int>(g.k / kStageK);
+  p.splits = g.split_k;
+  p.stages_per_split = (p.k_stages + g.split_k - 1) / g.split_k;
+  p.sfa_katoms = static_cast<int>(g.k / (FMT == 0 ? 128 : 64));
+  p.sfb_katoms = p.sfa_katoms;
+  p.n_row_atoms = static_cast<int>((g.n + 127) / 128);
+  p.out_fp32 = g.out_fp32;
+  p.num_units = p.m_tiles * p.n_tiles * p.splits;
+  const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
+  gemm_kernel<FMT, BN><<<grid, kThreads, C::kSmemBytes, s>>>(*g.tmap_a, *g.tmap_b, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || g.split_k <= 1) return e;
+  const int64_t mn = g.m * g.n;
+  int64_t rgrid = (mn / 4 + 255) / 256;
+  if (rgrid > 4 * g.num_sms) rgrid = 4 * g.num_sms;
+  splitk_reduce_kernel<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(
+      g.workspace, g.split_k, mn, g.d, g.out_fp32, FMT == 1 ? g.a_ts : nullptr,
+      FMT == 1 ? g.b_ts : nullptr);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits) {
+  const int64_t m_tiles = (m + kBM - 1) / kBM;
+  const int64_t tiles256 = m_tiles * ((n + 255) / 256);
+  *bn = (tiles256 >= 2 * num_sms) ? 256 : 128;
+  const int64_t tiles = m_tiles * ((n + *bn - 1) / *bn);
+  const int64_t k_stages = k / kStageK;
+  int s = split_k;
+  if (s <= 0) {
+    // Automatic: split K only when the tiles cannot fill the GPU, keeping at
+    // least 4 stages of K per split.
+    s = 1;
+    while (tiles * (s * 2) <= num_sms && k_stages / (s * 2) >= 4) s *= 2;
+  }
+  if (s > k_stages) s = static_cast<int>(k_stages);
+  if (s < 1) s = 1;
+  // Every split must own at least one stage: shrink s until it does.
+  while (s > 1 && (k_stages + s - 1) / s * (s - 1) >= k_stages) --s;
+  *splits = s;
+}
+
+cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t s) {
+  if (g.fmt == 0) {
+    return g.bn == 256 ? launch_typed<0, 256>(g, s) : launch_typed<0, 128>(g, s);
+  }
+  return g.bn == 256 ? launch_typed<1, 256>(g, s) : launch_typed<1, 128>(g, s);
+}
+
+cudaError_t launch_wait_selftest(uint32_t *status, uint64_t timeout_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace mx

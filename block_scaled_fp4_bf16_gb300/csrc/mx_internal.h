@@ -1,0 +1,58 @@
+// Host-side declarations shared by the library's translation units (not part
+// of the public ABI; the public ABI is include/mxfp4.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mx {
+
+// Number of partial maxima the NVFP4 amax pass writes (one per CTA).
+constexpr int kAmaxPartials = 512;
+
+// Bit of the device status word set when a bounded device wait runs out.
+constexpr uint32_t kStatusTimeoutBit = 1u;
+
+struct QuantizeArgs {
+  const void *x;
+  int64_t rows, cols, ld;
+  int tiled;            // scales in the tcgen05 tile order
+  void *codes;
+  void *scales;
+  float *tensor_scale;  // NVFP4 only
+  uint32_t *partials;   // NVFP4 only: kAmaxPartials words
+  int num_sms;
+};
+
+cudaError_t launch_mx_quantize(const QuantizeArgs &a, cudaStream_t s);
+cudaError_t launch_nvfp4_quantize(const QuantizeArgs &a, cudaStream_t s);
+cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
+                                  cudaStream_t s);
+
+struct GemmArgs {
+  int fmt;  // 0 MXFP4, 1 NVFP4
+  const CUtensorMap *tmap_a;  // codes A [M, K/2] bytes, box 128 rows
+  const CUtensorMap *tmap_b;  // codes B [N, K/2] bytes, box `bn` rows
+  const void *a_scales, *b_scales;
+  const float *a_ts, *b_ts;  // NVFP4 tensor scales (device)
+  void *d;
+  int out_fp32;
+  int64_t m, n, k;
+  int split_k;   // >= 1, already resolved
+  int bn;        // 128 or 256
+  float *workspace;
+  uint32_t *status;
+  int num_sms;
+};
+
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s);
+
+// Tile width and split count the GEMM uses for a shape (split_k 0 = auto).
+void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits);
+
+cudaError_t launch_wait_selftest(uint32_t *status, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace mx

@@ -1,0 +1,174 @@
+/*
+ * mxfp4.h: C ABI of the GB300 (sm_103a) block-scaled FP4 library.
+ *
+ * The library computes D = (A * sA)(B * sB)^T, where A [M, K] and B [N, K]
+ * hold FP4 E2M1 codes, two per byte, and sA, sB are block scales along K:
+ *   MXFP4: one UE8M0 scale (2^(e-127)) per 32 elements.
+ *   NVFP4: one E4M3 scale per 16 elements plus one FP32 scale per tensor.
+ * The pages this follows:
+ *   - "Integrate MXFP4 hipblaslt GEMM support" (ROCm/TransformerEngine #697),
+ *     Description / Changes: FP4 x FP4 with UE8M0 block-32 scales; TN; BF16
+ *     or FP32 output; K % 256 == 0, M % 32 == 0, N % 32 == 0; beta == 0; no
+ *     bias, no GELU.
+ *   - "Initial integration of a4w4 GEMM" (ROCm/TransformerEngine #663),
+ *     review comments: a torch-free C API returning an int status, with a
+ *     distinct code for "backend not compiled in" and an availability probe;
+ *     the bias argument is a hazard and is left out; the split-K argument is
+ *     a linear count.
+ *   - "feat(ck-tile): aquant GEMM TE to dispatcher bridge"
+ *     (ROCm/rocm-libraries #9980): packed 4-bit byte counts are packed counts;
+ *     only packed (contiguous) strides are accepted and a non-packed one is
+ *     rejected, never silently transposed; the architecture is checked at run
+ *     time and never defaulted.
+ *   - NVIDIA/TransformerEngine #3809 (NVFP4 quantize kernels): BF16 -> NVFP4
+ *     with E4M3 per-16 scales and an FP32 per-tensor amax; one kernel per
+ *     call where possible; round-to-nearest output byte-identical across
+ *     implementations.
+ *
+ * Conventions of every entry point:
+ *   - Return 0 (MX_OK) or a negative MX_ERR_* code.  On an argument error
+ *     nothing is launched and nothing is written.
+ *   - Every data pointer is a device pointer owned by the caller; the
+ *     library never allocates device memory and never synchronises the
+ *     stream (except mx_device_status, which says so).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) of the current device.
+ *   - Data pointers must be 16-byte aligned (TMA and 16-byte vector access).
+ *   - Sizes are element counts unless named *_bytes; FP4 code buffers hold
+ *     rows * cols / 2 bytes, element 2t in the low nibble of byte t.
+ *   - Stateless and thread-safe; the device architecture (sm_103) is checked
+ *     once per device and cached.
+ */
+#ifndef MXFP4_GB300_H
+#define MXFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define MX_OK 0
+#define MX_ERR_INVALID_ARG (-1)         /* null pointer, bad enum, ld < cols      */
+#define MX_ERR_NOT_COMPILED (-2)        /* library built without sm_103a code     */
+#define MX_ERR_UNSUPPORTED_ARCH (-3)    /* current device is not sm_103           */
+#define MX_ERR_UNSUPPORTED_SHAPE (-4)   /* K % 256, M % 32, N % 32, cols % block  */
+#define MX_ERR_UNSUPPORTED_FEATURE (-5) /* layout other than TN, bad out dtype    */
+#define MX_ERR_ALIGNMENT (-6)           /* pointer or leading dim not 16-B aligned */
+#define MX_ERR_WORKSPACE (-7)           /* workspace missing or too small         */
+#define MX_ERR_CUDA (-8)                /* CUDA runtime / driver / launch error   */
+#define MX_ERR_DEVICE_TIMEOUT (-9)      /* a bounded device-side wait ran out     */
+
+/* ---- enums ----------------------------------------------------------- */
+#define MX_FMT_MXFP4 0    /* UE8M0 scale per 32 elements                      */
+#define MX_FMT_NVFP4 1    /* E4M3 scale per 16 elements + FP32 tensor scale   */
+
+#define MX_SCALE_PLAIN 0   /* scales [rows, cols / block] row-major           */
+#define MX_SCALE_TCGEN05 1 /* 128x4 tiled order read by the GEMM (see below)  */
+
+#define MX_LAYOUT_TN 0     /* A [M, K] and B [N, K], both K-contiguous        */
+
+#define MX_OUT_BF16 0
+#define MX_OUT_FP32 1
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mx_error_string(int code);
+
+/* 1 when the library holds sm_103a kernels and the current device is an
+ * sm_103 GPU, 0 otherwise.  Never fails. */
+int mx_available(void);
+
+/* Bytes of a scale buffer for a [rows, cols] operand.
+ *   MX_SCALE_PLAIN:   rows * (cols / block)
+ *   MX_SCALE_TCGEN05: ceil(rows / 128) * 128 * ceil((cols / block) / 4) * 4
+ * block = 32 (MXFP4) or 16 (NVFP4).  Returns 0 for invalid arguments.
+ *
+ * The TCGEN05 order is the scale-factor order of the sm_100-family block-
+ * scaled tensor-core MMA: 512-byte atoms of 128 rows x 4 scale columns,
+ * atoms ordered by (row tile, column tile) with the column tile fastest;
+ * inside an atom the byte of (row r, scale column c) is at
+ * (r % 32) * 16 + (r / 32 % 4) * 4 + c % 4.  Padding bytes are 0. */
+size_t mx_scale_bytes(int64_t rows, int64_t cols, int format, int scale_layout);
+
+/* Workspace bytes that mx_quantize_bf16 needs (0 for MXFP4; a small buffer
+ * of partial maxima for NVFP4). */
+size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, int format);
+
+/* BF16 -> FP4 quantize pre-pass.
+ *   x:      BF16 [rows, cols], row stride ld_x elements (ld_x >= cols,
+ *           ld_x % 8 == 0); cols % 32 == 0 (MXFP4) or % 16 (NVFP4).
+ *   codes:  out, rows * cols / 2 bytes, row stride cols / 2.
+ *   scales: out, mx_scale_bytes(rows, cols, format, scale_layout) bytes.
+ *   tensor_scale: NVFP4 only, out, one float s_t = amax / (6 * 448)
+ *           (device pointer); must be NULL for MXFP4.
+ *   workspace: mx_quantize_workspace_bytes(...) bytes (NULL if 0).
+ * MXFP4, per row and per 32-element block: e = clamp(floor(log2 amax) - 2,
+ *   -127, 127) (e = -127 for an all-zero block), scale byte e + 127,
+ *   code = E2M1 round-to-nearest-even of x * 2^-e, saturating at +-6, sign
+ *   kept ("Integrate MXFP4 hipblaslt GEMM support", Description: UE8M0
+ *   block-32; the OCP MX shared-exponent rule).
+ * NVFP4: s_t = amax_t / 2688; per 16-element block sb = E4M3(amax_b /
+ *   (6 * s_t)) (RNE, satfinite); code = E2M1(x / (E4M3(sb) * s_t)); each
+ *   step one FP32 round-to-nearest operation; codes 0 where sb == 0 or
+ *   s_t == 0 (NVIDIA/TransformerEngine #3809, NVFP4 quantize).
+ * Launches one kernel (MXFP4) or two (NVFP4: amax, then quantize). */
+int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
+                     int scale_layout, void *codes, void *scales, float *tensor_scale,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Plain scales [rows, cols / block] -> MX_SCALE_TCGEN05 order (see
+ * mx_scale_bytes).  `tiled` receives mx_scale_bytes(rows, cols, format,
+ * MX_SCALE_TCGEN05) bytes, padding included ("Integrate MXFP4 hipblaslt GEMM
+ * support": plain vs swizzled scale layouts). */
+int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format, void *tiled,
+                      void *stream);
+
+/* Workspace bytes that mxfp4_gemm / nvfp4_gemm need for this shape and
+ * split count (split_k = 0 means the automatic choice): split_k * m * n * 4
+ * when more than one split is used, else 0. */
+size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k);
+
+/* MXFP4 GEMM, D[M, N] = sum_k A[m, k] * B[n, k] ("Integrate MXFP4 hipblaslt
+ * GEMM support", Description / Changes).
+ *   a_codes [M, K/2], b_codes [N, K/2] (K-contiguous, TN);
+ *   a_scales, b_scales: UE8M0 in MX_SCALE_TCGEN05 order
+ *     (mx_scale_bytes(M, K, MX_FMT_MXFP4, MX_SCALE_TCGEN05) bytes, etc.);
+ *   d: out [M, N] row-major, BF16 (out_dtype MX_OUT_BF16) or FP32; D is
+ *     overwritten (beta == 0), nothing in it is read;
+ *   layout: MX_LAYOUT_TN only;
+ *   split_k: 0 = automatic, else the linear number of K splits (each split
+ *     a multiple of 256 along K); more than one split writes FP32 partials
+ *     to `workspace` and a reduction kernel sums them in split order;
+ *   K % 256 == 0, M % 32 == 0, N % 32 == 0, M, N, K > 0. */
+int mxfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
+               const void *b_scales, void *d, int64_t m, int64_t n, int64_t k, int layout,
+               int out_dtype, int split_k, void *workspace, size_t workspace_bytes,
+               void *stream);
+
+/* NVFP4 GEMM: as mxfp4_gemm with E4M3 per-16 scales (MX_SCALE_TCGEN05 order
+ * for MX_FMT_NVFP4) and the product multiplied by s_tA * s_tB, read from the
+ * device floats a_tensor_scale and b_tensor_scale (NVIDIA/TransformerEngine
+ * #3809: E4M3 block scales plus an FP32 per-tensor scale). */
+int nvfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
+               const void *b_scales, const float *a_tensor_scale, const float *b_tensor_scale,
+               void *d, int64_t m, int64_t n, int64_t k, int layout, int out_dtype, int split_k,
+               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns MX_OK, MX_ERR_DEVICE_TIMEOUT when a kernel's
+ * bounded wait (on a TMA or tensor-core completion barrier) ran out and the
+ * kernel abandoned its work, or MX_ERR_CUDA. */
+int mx_device_status(void *stream);
+
+/* Self-test of the bounded device wait: launches one CTA that waits on a
+ * barrier nothing will complete, for at most timeout_ns nanoseconds, records
+ * MX_ERR_DEVICE_TIMEOUT in the status word and returns.  Asynchronous; read
+ * the result with mx_device_status.  timeout_ns must be in (0, 1e10]. */
+int mx_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXFP4_GB300_H */

@@ -78,6 +78,8 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.oracle_round_bf16.restype = ctypes.c_uint16
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16_array.restype = None
+        lib.oracle_round_bf16_array.argtypes = [c_f64p, c_i64, c_u16p]
         lib.oracle_mx_quantize.restype = None
         lib.oracle_mx_quantize.argtypes = [c_u16p, c_i64, c_i64, c_i64, c_u8p, c_u8p]
         lib.oracle_bf16_amax.restype = ctypes.c_float
@@ -131,12 +133,10 @@ def e4m3_encode(v: float) -> int:
 
 def round_bf16(d: np.ndarray) -> np.ndarray:
     """Round binary64 values to BF16 (ties to even), returned as uint16 bits."""
-    lib = _load()
     flat = np.ascontiguousarray(d, dtype=np.float64).ravel()
     out = np.empty(flat.shape, dtype=np.uint16)
-    f = lib.oracle_round_bf16
-    for i, v in enumerate(flat.tolist()):
-        out[i] = f(v)
+    _load().oracle_round_bf16_array(_ptr(flat, ctypes.c_double), flat.size,
+                                    _ptr(out, ctypes.c_uint16))
     return out.reshape(np.shape(d))
 
 

@@ -162,6 +162,14 @@ uint16_t oracle_round_bf16(double x)
     return sign | (uint16_t)((u >> 16) & 0x7FFFu);
 }
 
+/* oracle_round_bf16 over an array. */
+void oracle_round_bf16_array(const double *x, int64_t n, uint16_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_round_bf16(x[i]);
+}
+
 /* ------------------------------------------------------------------ */
 /* Quantizers                                                          */
 /* ------------------------------------------------------------------ */

@@ -1,0 +1,146 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+(via the ctypes binding) on host inputs, and compare with the CPU oracle under
+the tolerances of the block-scaled GEMM:
+
+* quantize: codes, scales (and the NVFP4 tensor scale) byte-equal;
+* FP32 out: |D - D_ref| <= 1e-5 * sum_k |a||b|;
+* BF16 out: within 1 BF16 ulp of the correctly rounded D_ref, or (near
+  cancellation, where the FP32 accumulation error exceeds a BF16 ulp of D)
+  within the FP32 bound above; the count of the latter is reported.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import block_scaled_fp4_bf16_gb300 as mx
+import oracle
+
+FP32_REL_TOL = 1e-5
+
+
+def dev_u8(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def gpu_quantize(x_bits: np.ndarray, fmt: int, layout: int, ld: int | None = None):
+    """Quantize BF16 bits [rows, cols] on the GPU; returns host (codes, scales, s_t)."""
+    rows, cols = x_bits.shape
+    if ld is None or ld == cols:
+        x = dev_bf16(x_bits)
+        ld = cols
+    else:
+        padded = np.zeros((rows, ld), np.uint16)
+        padded[:, :cols] = x_bits
+        x = dev_bf16(padded)
+    codes = torch.empty(rows * cols // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(mx.mx_scale_bytes(rows, cols, fmt, layout), dtype=torch.uint8,
+                         device="cuda")
+    ts = ws = None
+    if fmt == mx.MX_FMT_NVFP4:
+        ts = torch.empty(1, dtype=torch.float32, device="cuda")
+        ws = torch.empty(mx.mx_quantize_workspace_bytes(rows, cols, fmt), dtype=torch.uint8,
+                         device="cuda")
+    mx.mx_quantize_bf16(x, rows, cols, ld, fmt, layout, codes, scales, ts, ws)
+    torch.cuda.synchronize()
+    s_t = None if ts is None else np.float32(ts.item())
+    return codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(), s_t
+
+
+def gpu_relayout(plain: np.ndarray, rows: int, cols: int, fmt: int) -> torch.Tensor:
+    tiled = torch.full((mx.mx_scale_bytes(rows, cols, fmt, mx.MX_SCALE_TCGEN05),), 0xAB,
+                       dtype=torch.uint8, device="cuda")
+    mx.mx_scale_relayout(dev_u8(plain), rows, cols, fmt, tiled)
+    return tiled
+
+
+def gpu_gemm(fmt, a_codes, a_scales_tiled, b_codes, b_scales_tiled, m, n, k, out_fp32,
+             split_k=0, a_ts=None, b_ts=None, prefill_nan=True):
+    """Run the GEMM; operands may be host arrays or device tensors.  Returns host D
+    (float32 array, or uint16 BF16 bits)."""
+    def on_dev(a):
+        return a if isinstance(a, torch.Tensor) else dev_u8(a)
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    d = torch.empty((m, n), dtype=dt, device="cuda")
+    if prefill_nan:
+        d.fill_(float("nan"))
+    wsb = mx.mx_gemm_workspace_bytes(m, n, k, split_k)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
+    od = mx.MX_OUT_FP32 if out_fp32 else mx.MX_OUT_BF16
+    if fmt == mx.MX_FMT_MXFP4:
+        mx.mxfp4_gemm(on_dev(a_codes), on_dev(a_scales_tiled), on_dev(b_codes),
+                      on_dev(b_scales_tiled), d, m, n, k, mx.MX_LAYOUT_TN, od, split_k, ws)
+    else:
+        ta = a_ts if isinstance(a_ts, torch.Tensor) else torch.tensor([a_ts], dtype=torch.float32,
+                                                                      device="cuda")
+        tb = b_ts if isinstance(b_ts, torch.Tensor) else torch.tensor([b_ts], dtype=torch.float32,
+                                                                      device="cuda")
+        mx.nvfp4_gemm(on_dev(a_codes), on_dev(a_scales_tiled), on_dev(b_codes),
+                      on_dev(b_scales_tiled), ta, tb, d, m, n, k, mx.MX_LAYOUT_TN, od, split_k, ws)
+    torch.cuda.synchronize()
+    assert mx.mx_device_status() == mx.MX_OK
+    if out_fp32:
+        return d.cpu().numpy()
+    return d.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _bf16_ulp(bits: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 at each (finite) value: next-up minus value, in fp64."""
+    mag = np.asarray(bits, np.uint16) & np.uint16(0x7FFF)
+    v = bf16_bits_to_f64(mag)
+    nxt = bf16_bits_to_f64(mag + np.uint16(1))
+    return nxt - v
+
+
+def check_fp32(d: np.ndarray, d_ref: np.ndarray, s_abs: np.ndarray, what: str = ""):
+    d = np.asarray(d, np.float64)
+    assert np.all(np.isfinite(d)), f"{what}: non-finite outputs"
+    err = np.abs(d - d_ref)
+    bound = FP32_REL_TOL * s_abs
+    bad = err > bound
+    if bad.any():
+        i = np.argwhere(bad)[:5]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())}/{bad.size} FP32 outputs out of tolerance; first "
+            + ", ".join(f"{tuple(x)}: got {d[tuple(x)]!r} ref {d_ref[tuple(x)]!r} "
+                        f"s_abs {s_abs[tuple(x)]!r}" for x in i))
+    return float((err / np.maximum(s_abs, 1e-300)).max())
+
+
+def check_bf16(d_bits: np.ndarray, d_ref: np.ndarray, s_abs: np.ndarray, what: str = ""):
+    d_bits = np.asarray(d_bits, np.uint16)
+    d = bf16_bits_to_f64(d_bits)
+    assert np.all(np.isfinite(d)), f"{what}: non-finite outputs"
+    ref_bits = oracle.round_bf16(d_ref)
+    ref = bf16_bits_to_f64(ref_bits)
+    ulp = _bf16_ulp(ref_bits)
+    within_ulp = np.abs(d - ref) <= ulp
+    within_fp32 = np.abs(d - d_ref) <= FP32_REL_TOL * s_abs
+    ok = within_ulp | within_fp32
+    if not ok.all():
+        i = np.argwhere(~ok)[:5]
+        raise AssertionError(
+            f"{what}: {int((~ok).sum())}/{ok.size} BF16 outputs out of tolerance; first "
+            + ", ".join(f"{tuple(x)}: got {d[tuple(x)]!r} ref {d_ref[tuple(x)]!r}" for x in i))
+    return {"exact": int((d_bits == ref_bits).sum()), "within_1ulp": int(within_ulp.sum()),
+            "only_fp32_rule": int((~within_ulp & within_fp32).sum()), "total": int(ok.size)}
+
+
+def sample_indices(n: int, count: int, tile: int, seed: int) -> np.ndarray:
+    """Deterministic sample of indices covering the first and last tile and random interior."""
+    rng = np.random.default_rng(seed)
+    idx = set(range(min(n, 8))) | set(range(max(0, n - 8), n))
+    idx |= {min(n - 1, t) for t in (tile - 1, tile, 2 * tile - 1)}
+    if n > 0:
+        idx |= set(rng.integers(0, n, size=count).tolist())
+    return np.array(sorted(idx), dtype=np.int64)

@@ -1,0 +1,127 @@
+"""The C-ABI library loads and exports every entry point of include/mxfp4.h, and
+its host-side contract (sizes, error strings, argument validation) holds.  No
+call here reaches the GPU: validation rejects each call before any device
+work, and the library never dereferences the fake pointers used below."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_fp4_bf16_gb300 as mx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_fp4_bf16_gb300 import build
+    build.build()
+    return mx.lib()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mx\w+|mxfp4_\w+|nvfp4_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["mx_quantize_bf16", "mxfp4_gemm", "nvfp4_gemm", "mx_scale_relayout",
+                     "mx_device_status", "mx_error_string", "mx_available"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_error_strings(lib):
+    codes = [0, -1, -2, -3, -4, -5, -6, -7, -8, -9]
+    texts = [mx.mx_error_string(c) for c in codes]
+    assert len(set(texts)) == len(codes)
+    assert mx.mx_error_string(-100) == "unknown status code"
+
+
+def test_scale_bytes(lib):
+    assert mx.mx_scale_bytes(128, 256, mx.MX_FMT_MXFP4, mx.MX_SCALE_PLAIN) == 128 * 8
+    assert mx.mx_scale_bytes(128, 256, mx.MX_FMT_MXFP4, mx.MX_SCALE_TCGEN05) == 128 * 8
+    assert mx.mx_scale_bytes(32, 256, mx.MX_FMT_MXFP4, mx.MX_SCALE_TCGEN05) == 128 * 8
+    assert mx.mx_scale_bytes(200, 96, mx.MX_FMT_MXFP4, mx.MX_SCALE_TCGEN05) == 256 * 4
+    assert mx.mx_scale_bytes(16384, 8192, mx.MX_FMT_MXFP4, mx.MX_SCALE_TCGEN05) == 16384 * 256
+    assert mx.mx_scale_bytes(4096, 4096, mx.MX_FMT_NVFP4, mx.MX_SCALE_TCGEN05) == 4096 * 256
+    assert mx.mx_scale_bytes(4096, 4096, mx.MX_FMT_NVFP4, mx.MX_SCALE_PLAIN) == 4096 * 256
+    assert mx.mx_scale_bytes(4, 33, mx.MX_FMT_MXFP4, mx.MX_SCALE_PLAIN) == 0
+    assert mx.mx_scale_bytes(4, 32, 7, mx.MX_SCALE_PLAIN) == 0
+    assert mx.mx_scale_bytes(0, 32, mx.MX_FMT_MXFP4, mx.MX_SCALE_PLAIN) == 0
+
+
+def test_workspace_bytes(lib):
+    assert mx.mx_quantize_workspace_bytes(10, 32, mx.MX_FMT_MXFP4) == 0
+    assert mx.mx_quantize_workspace_bytes(10, 32, mx.MX_FMT_NVFP4) > 0
+    assert mx.mx_gemm_workspace_bytes(4096, 4096, 4096, 1) == 0
+    assert mx.mx_gemm_workspace_bytes(32, 8192, 8192, 4) == 4 * 32 * 8192 * 4
+    assert mx.mx_gemm_workspace_bytes(32, 8192, 8192, 0) % (32 * 8192 * 4) == 0
+    assert mx.mx_gemm_workspace_bytes(32, 8192, 100, 1) == 0  # K % 256 != 0
+
+
+FAKE = 1 << 40        # a 16-byte aligned address that is never dereferenced
+FAKE_ODD = FAKE + 8   # not 16-byte aligned
+
+
+def _gemm(lib, **kw):
+    a = dict(a=FAKE, sa=FAKE, b=FAKE, sb=FAKE, d=FAKE, m=128, n=128, k=256, layout=0, out=0,
+             split=1, ws=None, wsb=0)
+    a.update(kw)
+    return lib.mxfp4_gemm(a["a"], a["sa"], a["b"], a["sb"], a["d"], a["m"], a["n"], a["k"],
+                          a["layout"], a["out"], a["split"], a["ws"], a["wsb"], None)
+
+
+def test_gemm_argument_validation(lib):
+    assert _gemm(lib, a=None) == mx.MX_ERR_INVALID_ARG
+    assert _gemm(lib, d=None) == mx.MX_ERR_INVALID_ARG
+    assert _gemm(lib, split=-1) == mx.MX_ERR_INVALID_ARG
+    assert _gemm(lib, layout=1) == mx.MX_ERR_UNSUPPORTED_FEATURE
+    assert _gemm(lib, out=2) == mx.MX_ERR_UNSUPPORTED_FEATURE
+    assert _gemm(lib, k=128) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, m=48) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, n=40) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, m=0) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, a=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
+    assert _gemm(lib, d=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
+    # NVFP4 needs both tensor scales
+    assert lib.nvfp4_gemm(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 128, 128, 256, 0, 1, 1,
+                          None, 0, None) == mx.MX_ERR_INVALID_ARG
+
+
+def test_quantize_argument_validation(lib):
+    q = lib.mx_quantize_bf16
+    assert q(None, 4, 32, 32, 0, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert q(FAKE, 4, 32, 16, 0, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert q(FAKE, 4, 32, 32, 5, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert q(FAKE, 4, 32, 32, 0, 9, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert q(FAKE, 4, 48, 48, 0, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert q(FAKE, 4, 32, 36, 0, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_ALIGNMENT
+    assert q(FAKE_ODD, 4, 32, 32, 0, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_ALIGNMENT
+    # MXFP4 takes no tensor scale; NVFP4 needs one and a workspace
+    assert q(FAKE, 4, 32, 32, 0, 0, FAKE, FAKE, FAKE, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert q(FAKE, 4, 32, 32, 1, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    assert q(FAKE, 4, 32, 32, 1, 0, FAKE, FAKE, FAKE, None, 0, None) == mx.MX_ERR_WORKSPACE
+
+
+def test_relayout_and_selftest_validation(lib):
+    assert lib.mx_scale_relayout(None, 4, 32, 0, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_scale_relayout(FAKE, 4, 40, 0, FAKE, None) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert lib.mx_selftest_wait_timeout(0, None) == mx.MX_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host without a GPU only")
+def test_no_gpu_reports_unavailable(lib):
+    assert mx.mx_available() is False
+    # a well-formed call fails at the device check, not silently
+    rc = _gemm(lib)
+    assert rc in (mx.MX_ERR_CUDA, mx.MX_ERR_UNSUPPORTED_ARCH)

@@ -1,0 +1,205 @@
+"""GPU parity of the block-scaled GEMM (MXFP4 and NVFP4) against the CPU oracle,
+element by element at moderate sizes (several tiles, ragged tails) and on
+sampled outputs at the full workload sizes, plus closed-form probes of the
+scale and nibble conventions."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp4_bf16_gb300 as mx
+import oracle
+from block_scaled_fp4_bf16_gb300 import synth
+from tests.gpu_helpers import (bf16_bits_to_f64, check_bf16, check_fp32, dev_u8, gpu_gemm,
+                               gpu_quantize, gpu_relayout, sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+MX, NV = mx.MX_FMT_MXFP4, mx.MX_FMT_NVFP4
+TILED = mx.MX_SCALE_TCGEN05
+
+
+def _codes_case(m, n, k, seed, lo=120, hi=134):
+    return (synth.fp4_codes(m, k, seed), synth.scale_bytes(m, k // 32, lo, hi, seed + 1),
+            synth.fp4_codes(n, k, seed + 2), synth.scale_bytes(n, k // 32, lo, hi, seed + 3))
+
+
+def _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32, split_k=0):
+    d = gpu_gemm(MX, a, oracle.scale_tile(sa), b, oracle.scale_tile(sb), m, n, k, out_fp32,
+                 split_k=split_k)
+    ref, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
+    what = f"mxfp4 {m}x{n}x{k} {'fp32' if out_fp32 else 'bf16'} split {split_k}"
+    if out_fp32:
+        check_fp32(d, ref, s_abs, what)
+        assert np.count_nonzero(d) == np.count_nonzero(ref)
+    else:
+        check_bf16(d, ref, s_abs, what)
+    return d
+
+
+# ------------------------------------------------------------ closed forms
+
+@pytest.mark.parametrize("m,n,k", [(128, 128, 256), (256, 512, 1024), (4096, 4096, 256)])
+def test_all_ones_gives_k(m, n, k):
+    a = np.full((m, k // 2), 0x22, np.uint8)          # code 2 = 1.0 in both nibbles
+    b = np.full((n, k // 2), 0x22, np.uint8)
+    s = lambda r: oracle.scale_tile(np.full((r, k // 32), 127, np.uint8))
+    d = gpu_gemm(MX, a, s(m), b, s(n), m, n, k, out_fp32=True)
+    assert np.all(d == k)
+
+
+def test_scale_probe_rows_and_blocks():
+    """A = B = 1.0 everywhere; D[m, n] = 32 * sum_j 2^(sa[m, j] - 127) * 2^(sb[n, j] - 127)."""
+    m, n, k = 256, 256, 512
+    rng = np.random.default_rng(1)
+    sa = rng.integers(124, 131, size=(m, k // 32), dtype=np.uint8)
+    sb = rng.integers(124, 131, size=(n, k // 32), dtype=np.uint8)
+    ones = lambda r: np.full((r, k // 2), 0x22, np.uint8)
+    d = gpu_gemm(MX, ones(m), oracle.scale_tile(sa), ones(n), oracle.scale_tile(sb), m, n, k,
+                 out_fp32=True)
+    ea = np.ldexp(1.0, sa.astype(np.int64) - 127)
+    eb = np.ldexp(1.0, sb.astype(np.int64) - 127)
+    assert np.array_equal(d.astype(np.float64), 32.0 * ea @ eb.T)
+
+
+def test_k_position_probe():
+    """Row r of A holds 1.0 at k = 2r and 2.0 at k = 2r + 1, nothing else; B is random.
+    D[r, n] = B[n, 2r] + 2 B[n, 2r + 1] pins where each K element lands (the
+    nibble order itself cancels in a dot product when A and B share it)."""
+    m, n, k = 128, 128, 256
+    a = np.zeros((m, k), np.uint8)
+    a[np.arange(m), np.arange(m) * 2 % k] = 2       # even k in rows 0..127
+    a[np.arange(m), (np.arange(m) * 2 + 1) % k] = 4  # and 2.0 at the odd k after it
+    bcodes = np.random.default_rng(2).integers(0, 16, size=(n, k), dtype=np.uint8)
+    pack = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    s = lambda r: oracle.scale_tile(np.full((r, k // 32), 127, np.uint8))
+    d = gpu_gemm(MX, pack(a), s(m), pack(bcodes), s(n), m, n, k, out_fp32=True)
+    vals = np.array([oracle.e2m1_decode(c) for c in range(16)])
+    kk = np.arange(m) * 2 % k
+    expect = vals[bcodes[:, kk]].T + 2.0 * vals[bcodes[:, kk + 1]].T
+    assert np.array_equal(d.astype(np.float64), expect)
+
+
+# ------------------------------------------------------------ MXFP4 parity
+
+def test_mxfp4_128x128x256_fp32_through_relayout():
+    """The 128x128x256 seed-generated workload: plain scales re-laid out on the GPU."""
+    w = synth.workload_inputs("mxfp4_128x128x256")
+    m = n = 128
+    k = 256
+    sa_t = gpu_relayout(w["a_scales"], m, k, MX)
+    sb_t = gpu_relayout(w["b_scales"], n, k, MX)
+    d = gpu_gemm(MX, w["a_codes"], sa_t, w["b_codes"], sb_t, m, n, k, out_fp32=True)
+    ref, s_abs = oracle.mx_gemm(w["a_codes"], w["a_scales"], w["b_codes"], w["b_scales"], m, n, k)
+    check_fp32(d, ref, s_abs, "mxfp4 128x128x256")
+
+
+@pytest.mark.parametrize("m,n,k", [(32, 32, 256), (160, 96, 512), (320, 544, 1024),
+                                   (128, 256, 2048), (4000, 4064, 256)])
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_mxfp4_ragged_shapes(m, n, k, out_fp32):
+    a, sa, b, sb = _codes_case(m, n, k, seed=m + n + k)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32)
+
+
+@pytest.mark.parametrize("split_k", [1, 2, 3, 5, 8])
+def test_mxfp4_explicit_split_k(split_k):
+    m, n, k = 96, 384, 2048
+    a, sa, b, sb = _codes_case(m, n, k, seed=77)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=False, split_k=split_k)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=True, split_k=split_k)
+
+
+def test_skinny_32x8192x8192_split_k_full():
+    """Decode-shaped skinny GEMM with split-K: every output against the oracle,
+    and bit-identical across runs (fixed reduction order)."""
+    w = synth.workload_inputs("skinny_32x8192x8192")
+    m, n, k = 32, 8192, 8192
+    d1 = _run_and_check_mx(w["a_codes"], w["a_scales"], w["b_codes"], w["b_scales"], m, n, k,
+                           out_fp32=False, split_k=0)
+    d2 = gpu_gemm(MX, w["a_codes"], oracle.scale_tile(w["a_scales"]), w["b_codes"],
+                  oracle.scale_tile(w["b_scales"]), m, n, k, out_fp32=False, split_k=0)
+    assert np.array_equal(d1, d2)
+    assert mx.mx_gemm_workspace_bytes(m, n, k, 0) > 0   # split-K is in use
+
+
+def _quant_gemm_check(name, n_rows, n_cols):
+    wl = synth.WORKLOADS[name]
+    m, n, k = wl["m"], wl["n"], wl["k"]
+    w = synth.workload_inputs(name)
+    ca, sa_t, _ = gpu_quantize(w["a"], MX, TILED)
+    cb, sb_t, _ = gpu_quantize(w["b"], MX, TILED)
+    ra, rsa = oracle.mx_quantize(w["a"])
+    rb, rsb = oracle.mx_quantize(w["b"])
+    assert np.array_equal(ca, ra) and np.array_equal(cb, rb)
+    del w
+    d = gpu_gemm(MX, ca, sa_t, cb, sb_t, m, n, k, out_fp32=False)
+    rows = sample_indices(m, n_rows, 128, seed=1)
+    cols = sample_indices(n, n_cols, 256, seed=2)
+    ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k, rows=rows)
+    st = check_bf16(d[rows], ref, s_abs, f"{name} sampled rows")
+    ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k, cols=cols)
+    check_bf16(d[:, cols], ref, s_abs, f"{name} sampled cols")
+    assert np.count_nonzero(d) > 0.99 * d.size
+    return st
+
+
+def test_quant_gemm_2048x4096x4096_bf16():
+    _quant_gemm_check("quant_gemm_2048x4096x4096", 96, 64)
+
+
+def test_mlp_up_16384x28672x8192_bf16_sampled():
+    _quant_gemm_check("mlp_up_16384x28672x8192", 32, 24)
+
+
+# ------------------------------------------------------------ NVFP4 parity
+
+@pytest.mark.parametrize("m,n,k,split_k", [(128, 128, 256, 1), (256, 320, 1024, 1),
+                                           (160, 4096, 512, 1), (64, 512, 2048, 3)])
+def test_nvfp4_gemm_small(m, n, k, split_k):
+    xa = synth.bf16_normal(m, k, 1.0, seed=m * 3 + k)
+    xb = synth.bf16_normal(n, k, 1.0, seed=n * 5 + k)
+    ca, sa_t, ta = gpu_quantize(xa, NV, TILED)
+    cb, sb_t, tb = gpu_quantize(xb, NV, TILED)
+    ra, rsa, rta = oracle.nvfp4_quantize(xa)
+    rb, rsb, rtb = oracle.nvfp4_quantize(xb)
+    assert np.array_equal(ca, ra) and np.array_equal(cb, rb) and ta == rta and tb == rtb
+    d = gpu_gemm(NV, ca, sa_t, cb, sb_t, m, n, k, out_fp32=True, split_k=split_k, a_ts=ta, b_ts=tb)
+    ref, s_abs = oracle.nvfp4_gemm(ra, rsa, rb, rsb, m, n, k, rta, rtb)
+    check_fp32(d, ref, s_abs, f"nvfp4 {m}x{n}x{k}")
+
+
+def test_nvfp4_4096_cubed_fp32_sampled():
+    name = "nvfp4_4096x4096x4096"
+    m = n = k = 4096
+    w = synth.workload_inputs(name)
+    ca, sa_t, ta = gpu_quantize(w["a"], NV, TILED)
+    cb, sb_t, tb = gpu_quantize(w["b"], NV, TILED)
+    ra, rsa, rta = oracle.nvfp4_quantize(w["a"])
+    rb, rsb, rtb = oracle.nvfp4_quantize(w["b"])
+    d = gpu_gemm(NV, ca, sa_t, cb, sb_t, m, n, k, out_fp32=True, a_ts=ta, b_ts=tb)
+    rows = sample_indices(m, 96, 128, seed=3)
+    cols = sample_indices(n, 64, 256, seed=4)
+    ref, s_abs = oracle.nvfp4_gemm(ra, rsa, rb, rsb, m, n, k, rta, rtb, rows=rows)
+    check_fp32(d[rows], ref, s_abs, "nvfp4 4096^3 rows")
+    ref, s_abs = oracle.nvfp4_gemm(ra, rsa, rb, rsb, m, n, k, rta, rtb, cols=cols)
+    check_fp32(d[:, cols], ref, s_abs, "nvfp4 4096^3 cols")
+
+
+# ------------------------------------------------------------ contract on the GPU
+
+def test_workspace_too_small_is_rejected():
+    m, n, k = 32, 1024, 4096
+    a, sa, b, sb = _codes_case(m, n, k, seed=5)
+    d = torch.full((m, n), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.MXError) as e:
+        mx.mxfp4_gemm(dev_u8(a), dev_u8(oracle.scale_tile(sa)), dev_u8(b),
+                      dev_u8(oracle.scale_tile(sb)), d, m, n, k, mx.MX_LAYOUT_TN, mx.MX_OUT_FP32,
+                      4, ws)
+    assert e.value.code == mx.MX_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(d == 7.0)           # nothing written on an argument error
+
+
+def test_device_is_available():
+    assert mx.mx_available()
