@@ -16,8 +16,9 @@ Timing: inputs are resident in HBM; the K steps are replayed from CUDA graphs
 (one per rotating input set) between two CUDA events on the launching stream,
 with enough rotating sets that the working set exceeds 3x the L2 (129 MB),
 so every step reads cold operands.  Per-kernel durations come from CUDA
-events around each launch in an eager pass over the same K steps.  SM clocks
-and throttle reasons are sampled with nvidia-smi during the timed region.
+events around graphs of back-to-back launches of each call over the same
+rotating sets.  SM clocks and throttle reasons are sampled with nvidia-smi
+during the timed region.
 
 `e2e` is the same metric through the public C ABI with the inputs in pinned
 host memory: every step copies A and W host->device, quantizes, multiplies
@@ -318,30 +319,33 @@ def run_graph_region(wl, graphs, stream, start, end, steps, barrier):
     return start.elapsed_time(end), t0, t1
 
 
-def time_kernels_eager(wl, steps):
-    """Per-call device durations: events around every C-ABI call, K steps."""
+def time_calls(wl, steps, per_graph=40):
+    """Per-call device durations: for each C-ABI call of the step, a CUDA graph of
+    `per_graph` back-to-back calls over the rotating sets, replayed between two
+    events on the launching stream (no host gaps); returns ms per call."""
     torch = wl.torch
-    calls = wl.calls()
     stream = torch.cuda.Stream()
-    n = len(calls)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(200_000_000)         # ~0.1 s head start: the host stays ahead
-        h = stream.cuda_stream
-        for i in range(steps):
-            s = wl.sets[i % len(wl.sets)]
-            evs[i][0].record(stream)
-            for j, (_, fn) in enumerate(calls):
-                fn(s, h)
-                evs[i][j + 1].record(stream)
-    torch.cuda.synchronize()
-    per_call = {label: [] for label, _ in calls}
-    for i in range(steps):
-        for j, (label, _) in enumerate(calls):
-            per_call[label].append(evs[i][j].elapsed_time(evs[i][j + 1]))
-    step_ms = [evs[i][0].elapsed_time(evs[i][n]) for i in range(steps)]
-    return {k: statistics.fmean(v) for k, v in per_call.items()}, statistics.fmean(step_ms)
+    out = {}
+    reps = max(2, steps // per_graph)
+    for label, fn in wl.calls():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            h = torch.cuda.current_stream().cuda_stream
+            for i in range(per_graph):
+                fn(wl.sets[i % len(wl.sets)], h)
+        with torch.cuda.stream(stream):
+            g.replay()
+            g.replay()
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(reps):
+                g.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        out[label] = start.elapsed_time(end) / (reps * per_graph)
+        del g
+    return out
 
 
 def time_e2e(wl, host_inputs, steps):
@@ -527,7 +531,7 @@ def main_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step = float(t.item())
 
-    per_call, eager_step_ms = time_kernels_eager(wl, min(args.steps, 1000))
+    per_call = time_calls(wl, args.steps)
     e2e_steps = args.e2e_steps or min(args.steps, 200)
     e2e_ms, h2d, d2h = time_e2e(wl, host, e2e_steps)
     if world > 1:
@@ -578,7 +582,7 @@ def main_ours(args):
                    "step": " + ".join(per_call.keys())},
         "roofline": roofline,
         "kernels": kernels,
-        "eager_ms_per_step": eager_step_ms,
+        "sum_of_calls_ms": sum(per_call.values()),
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps * sum(kpc.values()),

@@ -113,6 +113,40 @@ int encode_codes_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t k,
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
+// Tensor map over the output (or the split-K partials [splits * M, N]):
+// boxes of 32 rows x 64 bytes, 64-byte swizzle.
+int encode_out_map(CUtensorMap *tm, void *base, int64_t rows, int64_t cols, bool f32,
+                   int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MX_ERR_CUDA;
+  const int esize = f32 ? 4 : 2;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
+// Tensor map over a tile-ordered scale buffer viewed as [bytes / 16, 16]:
+// boxes of box_rows x 16 bytes (32 rows per 512-byte atom), zero past the end.
+int encode_scale_map(CUtensorMap *tm, const void *base, size_t bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MX_ERR_CUDA;
+  const cuuint64_t dims[2] = {16u, static_cast<cuuint64_t>(bytes / 16)};
+  const cuuint64_t strides[1] = {16u};
+  const cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
+}
+
 int launch_rc(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
 int num_sms_or_default() {
@@ -146,21 +180,40 @@ int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *
   DeviceInfo *dev = nullptr;
   const int rc = device_info(&dev);
   if (rc != MX_OK) return rc;
-  int bn = 128, splits = 1;
-  mx::gemm_plan(m, n, k, split_k, dev->num_sms, &bn, &splits);
+  int bn = 128, splits = 1, pair = 0;
+  mx::gemm_plan(m, n, k, split_k, dev->num_sms, &bn, &splits, &pair);
   if (splits > 1) {
     const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(m) *
                         static_cast<size_t>(n) * sizeof(float);
     if (!workspace || workspace_bytes < need) return MX_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
   }
-  CUtensorMap tma, tmb;
+  CUtensorMap tma, tmb, tmd, tmsa, tmsb;
   if (encode_codes_map(&tma, a_codes, m, k, 128) != MX_OK) return MX_ERR_CUDA;
-  if (encode_codes_map(&tmb, b_codes, n, k, bn) != MX_OK) return MX_ERR_CUDA;
+  // the pair kernel stages half of each 256-row B tile per CTA
+  if (encode_codes_map(&tmb, b_codes, n, k, pair ? 128 : bn) != MX_OK) return MX_ERR_CUDA;
+  if (pair) {
+    const int atoms_per_stage = fmt == MX_FMT_MXFP4 ? 2 : 4;
+    if (encode_scale_map(&tmsa, a_scales, mx_scale_bytes(m, k, fmt, MX_SCALE_TCGEN05),
+                         atoms_per_stage * 32) != MX_OK ||
+        encode_scale_map(&tmsb, b_scales, mx_scale_bytes(n, k, fmt, MX_SCALE_TCGEN05),
+                         atoms_per_stage * 32) != MX_OK)
+      return MX_ERR_CUDA;
+  }
+  const int box_cols = mx::gemm_out_box_cols(out_dtype == MX_OUT_FP32, splits);
+  const int orc = splits > 1
+                      ? encode_out_map(&tmd, workspace, static_cast<int64_t>(splits) * m, n, true,
+                                       box_cols)
+                      : encode_out_map(&tmd, d, m, n, out_dtype == MX_OUT_FP32, box_cols);
+  if (orc != MX_OK) return MX_ERR_CUDA;
   mx::GemmArgs g{};
   g.fmt = fmt;
   g.tmap_a = &tma;
   g.tmap_b = &tmb;
+  g.tmap_d = &tmd;
+  g.tmap_sfa = pair ? &tmsa : nullptr;
+  g.tmap_sfb = pair ? &tmsb : nullptr;
+  g.pair = pair;
   g.a_scales = a_scales;
   g.b_scales = b_scales;
   g.a_ts = a_ts;
@@ -231,6 +284,9 @@ MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t l
   if (format == MX_FMT_NVFP4 && tensor_scale == nullptr) return MX_ERR_INVALID_ARG;
   if (cols % block_of(format) != 0) return MX_ERR_UNSUPPORTED_SHAPE;
   if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED_SHAPE;
+  // the kernels index scale blocks of the (row-padded) tensor with 32 bits
+  if ((rows + 127) / 128 * 128 * (cols / block_of(format)) >= (int64_t(1) << 31))
+    return MX_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || (ld_x % 8) != 0 || !aligned16(codes) || !aligned16(scales))
     return MX_ERR_ALIGNMENT;
   if (format == MX_FMT_NVFP4) {
@@ -273,8 +329,8 @@ MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int 
 
 MX_API size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k) {
   if (m <= 0 || n <= 0 || k <= 0 || k % 256 != 0 || split_k < 0) return 0;
-  int bn = 128, splits = 1;
-  mx::gemm_plan(m, n, k, split_k, num_sms_or_default(), &bn, &splits);
+  int bn = 128, splits = 1, pair = 0;
+  mx::gemm_plan(m, n, k, split_k, num_sms_or_default(), &bn, &splits, &pair);
   if (splits <= 1) return 0;
   return static_cast<size_t>(splits) * static_cast<size_t>(m) * static_cast<size_t>(n) *
          sizeof(float);

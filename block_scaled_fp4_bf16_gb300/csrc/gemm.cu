@@ -14,13 +14,17 @@
 //               and the scale atoms of the stage, into an S-stage ring of
 //               shared memory, completion tracked by mbarriers.
 //   warp 1      allocates tensor memory; one lane issues, per stage,
-//               tcgen05.cp of the scale atoms into tensor memory and four
-//               K=64 block-scaled MMAs into the tile's accumulator, then
-//               commits the stage back to the producer.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (lane = row),
-//               conversion to BF16 / FP32 (times alpha for NVFP4), stores.
+//               tcgen05.cp of the stage's scale atoms into that stage's own
+//               set of tensor-memory columns (so copies never wait on the
+//               MMAs of earlier stages) and four K=64 block-scaled MMAs into
+//               the tile's accumulator, then commits the stage back to the
+//               producer.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (lane = row), FP32
+//               (times alpha for NVFP4) or BF16 conversion into a swizzled
+//               2 KB shared-memory buffer per warp, TMA store of 32-row boxes.
 // With BN = 128 there are two accumulators in tensor memory so the
-// epilogue of one tile overlaps the main loop of the next.
+// epilogue of one tile overlaps the main loop of the next; with BN = 256 the
+// accumulator is released as soon as its last columns are in registers.
 // Every wait is bounded; a wait that runs out records a status bit, makes
 // the other roles stop, drains what is in flight and frees tensor memory.
 #include <cuda_bf16.h>
@@ -38,6 +42,7 @@ constexpr int kStageK = 256;         // FP4 elements of K per stage
 constexpr int kStageKBytes = 128;    // = one 128-byte swizzle row
 constexpr int kThreads = 192;
 constexpr int kEpilogueWarps = 4;
+constexpr int kStagingBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
 
 template <int FMT, int BN>
 struct Cfg {
@@ -50,24 +55,28 @@ struct Cfg {
   static constexpr int kSfaBytes = kAtomsK * 512;
   static constexpr int kSfbBytes = kRowAtomsB * kAtomsK * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kAccCol = 0;
-  static constexpr int kSfaCol = kNumAcc * BN;
+  // tensor memory: accumulators, then one scale-factor set per stage
   static constexpr int kSfaCols = kAtomsK * 4;
-  static constexpr int kSfbCol = kSfaCol + kSfaCols;
   static constexpr int kSfbCols = kAtomsK * (BN / 32);
+  static constexpr int kSfSetCols = kSfaCols + kSfbCols;
+  static constexpr int kSfCol = kNumAcc * BN;
   static constexpr int kTmemCols = 512;
-  static_assert(kSfbCol + kSfbCols <= kTmemCols, "tensor memory budget");
+  static_assert(kSfCol + kStages * kSfSetCols <= kTmemCols, "tensor memory budget");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+  static constexpr int kStagingOff = kStages * kStageBytes;
   // barriers: full[S], empty[S], tfull[A], tempty[A]; then tmem slot, abort
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNumAcc) + 16;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  // two staging buffers per epilogue warp when shared memory allows
+  static constexpr int kStagingBufs =
+      (1024 + kStagingOff + 2 * kEpilogueWarps * kStagingBytes + kBarBytes <= 232448) ? 2 : 1;
+  static constexpr int kBarOff = kStagingOff + kStagingBufs * kEpilogueWarps * kStagingBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOff + kBarBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct Params {
   const uint8_t *sfa;
   const uint8_t *sfb;
-  void *d;
-  float *partial;        // split-K workspace [splits, M, N] or null
   const float *a_ts;     // NVFP4 tensor scales or null
   const float *b_ts;
   uint32_t *status;
@@ -76,7 +85,7 @@ struct Params {
   int k_stages, stages_per_split;
   int sfa_katoms, sfb_katoms;  // scale atoms along K per 128-row tile
   int n_row_atoms;             // ceil(N / 128)
-  int out_fp32;
+  int partial;                 // 1: write FP32 partials of split s at rows s*M + m
   int num_units;
 };
 
@@ -101,15 +110,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-template <int FMT, int BN>
+// OUT_F32: 1 -> FP32 boxes of 32 rows x 16 columns, 0 -> BF16 boxes of 32 x 32;
+// either way 64 bytes per row, stored with the 64-byte swizzle.
+template <int FMT, int BN, int OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+                const __grid_constant__ CUtensorMap tmap_b,
+                const __grid_constant__ CUtensorMap tmap_d, const Params p) {
   using C = Cfg<FMT, BN>;
+  constexpr int kChunk = OUT_F32 ? 16 : 32;  // output columns per box
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
   uint64_t *full = bars;
   uint64_t *empty = bars + C::kStages;
   uint64_t *tfull = bars + 2 * C::kStages;
@@ -133,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
+    prefetch_tmap(&tmap_d);
   }
   // B scale atoms past the end of N are never loaded: make them 0 (2^-127
   // or 0.0, both finite) once, for every stage.
@@ -206,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + C::kAccCol + acc * BN;
+      const uint32_t d_tmem = tmem + acc * BN;
       for (int ks = k0; ks < k1; ++ks, ++it) {
         const uint32_t s = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1u;
@@ -218,14 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = smem_u32(smem + s * C::kStageBytes);
         const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
         const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+        const uint32_t sfa_t = tmem + C::kSfCol + s * C::kSfSetCols;
+        const uint32_t sfb_t = sfa_t + C::kSfaCols;
 #pragma unroll
         for (int a = 0; a < C::kAtomsK; ++a)
-          tc_cp_32x128b_warpx4(tmem + C::kSfaCol + a * 4, smem_desc_scale_block(sfa_s + a * 512));
+          tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_scale_block(sfa_s + a * 512));
 #pragma unroll
         for (int ra = 0; ra < C::kRowAtomsB; ++ra)
 #pragma unroll
           for (int a = 0; a < C::kAtomsK; ++a)
-            tc_cp_32x128b_warpx4(tmem + C::kSfbCol + a * (BN / 32) + ra * 4,
+            tc_cp_32x128b_warpx4(sfb_t + a * (BN / 32) + ra * 4,
                                  smem_desc_scale_block(sfb_s + (ra * C::kAtomsK + a) * 512));
         const uint64_t a_desc = smem_desc_sw128_kmajor(st);
         const uint64_t b_desc = smem_desc_sw128_kmajor(st + C::kABytes);
@@ -235,9 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ka = FMT == 0 ? (kk >> 1) : kk;
           const uint32_t sf_id = FMT == 0 ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
           tc_mma_block_scaled<FMT>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk,
-                                   mma_idesc<FMT>(kBM, BN, sf_id), tmem + C::kSfaCol + ka * 4,
-                                   tmem + C::kSfbCol + ka * (BN / 32),
-                                   (ks > k0 || kk > 0) ? 1u : 0u);
+                                   mma_idesc<FMT>(kBM, BN, sf_id), sfa_t + ka * 4,
+                                   sfb_t + ka * (BN / 32), (ks > k0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&empty[s]));
       }
@@ -253,9 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may access tensor-memory lanes 32q..32q+31
-    const int row_in_tile = q * 32 + lane;
+    uint8_t *stage_base = smem + C::kStagingOff + (warp - 2) * C::kStagingBufs * kStagingBytes;
+    uint32_t nbox = 0;  // boxes this warp has stored (selects the staging buffer)
     float alpha = 1.0f;
-    if (FMT == 1) alpha = __fmul_rn(*p.a_ts, *p.b_ts);
+    if (FMT == 1 && !p.partial) alpha = __fmul_rn(*p.a_ts, *p.b_ts);
     uint32_t tile = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tile) {
       int mt, nt, sp;
@@ -266,49 +282,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ready = mbar_wait(smem_u32(&tfull[acc]), aph, abort, p.status);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
-      const int row = mt * kBM + row_in_tile;
-      const bool row_ok = row < p.m;
+      const int row0 = mt * kBM + q * 32;          // first row of this warp's box
+      const bool rows_ok = row0 < p.m;             // M % 32 == 0: all or none
+      const int y = p.partial ? sp * p.m + row0 : row0;
+      constexpr int kChunks = BN / kChunk;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kAccCol + acc * BN + c * 32,
-                         r);
-        tc_wait_ld();
-        const int col = nt * BN + c * 32;
-        if (!row_ok || col >= p.n) continue;
-        if (p.partial != nullptr) {
-          float4 *dst = reinterpret_cast<float4 *>(
-              p.partial + (static_cast<size_t>(sp) * p.m + row) * p.n + col);
+      for (int c = 0; c < kChunks; ++c) {
+        float f[kChunk];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * kChunk;
+        if constexpr (kChunk == 32) {
+          uint32_t r[32];
+          tc_ld_32x32b_x32(taddr, r);
+          tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-        } else if (p.out_fp32) {
-          float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.d) +
-                                                   static_cast<size_t>(row) * p.n + col);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
         } else {
-          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.d) +
-                                                 static_cast<size_t>(row) * p.n + col);
+          uint32_t r[16];
+          tc_ld_32x32b_x16(taddr, r);
+          tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float f[8];
+          for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(r[j]);
+        }
+        if (c == kChunks - 1) {
+          // The accumulator is in registers: hand it back to the MMA warp.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+        const int col0 = nt * BN + c * kChunk;
+        if (!rows_ok || col0 >= p.n) continue;  // warp-uniform
+        if (FMT == 1 && !p.partial) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(__uint_as_float(r[8 * i + j]), alpha);
-            dst[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-          }
+          for (int j = 0; j < kChunk; ++j) f[j] = __fmul_rn(f[j], alpha);
+        }
+        // The box stored from this staging buffer last time must have left it.
+        uint8_t *stage_buf = stage_base + (nbox % C::kStagingBufs) * kStagingBytes;
+        ++nbox;
+        if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
+        __syncwarp();
+        uint4 v[4];
+        if constexpr (kChunk == 32) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[i] = make_uint4(pack_bf16x2(f[8 * i], f[8 * i + 1]),
+                              pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
+                              pack_bf16x2(f[8 * i + 4], f[8 * i + 5]),
+                              pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[i] = make_uint4(__float_as_uint(f[4 * i]), __float_as_uint(f[4 * i + 1]),
+                              __float_as_uint(f[4 * i + 2]), __float_as_uint(f[4 * i + 3]));
+        }
+        // 64-byte swizzle: the 16-byte unit i of row `lane` goes to unit
+        // i ^ ((lane >> 1) & 3), which also spreads the warp over all banks.
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4 *>(stage_buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) = v[i];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_d, smem_u32(stage_buf), col0, y);
+          bulk_commit_group();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
     }
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -346,7 +386,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
     if (out_fp32) {
       reinterpret_cast<float4 *>(out)[i] = acc;
     } else {
-      reinterpret_cast<uint2 *>(out)[i] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      reinterpret_cast<uint2 *>(out)[i] =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     }
   }
 }
@@ -365,7 +406,7 @@ __global__ void wait_selftest_kernel(uint32_t *status, uint64_t timeout_ns) {
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0u, &abort_flag, status, timeout_ns);
 }
 
-template <int FMT, int BN>
+template <int FMT, int BN, int OUT_F32>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   using C = Cfg<FMT, BN>;
   static bool attr_set[64] = {};
@@ -373,16 +414,14 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, OUT_F32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   Params p{};
   p.sfa = static_cast<const uint8_t *>(g.a_scales);
   p.sfb = static_cast<const uint8_t *>(g.b_scales);
-  p.d = g.d;
-  p.partial = g.split_k > 1 ? g.workspace : nullptr;
   p.a_ts = g.a_ts;
   p.b_ts = g.b_ts;
   p.status = g.status;
@@ -396,35 +435,50 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.sfa_katoms = static_cast<int>(g.k / (FMT == 0 ? 128 : 64));
   p.sfb_katoms = p.sfa_katoms;
   p.n_row_atoms = static_cast<int>((g.n + 127) / 128);
-  p.out_fp32 = g.out_fp32;
+  p.partial = g.split_k > 1 ? 1 : 0;
   p.num_units = p.m_tiles * p.n_tiles * p.splits;
   const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
-  gemm_kernel<FMT, BN><<<grid, kThreads, C::kSmemBytes, s>>>(*g.tmap_a, *g.tmap_b, p);
+  gemm_kernel<FMT, BN, OUT_F32>
+      <<<grid, kThreads, C::kSmemBytes, s>>>(*g.tmap_a, *g.tmap_b, *g.tmap_d, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || g.split_k <= 1) return e;
-  const int64_t mn = g.m * g.n;
-  int64_t rgrid = (mn / 4 + 255) / 256;
-  if (rgrid > 4 * g.num_sms) rgrid = 4 * g.num_sms;
-  splitk_reduce_kernel<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(
-      g.workspace, g.split_k, mn, g.d, g.out_fp32, FMT == 1 ? g.a_ts : nullptr,
-      FMT == 1 ? g.b_ts : nullptr);
-  return cudaGetLastError();
+  return launch_splitk_reduce(g, s);
+}
+
+template <int FMT, int BN>
+cudaError_t launch_bn(const GemmArgs &g, cudaStream_t s) {
+  // split-K partials are FP32 whatever the final output type
+  return (g.out_fp32 || g.split_k > 1) ? launch_typed<FMT, BN, 1>(g, s)
+                                       : launch_typed<FMT, BN, 0>(g, s);
 }
 
 }  // namespace
 
-void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits) {
-  const int64_t m_tiles = (m + kBM - 1) / kBM;
-  const int64_t tiles256 = m_tiles * ((n + 255) / 256);
-  *bn = (tiles256 >= 2 * num_sms) ? 256 : 128;
-  const int64_t tiles = m_tiles * ((n + *bn - 1) / *bn);
+void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits,
+               int *pair) {
   const int64_t k_stages = k / kStageK;
+  int64_t tiles;
+  int64_t slots;  // units the GPU runs at once
+  if (m > kBM) {
+    // CTA pairs with 256 x 256 tiles
+    *pair = 1;
+    *bn = 256;
+    tiles = ((m + 255) / 256) * ((n + 255) / 256);
+    slots = num_sms / 2;
+  } else {
+    *pair = 0;
+    const int64_t m_tiles = (m + kBM - 1) / kBM;
+    const int64_t tiles256 = m_tiles * ((n + 255) / 256);
+    *bn = (tiles256 >= 2 * num_sms) ? 256 : 128;
+    tiles = m_tiles * ((n + *bn - 1) / *bn);
+    slots = num_sms;
+  }
   int s = split_k;
   if (s <= 0) {
     // Automatic: split K only when the tiles cannot fill the GPU, keeping at
     // least 4 stages of K per split.
     s = 1;
-    while (tiles * (s * 2) <= num_sms && k_stages / (s * 2) >= 4) s *= 2;
+    while (tiles * (s * 2) <= slots && k_stages / (s * 2) >= 4) s *= 2;
   }
   if (s > k_stages) s = static_cast<int>(k_stages);
   if (s < 1) s = 1;
@@ -433,11 +487,22 @@ void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *b
   *splits = s;
 }
 
+int gemm_out_box_cols(int out_fp32, int split_k) { return (out_fp32 || split_k > 1) ? 16 : 32; }
+
+cudaError_t launch_splitk_reduce(const GemmArgs &g, cudaStream_t s) {
+  const int64_t mn = g.m * g.n;
+  int64_t rgrid = (mn / 4 + 255) / 256;
+  if (rgrid > 4 * g.num_sms) rgrid = 4 * g.num_sms;
+  splitk_reduce_kernel<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(
+      g.workspace, g.split_k, mn, g.d, g.out_fp32, g.fmt == 1 ? g.a_ts : nullptr,
+      g.fmt == 1 ? g.b_ts : nullptr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t s) {
-  if (g.fmt == 0) {
-    return g.bn == 256 ? launch_typed<0, 256>(g, s) : launch_typed<0, 128>(g, s);
-  }
-  return g.bn == 256 ? launch_typed<1, 256>(g, s) : launch_typed<1, 128>(g, s);
+  if (g.pair) return launch_gemm_pair(g, s);
+  if (g.fmt == 0) return g.bn == 256 ? launch_bn<0, 256>(g, s) : launch_bn<0, 128>(g, s);
+  return g.bn == 256 ? launch_bn<1, 256>(g, s) : launch_bn<1, 128>(g, s);
 }
 
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t timeout_ns, cudaStream_t s) {

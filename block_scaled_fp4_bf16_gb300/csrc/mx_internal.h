@@ -36,22 +36,33 @@ struct GemmArgs {
   int fmt;  // 0 MXFP4, 1 NVFP4
   const CUtensorMap *tmap_a;  // codes A [M, K/2] bytes, box 128 rows
   const CUtensorMap *tmap_b;  // codes B [N, K/2] bytes, box `bn` rows
+  const CUtensorMap *tmap_d;  // output (or split-K partials), box 32 rows x 64 bytes
+  const CUtensorMap *tmap_sfa;  // CTA-pair kernel: scale buffers as [bytes/16, 16] rows
+  const CUtensorMap *tmap_sfb;
   const void *a_scales, *b_scales;
   const float *a_ts, *b_ts;  // NVFP4 tensor scales (device)
   void *d;
   int out_fp32;
   int64_t m, n, k;
   int split_k;   // >= 1, already resolved
-  int bn;        // 128 or 256
+  int bn;        // single-CTA kernel: 128 or 256
+  int pair;      // 1: CTA-pair kernel with 256 x 256 tiles
   float *workspace;
   uint32_t *status;
   int num_sms;
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s);
+cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t s);
+cudaError_t launch_splitk_reduce(const GemmArgs &a, cudaStream_t s);
 
-// Tile width and split count the GEMM uses for a shape (split_k 0 = auto).
-void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits);
+// Kernel (single CTA with tile width bn, or CTA pair) and split count the
+// GEMM uses for a shape (split_k 0 = auto).
+void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits,
+               int *pair);
+
+// Columns per output box of the GEMM epilogue (64 bytes of BF16 or FP32).
+int gemm_out_box_cols(int out_fp32, int split_k);
 
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t timeout_ns, cudaStream_t s);
 

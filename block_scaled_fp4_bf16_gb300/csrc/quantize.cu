@@ -9,13 +9,14 @@
 // scales per 16 elements relative to an FP32 per-tensor scale
 // s_t = amax_t / (6 * 448).
 //
-// Design (HBM bound: 2 bytes read, 0.53 bytes written per element): the
-// row-resident layout of the register (G2R) quantizers on the NVFP4 page:
-// one 16-byte load of 8 BF16 per thread, 4 (MX) or 2 (NV) neighbouring
-// lanes form a block and take its amax with xor shuffles, each lane then
-// writes its 8 codes as one 32-bit store.  No shared memory; several loads
-// per thread in flight; no integer division on the hot path (a CTA owns
-// whole rows).
+// Design (HBM bound: 2 bytes read, 0.53 bytes written per element), after
+// the register-resident (G2R) quantizers of the NVFP4 page: one thread owns
+// one scale block, reads it with 32-byte loads (a warp covers 1-2 KB of
+// consecutive memory), takes the block's abs-max with packed BF16x2 max
+// instructions (no shuffles), scales with packed FP32x2 multiplies, converts
+// two elements per cvt instruction and writes its codes with one store.  No
+// shared memory, 32-bit index arithmetic, and a multiply-high division for
+// (row, block).
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -27,7 +28,23 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+
+// q = n / d for 32-bit n, by a 64-bit multiply-high: m = floor((2^64-1)/d) + 1.
+struct FastDiv {
+  uint32_t d;
+  unsigned long long m;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.m = d <= 1 ? 0ull : (~0ull / d) + 1ull;
+  return f;
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
+  return f.d <= 1 ? n : static_cast<uint32_t>(__umul64hi(static_cast<unsigned long long>(n), f.m));
+}
 
 // floor(log2 |x|) of a non-zero BF16 magnitude (15-bit pattern).
 __device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
@@ -36,117 +53,136 @@ __device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
   return (31 - __clz(static_cast<int>(mag & 0x7Fu))) - 133;  // subnormal m * 2^-133
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 // Byte offset of scale (row r, scale column c) in the 128x4 tile order.
-__device__ __forceinline__ int64_t tiled_offset(int64_t r, int64_t c, int64_t katoms) {
-  return ((r >> 7) * katoms + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+__device__ __forceinline__ uint32_t tiled_offset(uint32_t r, uint32_t c, uint32_t katoms) {
+  return ((r >> 7) * katoms + (c >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (c & 3u);
 }
 
-__device__ __forceinline__ uint4 load_streaming(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// 32 bytes from global memory (read-only path): one 32-byte load when the
+// address is 32-byte aligned (WIDE), else two 16-byte loads.
+template <bool WIDE>
+__device__ __forceinline__ void load32(const void *p, uint32_t *w) {
+  if constexpr (WIDE) {
+    asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "l"(p));
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(static_cast<const uint8_t *>(p) + 16));
+  }
 }
 
-// MXFP4 quantize.  Grid: ceil(rows_pad / rows_per_cta) CTAs.
+// max(|a|, |b|) per BF16 lane (the sign bits of the result are to be masked).
+__device__ __forceinline__ uint32_t maxabs2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Largest magnitude (15-bit BF16 pattern) over N packed BF16x2 words.
+template <int N>
+__device__ __forceinline__ uint32_t block_amax(const uint32_t *w) {
+  uint32_t t[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) t[i] = maxabs2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+  for (int s = N / 4; s >= 1; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < s; ++i) t[i] = maxabs2(t[i], t[i + s]);
+  const uint32_t m = t[0] & 0x7FFF7FFFu;
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// Four BF16x2 words (8 elements, element 2i in the low half of word i)
+// times `scale`, rounded to E2M1 (nearest even, saturating), packed into
+// one 32-bit word with element 0 in bits 0..3.  The products are exact
+// (power-of-two scale) for the MX quantizer.
+__device__ __forceinline__ uint32_t scale_to_e2m1x8(const uint32_t *w, float scale) {
+  uint32_t out;
+  asm("{\n"
+      " .reg .b64 s, p0, p1, p2, p3;\n"
+      " .reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n"
+      " .reg .b8 c0, c1, c2, c3;\n"
+      " mov.b64 s, {%1, %1};\n"
+      " mov.b64 p0, {%2, %3};\n mul.rn.f32x2 p0, p0, s;\n mov.b64 {a0, b0}, p0;\n"
+      " mov.b64 p1, {%4, %5};\n mul.rn.f32x2 p1, p1, s;\n mov.b64 {a1, b1}, p1;\n"
+      " mov.b64 p2, {%6, %7};\n mul.rn.f32x2 p2, p2, s;\n mov.b64 {a2, b2}, p2;\n"
+      " mov.b64 p3, {%8, %9};\n mul.rn.f32x2 p3, p3, s;\n mov.b64 {a3, b3}, p3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c0, b0, a0;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c1, b1, a1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c2, b2, a2;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c3, b3, a3;\n"
+      " mov.b32 %0, {c0, c1, c2, c3};\n"
+      "}\n"
+      : "=r"(out)
+      : "f"(scale), "f"(__uint_as_float(w[0] << 16)), "f"(__uint_as_float(w[0] & 0xFFFF0000u)),
+        "f"(__uint_as_float(w[1] << 16)), "f"(__uint_as_float(w[1] & 0xFFFF0000u)),
+        "f"(__uint_as_float(w[2] << 16)), "f"(__uint_as_float(w[2] & 0xFFFF0000u)),
+        "f"(__uint_as_float(w[3] << 16)), "f"(__uint_as_float(w[3] & 0xFFFF0000u)));
+  return out;
+}
+
+// MXFP4 quantize: thread b owns block b of the [rows_pad, kb] block grid.
 // x: BF16 bits [rows, cols] stride ld.  codes [rows, cols/2].
 // scales: plain [rows, kb] or tiled (rows padded to rows_pad with 0 bytes).
+// WIDE: x is 32-byte aligned and ld % 16 == 0.
+template <bool WIDE>
 __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(
-    const uint16_t *__restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, int64_t rows_pad,
-    int tpr_log2) {
-  const int64_t vpr = cols >> 3;  // 16-byte vectors per row (multiple of 4)
-  const int64_t kb = cols >> 5;
-  const int64_t katoms = (kb + 3) >> 2;
-  const int tpr = 1 << tpr_log2;
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * (kThreads >> tpr_log2) +
-                    (threadIdx.x >> tpr_log2);
-  const int lane_in_row = threadIdx.x & (tpr - 1);
-  // No lane leaves early: every lane runs the same number of iterations and
-  // executes every shuffle; rows past rows_pad and slots past vpr only skip
-  // their loads and stores.  A 4-lane block group shares one row and has the
-  // same c8 < vpr outcome (vpr % 4 == 0, tpr >= 4).
-  const bool in_grid = r < rows_pad;
-  const bool real = r < rows;
-  const uint16_t *xrow = x + r * ld;
-  uint8_t *crow = codes + r * (cols >> 1);
-
-  for (int64_t base = 0; base < vpr; base += static_cast<int64_t>(tpr) * kUnroll) {
-    uint4 v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c8 = base + lane_in_row + static_cast<int64_t>(u) * tpr;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (real && c8 < vpr) v[u] = load_streaming(xrow + c8 * 8);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c8 = base + lane_in_row + static_cast<int64_t>(u) * tpr;
-      const uint32_t w0 = v[u].x, w1 = v[u].y, w2 = v[u].z, w3 = v[u].w;
-      const uint32_t m2 = __vmaxu2(__vmaxu2(w0 & 0x7FFF7FFFu, w1 & 0x7FFF7FFFu),
-                                   __vmaxu2(w2 & 0x7FFF7FFFu, w3 & 0x7FFF7FFFu));
-      uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
-      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-      if (!in_grid || c8 >= vpr) continue;
-      const int e = amax ? max(bf16_floor_log2(amax) - 2, -127) : -127;
-      const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-      if (real) {
-        uint32_t packed = cvt_e2m1x2(bf16_lo(w0) * inv, bf16_hi(w0) * inv);
-        packed |= cvt_e2m1x2(bf16_lo(w1) * inv, bf16_hi(w1) * inv) << 8;
-        packed |= cvt_e2m1x2(bf16_lo(w2) * inv, bf16_hi(w2) * inv) << 16;
-        packed |= cvt_e2m1x2(bf16_lo(w3) * inv, bf16_hi(w3) * inv) << 24;
-        *reinterpret_cast<uint32_t *>(crow + c8 * 4) = packed;
-      }
-      if ((c8 & 3) == 0) {
-        const int64_t j = c8 >> 2;
-        const uint8_t sb = real ? static_cast<uint8_t>(e + 127) : 0;
-        if (tiled) {
-          scales[tiled_offset(r, j, katoms)] = sb;
-          if (j == kb - 1)
-            for (int64_t jj = kb; jj < katoms * 4; ++jj) scales[tiled_offset(r, jj, katoms)] = 0;
-        } else {
-          scales[r * kb + j] = sb;
-        }
-      }
-    }
+    const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, int64_t ld,
+    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, uint32_t total,
+    FastDiv kbdiv, uint32_t katoms) {
+  const uint32_t b = blockIdx.x * kThreads + threadIdx.x;
+  if (b >= total) return;
+  const uint32_t kb = kbdiv.d;
+  const uint32_t r = fast_div(b, kbdiv);
+  const uint32_t j = b - r * kb;
+  uint32_t sbyte = 0;
+  if (r < rows) {
+    const uint16_t *src = x + static_cast<int64_t>(r) * ld + j * 32u;
+    uint32_t w[16];
+    load32<WIDE>(src, &w[0]);
+    load32<WIDE>(src + 16, &w[8]);
+    const uint32_t amax = block_amax<16>(w);
+    const int e = amax ? max(bf16_floor_log2(amax) - 2, -127) : -127;
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+    uint4 out;
+    out.x = scale_to_e2m1x8(&w[0], inv);
+    out.y = scale_to_e2m1x8(&w[4], inv);
+    out.z = scale_to_e2m1x8(&w[8], inv);
+    out.w = scale_to_e2m1x8(&w[12], inv);
+    *reinterpret_cast<uint4 *>(codes + static_cast<int64_t>(r) * (cols >> 1) + j * 16u) = out;
+    sbyte = static_cast<uint32_t>(e + 127);
+  }
+  if (tiled) {
+    scales[tiled_offset(r, j, katoms)] = static_cast<uint8_t>(sbyte);
+    if (j == kb - 1)
+      for (uint32_t jj = kb; jj < katoms * 4u; ++jj) scales[tiled_offset(r, jj, katoms)] = 0;
+  } else {
+    scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sbyte);
   }
 }
 
 // NVFP4 pass 1: per-CTA partial amax (as the 15-bit BF16 magnitude
-// pattern, whose integer order is the order of the values) over rows
-// r = blockIdx.x * rpc + ..., stepping by gridDim.x * rpc.
-__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(
-    const uint16_t *__restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-    uint32_t *__restrict__ partials, int tpr_log2) {
-  const int64_t vpr = cols >> 3;
-  const int tpr = 1 << tpr_log2;
-  const int rpc = kThreads >> tpr_log2;
-  const int lane_in_row = threadIdx.x & (tpr - 1);
-  uint32_t m2 = 0;
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * rpc + (threadIdx.x >> tpr_log2); r < rows;
-       r += static_cast<int64_t>(gridDim.x) * rpc) {
-    const uint16_t *xrow = x + r * ld;
-    for (int64_t c0 = lane_in_row; c0 < vpr; c0 += static_cast<int64_t>(tpr) * kUnroll) {
-      uint4 v[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t c8 = c0 + static_cast<int64_t>(u) * tpr;
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (c8 < vpr) v[u] = load_streaming(xrow + c8 * 8);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
-                                   __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu)));
-      }
-    }
+// pattern, whose integer order is the order of the values), grid-stride over
+// the 16-element blocks.
+template <bool WIDE>
+__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const uint16_t *__restrict__ x,
+                                                              int64_t ld, uint32_t total,
+                                                              FastDiv kbdiv,
+                                                              uint32_t *__restrict__ partials) {
+  uint32_t m = 0;
+  for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < total; b += gridDim.x * kThreads) {
+    const uint32_t r = fast_div(b, kbdiv);
+    const uint32_t j = b - r * kbdiv.d;
+    uint32_t w[8];
+    load32<WIDE>(x + static_cast<int64_t>(r) * ld + j * 16u, w);
+    m = max(m, block_amax<8>(w));
   }
-  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
   __shared__ uint32_t warp_max[kThreads / 32];
@@ -167,13 +203,77 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// NVFP4 pass 2: reduce the partial maxima, then quantize.  Every binary32
-// step is an explicit round-to-nearest operation (no contraction, IEEE
-// division) so the result is byte-identical to the definition.
+__device__ __forceinline__ float rcp_rn(float v) {
+  float r;
+  asm("rcp.rn.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Eight BF16 (four words) divided by den, each quotient rounded to nearest
+// binary32, then to E2M1; packed as in scale_to_e2m1x8.  With r = RN(1/den),
+// q0 = RN(x * r), the exact residual t = x - q0 * den (one FMA) and
+// q = RN(q0 + t * r) is the correctly rounded quotient x / den (Markstein's
+// correction); den is kept away from overflow and underflow by the caller.
+// The sign of x is then copied onto q, which only matters for x = -0.
+__device__ __forceinline__ uint32_t div_to_e2m1x8(const uint32_t *w, float den, float r) {
+  uint32_t out;
+  asm("{\n"
+      " .reg .b64 rr, nd, x0, x1, x2, x3, q0, q1, q2, q3, t0, t1, t2, t3;\n"
+      " .reg .f32 a0, b0, a1, b1, a2, b2, a3, b3, nden;\n"
+      " .reg .b8 c0, c1, c2, c3;\n"
+      " neg.f32 nden, %1;\n"
+      " mov.b64 rr, {%2, %2};\n mov.b64 nd, {nden, nden};\n"
+      " mov.b64 x0, {%3, %4};\n mov.b64 x1, {%5, %6};\n"
+      " mov.b64 x2, {%7, %8};\n mov.b64 x3, {%9, %10};\n"
+      " mul.rn.f32x2 q0, x0, rr;\n mul.rn.f32x2 q1, x1, rr;\n"
+      " mul.rn.f32x2 q2, x2, rr;\n mul.rn.f32x2 q3, x3, rr;\n"
+      " fma.rn.f32x2 t0, q0, nd, x0;\n fma.rn.f32x2 t1, q1, nd, x1;\n"
+      " fma.rn.f32x2 t2, q2, nd, x2;\n fma.rn.f32x2 t3, q3, nd, x3;\n"
+      " fma.rn.f32x2 q0, t0, rr, q0;\n fma.rn.f32x2 q1, t1, rr, q1;\n"
+      " fma.rn.f32x2 q2, t2, rr, q2;\n fma.rn.f32x2 q3, t3, rr, q3;\n"
+      // the quotient takes the sign of x (den > 0); the residual step alone
+      // would turn x = -0 into +0
+      " and.b64 t0, x0, 0x8000000080000000;\n or.b64 q0, q0, t0;\n"
+      " and.b64 t1, x1, 0x8000000080000000;\n or.b64 q1, q1, t1;\n"
+      " and.b64 t2, x2, 0x8000000080000000;\n or.b64 q2, q2, t2;\n"
+      " and.b64 t3, x3, 0x8000000080000000;\n or.b64 q3, q3, t3;\n"
+      " mov.b64 {a0, b0}, q0;\n mov.b64 {a1, b1}, q1;\n"
+      " mov.b64 {a2, b2}, q2;\n mov.b64 {a3, b3}, q3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c0, b0, a0;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c1, b1, a1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c2, b2, a2;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 c3, b3, a3;\n"
+      " mov.b32 %0, {c0, c1, c2, c3};\n"
+      "}\n"
+      : "=r"(out)
+      : "f"(den), "f"(r), "f"(__uint_as_float(w[0] << 16)),
+        "f"(__uint_as_float(w[0] & 0xFFFF0000u)), "f"(__uint_as_float(w[1] << 16)),
+        "f"(__uint_as_float(w[1] & 0xFFFF0000u)), "f"(__uint_as_float(w[2] << 16)),
+        "f"(__uint_as_float(w[2] & 0xFFFF0000u)), "f"(__uint_as_float(w[3] << 16)),
+        "f"(__uint_as_float(w[3] & 0xFFFF0000u)));
+  return out;
+}
+
+// The same with IEEE divisions (used where den is outside the safe range).
+__device__ __forceinline__ uint32_t div_to_e2m1x8_ieee(const uint32_t *w, float den) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    out |= cvt_e2m1x2(__fdiv_rn(__uint_as_float(w[i] << 16), den),
+                      __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), den))
+           << (8 * i);
+  return out;
+}
+
+// NVFP4 pass 2: every CTA reduces the partial maxima to s_t, then thread b
+// quantizes 16-element block b.  Each binary32 step of the definition is one
+// round-to-nearest operation (correctly rounded divisions where it divides).
+template <bool WIDE>
 __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
-    const uint16_t *__restrict__ x, int64_t rows, int64_t cols, int64_t ld,
-    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, int64_t rows_pad,
-    const uint32_t *__restrict__ partials, float *__restrict__ tensor_scale, int tpr_log2) {
+    const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, int64_t ld,
+    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, uint32_t total,
+    FastDiv kbdiv, uint32_t katoms, const uint32_t *__restrict__ partials,
+    float *__restrict__ tensor_scale) {
   __shared__ uint32_t warp_max[kThreads / 32];
   __shared__ float s_t_shared;
   {
@@ -196,61 +296,37 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
   const float s_t = s_t_shared;
   const float six_s_t = __fmul_rn(6.0f, s_t);
 
-  const int64_t vpr = cols >> 3;  // multiple of 2
-  const int64_t kb = cols >> 4;
-  const int64_t katoms = (kb + 3) >> 2;
-  const int tpr = 1 << tpr_log2;
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * (kThreads >> tpr_log2) +
-                    (threadIdx.x >> tpr_log2);
-  const int lane_in_row = threadIdx.x & (tpr - 1);
-  // Same lane discipline as the MXFP4 kernel (2-lane block groups).
-  const bool in_grid = r < rows_pad;
-  const bool real = r < rows;
-  const uint16_t *xrow = x + r * ld;
-  uint8_t *crow = codes + r * (cols >> 1);
-
-  for (int64_t base = 0; base < vpr; base += static_cast<int64_t>(tpr) * kUnroll) {
-    uint4 v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c8 = base + lane_in_row + static_cast<int64_t>(u) * tpr;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (real && c8 < vpr) v[u] = load_streaming(xrow + c8 * 8);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t c8 = base + lane_in_row + static_cast<int64_t>(u) * tpr;
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      const uint32_t m2 = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                   __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
-      uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
-      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      if (!in_grid || c8 >= vpr) continue;
-      uint32_t sb = 0;
-      if (s_t > 0.0f) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(amax << 16), six_s_t));
-      if (real) {
-        uint32_t packed = 0;
-        if (sb != 0) {
-          const float den = __fmul_rn(e4m3_to_f32(sb), s_t);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            packed |= cvt_e2m1x2(__fdiv_rn(bf16_lo(w[i]), den), __fdiv_rn(bf16_hi(w[i]), den))
-                      << (8 * i);
-        }
-        *reinterpret_cast<uint32_t *>(crow + c8 * 4) = packed;
-      }
-      if ((c8 & 1) == 0) {
-        const int64_t j = c8 >> 1;
-        const uint8_t sbyte = real ? static_cast<uint8_t>(sb) : 0;
-        if (tiled) {
-          scales[tiled_offset(r, j, katoms)] = sbyte;
-          if (j == kb - 1)
-            for (int64_t jj = kb; jj < katoms * 4; ++jj) scales[tiled_offset(r, jj, katoms)] = 0;
-        } else {
-          scales[r * kb + j] = sbyte;
-        }
+  const uint32_t b = blockIdx.x * kThreads + threadIdx.x;
+  if (b >= total) return;
+  const uint32_t kb = kbdiv.d;
+  const uint32_t r = fast_div(b, kbdiv);
+  const uint32_t j = b - r * kb;
+  uint32_t sb = 0;
+  if (r < rows) {
+    uint32_t w[8];
+    load32<WIDE>(x + static_cast<int64_t>(r) * ld + j * 16u, w);
+    const uint32_t amax = block_amax<8>(w);
+    if (s_t > 0.0f) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(amax << 16), six_s_t));
+    uint2 out = make_uint2(0u, 0u);
+    if (sb != 0) {
+      const float den = __fmul_rn(e4m3_to_f32(sb), s_t);
+      if (den >= 0x1p-100f && den <= 0x1p+100f) {
+        const float rc = rcp_rn(den);
+        out.x = div_to_e2m1x8(&w[0], den, rc);
+        out.y = div_to_e2m1x8(&w[4], den, rc);
+      } else {
+        out.x = div_to_e2m1x8_ieee(&w[0], den);
+        out.y = div_to_e2m1x8_ieee(&w[4], den);
       }
     }
+    *reinterpret_cast<uint2 *>(codes + static_cast<int64_t>(r) * (cols >> 1) + j * 8u) = out;
+  }
+  if (tiled) {
+    scales[tiled_offset(r, j, katoms)] = static_cast<uint8_t>(sb);
+    if (j == kb - 1)
+      for (uint32_t jj = kb; jj < katoms * 4u; ++jj) scales[tiled_offset(r, jj, katoms)] = 0;
+  } else {
+    scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
   }
 }
 
@@ -270,41 +346,44 @@ __global__ void __launch_bounds__(kThreads) scale_relayout_kernel(
   }
 }
 
-int tpr_log2_for(int64_t vpr) {
-  // threads per row: a power of two, at least 4, at most kThreads, and not
-  // much more than the row needs
-  int l = 2;
-  while ((1 << l) < vpr && (1 << l) < kThreads) ++l;
-  return l;
+bool wide_ok(const void *x, int64_t ld) {
+  return (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && (ld % 16) == 0;
 }
 
 }  // namespace
 
 cudaError_t launch_mx_quantize(const QuantizeArgs &a, cudaStream_t s) {
-  const int64_t vpr = a.cols / 8;
-  const int tl = tpr_log2_for(vpr);
-  const int64_t rpc = kThreads >> tl;
-  const int64_t rows_pad = a.tiled ? (a.rows + 127) / 128 * 128 : a.rows;
-  const int64_t grid = (rows_pad + rpc - 1) / rpc;
-  mx_quantize_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
-      static_cast<const uint16_t *>(a.x), a.rows, a.cols, a.ld, static_cast<uint8_t *>(a.codes),
-      static_cast<uint8_t *>(a.scales), a.tiled, rows_pad, tl);
+  const uint32_t kb = static_cast<uint32_t>(a.cols / 32);
+  const uint32_t rows_pad = static_cast<uint32_t>(a.tiled ? (a.rows + 127) / 128 * 128 : a.rows);
+  const uint32_t total = rows_pad * kb;
+  const uint32_t grid = (total + kThreads - 1) / kThreads;
+  auto kern = wide_ok(a.x, a.ld) ? mx_quantize_kernel<true> : mx_quantize_kernel<false>;
+  kern<<<grid, kThreads, 0, s>>>(
+      static_cast<const uint16_t *>(a.x), static_cast<uint32_t>(a.rows),
+      static_cast<uint32_t>(a.cols), a.ld, static_cast<uint8_t *>(a.codes),
+      static_cast<uint8_t *>(a.scales), a.tiled, total, make_fastdiv(kb), (kb + 3) / 4);
   return cudaGetLastError();
 }
 
 cudaError_t launch_nvfp4_quantize(const QuantizeArgs &a, cudaStream_t s) {
-  const int64_t vpr = a.cols / 8;
-  const int tl = tpr_log2_for(vpr);
-  const int64_t rpc = kThreads >> tl;
-  nvfp4_amax_kernel<<<kAmaxPartials, kThreads, 0, s>>>(static_cast<const uint16_t *>(a.x), a.rows,
-                                                       a.cols, a.ld, a.partials, tl);
+  const uint32_t kb = static_cast<uint32_t>(a.cols / 16);
+  const FastDiv kbdiv = make_fastdiv(kb);
+  const uint32_t real_total = static_cast<uint32_t>(a.rows) * kb;
+  const bool wide = wide_ok(a.x, a.ld);
+  auto amax_kern = wide ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>;
+  amax_kern<<<kAmaxPartials, kThreads, 0, s>>>(static_cast<const uint16_t *>(a.x), a.ld,
+                                               real_total, kbdiv, a.partials);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t rows_pad = a.tiled ? (a.rows + 127) / 128 * 128 : a.rows;
-  const int64_t grid = (rows_pad + rpc - 1) / rpc;
-  nvfp4_quantize_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
-      static_cast<const uint16_t *>(a.x), a.rows, a.cols, a.ld, static_cast<uint8_t *>(a.codes),
-      static_cast<uint8_t *>(a.scales), a.tiled, rows_pad, a.partials, a.tensor_scale, tl);
+  const uint32_t rows_pad = static_cast<uint32_t>(a.tiled ? (a.rows + 127) / 128 * 128 : a.rows);
+  const uint32_t total = rows_pad * kb;
+  const uint32_t grid = (total + kThreads - 1) / kThreads;
+  auto quant_kern = wide ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>;
+  quant_kern<<<grid, kThreads, 0, s>>>(
+      static_cast<const uint16_t *>(a.x), static_cast<uint32_t>(a.rows),
+      static_cast<uint32_t>(a.cols), a.ld, static_cast<uint8_t *>(a.codes),
+      static_cast<uint8_t *>(a.scales), a.tiled, total, kbdiv, (kb + 3) / 4, a.partials,
+      a.tensor_scale);
   return cudaGetLastError();
 }
 

@@ -94,7 +94,8 @@ def test_mxfp4_128x128x256_fp32_through_relayout():
 
 
 @pytest.mark.parametrize("m,n,k", [(32, 32, 256), (160, 96, 512), (320, 544, 1024),
-                                   (128, 256, 2048), (4000, 4064, 256)])
+                                   (128, 256, 2048), (4000, 4064, 256), (544, 288, 768),
+                                   (256, 256, 256)])
 @pytest.mark.parametrize("out_fp32", [True, False])
 def test_mxfp4_ragged_shapes(m, n, k, out_fp32):
     a, sa, b, sb = _codes_case(m, n, k, seed=m + n + k)
@@ -102,11 +103,19 @@ def test_mxfp4_ragged_shapes(m, n, k, out_fp32):
 
 
 @pytest.mark.parametrize("split_k", [1, 2, 3, 5, 8])
-def test_mxfp4_explicit_split_k(split_k):
-    m, n, k = 96, 384, 2048
+@pytest.mark.parametrize("m,n,k", [(96, 384, 2048), (288, 320, 2048)])
+def test_mxfp4_explicit_split_k(split_k, m, n, k):
+    """Single-CTA (M <= 128) and CTA-pair (M > 128) kernels with every split count."""
     a, sa, b, sb = _codes_case(m, n, k, seed=77)
     _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=False, split_k=split_k)
     _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=True, split_k=split_k)
+
+
+def test_single_cta_wide_tile_path():
+    """M <= 128 with N wide enough for the single-CTA 256-column tile."""
+    m, n, k = 96, 78848, 256
+    a, sa, b, sb = _codes_case(m, n, k, seed=78)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=False, split_k=1)
 
 
 def test_skinny_32x8192x8192_split_k_full():
@@ -154,7 +163,8 @@ def test_mlp_up_16384x28672x8192_bf16_sampled():
 # ------------------------------------------------------------ NVFP4 parity
 
 @pytest.mark.parametrize("m,n,k,split_k", [(128, 128, 256, 1), (256, 320, 1024, 1),
-                                           (160, 4096, 512, 1), (64, 512, 2048, 3)])
+                                           (160, 4096, 512, 1), (64, 512, 2048, 3),
+                                           (416, 352, 2048, 3)])
 def test_nvfp4_gemm_small(m, n, k, split_k):
     xa = synth.bf16_normal(m, k, 1.0, seed=m * 3 + k)
     xb = synth.bf16_normal(n, k, 1.0, seed=n * 5 + k)

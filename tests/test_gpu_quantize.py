@@ -14,10 +14,31 @@ MX, NV = mx.MX_FMT_MXFP4, mx.MX_FMT_NVFP4
 PLAIN, TILED = mx.MX_SCALE_PLAIN, mx.MX_SCALE_TCGEN05
 
 
+def _unpack(c):
+    c = np.asarray(c, np.uint8)
+    out = np.empty(c.shape[:-1] + (c.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = c & 0xF
+    out[..., 1::2] = c >> 4
+    return out
+
+
+def _explain(x, codes, ref_codes, scales, ref_scales, blk):
+    """Assertion text naming the first mismatching elements and their blocks."""
+    g, r = _unpack(codes), _unpack(ref_codes)
+    bad = np.argwhere(g != r)
+    lines = [f"{len(bad)} code mismatches"]
+    xf = synth.bf16_bits_to_f32(x)
+    for row, col in bad[:6]:
+        j = col // blk
+        lines.append(f"  [{row},{col}] x={xf[row, col]!r} gpu={g[row, col]} oracle={r[row, col]} "
+                     f"block_amax={np.abs(xf[row, j * blk:(j + 1) * blk]).max()!r}")
+    return "\n".join(lines)
+
+
 def _check_mx(x, layout=PLAIN, ld=None):
     codes, scales, _ = gpu_quantize(x, MX, layout, ld=ld)
     rc, rs = oracle.mx_quantize(x)
-    assert np.array_equal(codes, rc)
+    assert np.array_equal(codes, rc), _explain(x, codes, rc, scales, rs, 32)
     if layout == PLAIN:
         assert np.array_equal(scales.reshape(rs.shape), rs)
     else:
@@ -28,11 +49,14 @@ def _check_nv(x, layout=PLAIN, ld=None):
     codes, scales, s_t = gpu_quantize(x, NV, layout, ld=ld)
     rc, rs, rt = oracle.nvfp4_quantize(x)
     assert np.float32(s_t).view(np.uint32) == np.float32(rt).view(np.uint32)
-    assert np.array_equal(codes, rc)
     if layout == PLAIN:
-        assert np.array_equal(scales.reshape(rs.shape), rs)
+        bad_s = np.argwhere(scales.reshape(rs.shape) != rs)
     else:
-        assert np.array_equal(scales, oracle.scale_tile(rs))
+        bad_s = np.argwhere(scales != oracle.scale_tile(rs))
+    assert np.array_equal(codes, rc), (f"scale mismatches {len(bad_s)} first {bad_s[:4].tolist()}; "
+                                       + _explain(x, codes, rc, scales, rs, 16)
+                                       + f"\n  s_t={float(rt)!r}")
+    assert len(bad_s) == 0
 
 
 @pytest.mark.parametrize("rows,cols", [(1, 32), (3, 96), (33, 160), (128, 256), (129, 4096),
@@ -122,3 +146,39 @@ def test_scale_relayout_matches_oracle(rows, cols, fmt):
                                                         dtype=np.uint8)
     tiled = gpu_relayout(plain, rows, cols, fmt).cpu().numpy()
     assert np.array_equal(tiled, oracle.scale_tile(plain))
+
+
+def _finite_bf16_upto(limit: float) -> np.ndarray:
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = ((b >> 7) & 0xFF) != 0xFF
+    vals = synth.bf16_bits_to_f32(b)
+    return b[finite & (np.abs(vals) <= limit)]
+
+
+@pytest.mark.parametrize("tmax", [1.0, 3.0, 448.0, 1000.0, 1.5e-3, 7.5e5, 3e30, 2e-30])
+def test_nvfp4_quantize_every_bf16_under_many_divisors(tmax):
+    """Each finite BF16 value v (|v| <= block max) quantized in blocks whose
+    divisor E4M3(sb) * s_t takes many values: the per-block correctly rounded
+    division must agree byte for byte with the oracle's binary32 division."""
+    rows = []
+    for k in (0, 1, 3, 6, 9, 13):
+        for mant in (1.0, 1.375, 1.875):
+            bmax = tmax * 2.0 ** -k * mant / 1.875
+            bb = synth.f32_to_bf16_bits(np.array([bmax], np.float32))[0]
+            bval = float(synth.bf16_bits_to_f32(np.array([bb], np.uint16))[0])
+            v = _finite_bf16_upto(bval)
+            y = np.zeros((v.size, 16), np.uint16)
+            y[:, 0] = bb
+            y[:, 7] = v
+            rows.append(y)
+    x = np.concatenate(rows)
+    x[0, 15] = synth.f32_to_bf16_bits(np.array([tmax], np.float32))[0]
+    _check_nv(x, PLAIN)
+
+
+def test_leading_dim_not_32_byte_aligned():
+    """ld % 16 != 0 takes the 16-byte load path (x is only 16-byte aligned per row)."""
+    x = synth.bf16_normal(96, 512, 1.0, seed=31)
+    _check_mx(x, TILED, ld=520)
+    _check_nv(x, TILED, ld=520)
+    _check_nv(x, PLAIN, ld=528)
