@@ -131,18 +131,19 @@ int encode_out_map(CUtensorMap *tm, void *base, int64_t rows, int64_t cols, bool
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
 
-// Tensor map over a tile-ordered scale buffer viewed as [bytes / 16, 16]:
-// boxes of box_rows x 16 bytes (32 rows per 512-byte atom), zero past the end.
-int encode_scale_map(CUtensorMap *tm, const void *base, size_t bytes, int box_rows) {
+// Tensor map over a tile-ordered scale buffer viewed as [atoms, 512 bytes]
+// (32-bit elements, one 512-byte row per 128x4 atom): boxes of box_atoms
+// rows, zero past the end.
+int encode_scale_map(CUtensorMap *tm, const void *base, size_t bytes, int box_atoms) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return MX_ERR_CUDA;
-  const cuuint64_t dims[2] = {16u, static_cast<cuuint64_t>(bytes / 16)};
-  const cuuint64_t strides[1] = {16u};
-  const cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(bytes / 512)};
+  const cuuint64_t strides[1] = {512u};
+  const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_atoms)};
   const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MX_OK : MX_ERR_CUDA;
 }
@@ -195,9 +196,9 @@ int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *
   if (pair) {
     const int atoms_per_stage = fmt == MX_FMT_MXFP4 ? 2 : 4;
     if (encode_scale_map(&tmsa, a_scales, mx_scale_bytes(m, k, fmt, MX_SCALE_TCGEN05),
-                         atoms_per_stage * 32) != MX_OK ||
+                         atoms_per_stage) != MX_OK ||
         encode_scale_map(&tmsb, b_scales, mx_scale_bytes(n, k, fmt, MX_SCALE_TCGEN05),
-                         atoms_per_stage * 32) != MX_OK)
+                         atoms_per_stage) != MX_OK)
       return MX_ERR_CUDA;
   }
   const int box_cols = mx::gemm_out_box_cols(out_dtype == MX_OUT_FP32, splits);

@@ -12,7 +12,8 @@
 // Roles (320 threads per CTA, one CTA per SM, persistent over 256x256 tiles):
 //   warp 0      both CTAs: TMA producer of the CTA's A rows, B half and the
 //               stage's scale atoms (A's own, B's full 256 rows), all counted
-//               on the leader CTA's stage barrier (.cta_group::2).
+//               on the leader CTA's stage barrier (.cta_group::2); only the
+//               leader arrives on it, announcing the bytes of both CTAs.
 //   warp 1      both CTAs allocate the pair's tensor memory; in the leader,
 //               one lane issues tcgen05.cp of each CTA's scale atoms into its
 //               own tensor memory and the pair MMAs, and multicasts the
@@ -41,7 +42,7 @@ constexpr int kStageKBytes = 128;    // 256 FP4 codes of K per stage
 template <int FMT>
 struct PairCfg {
   static constexpr int kAtomsK = FMT == 0 ? 2 : 4;  // 4-scale atoms per stage along K
-  static constexpr int kStages = 5;
+  static constexpr int kStages = FMT == 0 ? 6 : 5;
   static constexpr int kABytes = 128 * kStageKBytes;
   static constexpr int kBBytes = 128 * kStageKBytes;  // this CTA's half of B
   static constexpr int kSfaBytes = kAtomsK * 512;
@@ -55,9 +56,9 @@ struct PairCfg {
   static constexpr int kStagingOff = kStages * kStageBytes;
   static constexpr int kBarBytes = 8 * (2 * kStages + 2) + 16;
   static constexpr int kStagingBufs =
-      (1024 + kStagingOff + 2 * kEpiWarps * kStagingBytes + kBarBytes <= 232448) ? 2 : 1;
+      (kStagingOff + 2 * kEpiWarps * kStagingBytes + kBarBytes <= 232448) ? 2 : 1;
   static constexpr int kBarOff = kStagingOff + kStagingBufs * kEpiWarps * kStagingBytes;
-  static constexpr int kSmemBytes = 1024 + kBarOff + kBarBytes;
+  static constexpr int kSmemBytes = kBarOff + kBarBytes;  // base is 1024-byte aligned
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -73,14 +74,16 @@ struct PairParams {
   int num_units;
 };
 
-// Unit -> (256-row tile of M, 256-column tile of N, split), in groups of 4
-// M tiles so that concurrently running pairs share panels in L2.
+// Unit -> (256-row tile of M, 256-column tile of N, split), in groups of 16
+// M tiles: the pairs running at once cover 16 M tiles x a few N tiles, so
+// A panels stay in L2 across waves and each B panel is read from DRAM once
+// per group.
 __device__ __forceinline__ void decode_unit(const PairParams &p, int u, int &pm, int &nt,
                                             int &sp) {
   const int tiles = p.pm_tiles * p.n_tiles;
   sp = u / tiles;
   const int t = u - sp * tiles;
-  constexpr int kGroup = 4;
+  constexpr int kGroup = 16;
   const int per_group = kGroup * p.n_tiles;
   const int g = t / per_group;
   const int first = g * kGroup;
@@ -105,11 +108,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = PairCfg<FMT>;
   constexpr int kBoxCols = OUT_F32 ? 16 : 32;
   constexpr int kBoxes = 128 / kBoxCols;  // per epilogue warp and tile
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The 128-byte swizzle needs 1024-byte aligned stages; were the dynamic
+  // shared memory ever placed otherwise, report it and leave (every thread
+  // of both CTAs takes this branch, nothing has been issued yet).
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusTimeout);
+    return;
+  }
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-  uint64_t *full = bars;                   // leader: 2 arrivals (one per CTA) + bytes
+  uint64_t *full = bars;                   // leader: its arrival + both CTAs' bytes
   uint64_t *empty = bars + C::kStages;     // both: the leader's stage commit
   uint64_t *tfull = bars + 2 * C::kStages; // both: the leader's accumulator commit
   uint64_t *tempty = tfull + 1;            // leader: 8 epilogue warps x 2 CTAs
@@ -123,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 2);
+      mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(tfull), 1);
@@ -168,19 +176,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t st = smem_u32(smem + s * C::kStageBytes);
         const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-        if (leader)
-          mbar_arrive_expect_tx(smem_u32(&full[s]), C::kStageBytes);
-        else
-          mbar_arrive_expect_tx_cluster(fb, C::kStageBytes);
+        // The leader announces the bytes of both CTAs; the peer's loads only
+        // complete bytes on the leader's barrier.  (A peer-side remote arrive
+        // would be a cluster-scope release, which waits for this thread's
+        // earlier loads and serialises the peer's stages.)
+        if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::kStageBytes);
         tma_load_2d_pair(st, &tmap_a, ks * kStageKBytes, row_a, fb);
         tma_load_2d_pair(st + C::kABytes, &tmap_b, ks * kStageKBytes, row_b, fb);
-        // scale atoms: rows of 16 bytes, 32 rows per atom (zero past the end)
-        tma_load_2d_pair(st + C::kABytes + C::kBBytes, &tmap_sfa, 0,
-                         (sfa_row + ks * C::kAtomsK) * 32, fb);
+        // scale atoms: one 512-byte row per atom (zero past the end)
+        tma_load_2d_pair(st + C::kABytes + C::kBBytes, &tmap_sfa, 0, sfa_row + ks * C::kAtomsK,
+                         fb);
 #pragma unroll
         for (int ra = 0; ra < 2; ++ra)
           tma_load_2d_pair(st + C::kABytes + C::kBBytes + C::kSfaBytes + ra * C::kAtomsK * 512,
-                           &tmap_sfb, 0, ((nt * 2 + ra) * p.katoms + ks * C::kAtomsK) * 32, fb);
+                           &tmap_sfb, 0, (nt * 2 + ra) * p.katoms + ks * C::kAtomsK, fb);
       }
     }
     // Wait (bounded) until the leader has released every stage this CTA
