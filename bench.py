@@ -449,21 +449,31 @@ def cpu_baseline(name, host, target_s):
 
 # --------------------------------------------------------------------- traffic record
 
-def kernel_source_hash():
+# Source files that define the kernels of each call of the step.
+CALL_SOURCES = {
+    "gemm": ["gemm.cu", "gemm_pair.cu", "mx_device.cuh", "mx_internal.h"],
+    "quantize_a": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
+    "quantize_w": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
+}
+
+
+def kernel_source_hash(call):
+    """Short hash of the sources of a call's kernels (ties an ncu record to them)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp4_bf16_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(CALL_SOURCES[call]):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(name, call):
-    """DRAM bytes per launch from the committed ncu summary, if it is current."""
+    """DRAM bytes per launch from the committed ncu summary, if its kernels
+    have not changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or call not in CALL_SOURCES:
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(call)
     for line in open(path):
         kv = dict(re.findall(r"(\w+)=(\S+)", line))
         if kv.get("workload") == name and kv.get("call") == call and kv.get("source") == src:
