@@ -11,4 +11,5 @@ from ._binding import (  # noqa: F401
     MX_ERR_WORKSPACE, MX_FMT_MXFP4, MX_FMT_NVFP4, MX_LAYOUT_TN, MX_OK, MX_OUT_BF16, MX_OUT_FP32,
     MX_SCALE_PLAIN, MX_SCALE_TCGEN05, MXError, lib, mx_available, mx_device_status,
     mx_error_string, mx_gemm_workspace_bytes, mx_quantize_bf16, mx_quantize_workspace_bytes,
-    mx_scale_bytes, mx_scale_relayout, mx_selftest_wait_timeout, mxfp4_gemm, nvfp4_gemm)
+    mx_scale_bytes, mx_scale_relayout, mx_selftest_wait_timeout, mxfp4_gemm, nvfp4_gemm,
+    mxfp4_gemm_static_workspace, MX_STATIC_WORKSPACE_BYTES)

@@ -33,6 +33,7 @@ MX_SCALE_TCGEN05 = 1
 MX_LAYOUT_TN = 0
 MX_OUT_BF16 = 0
 MX_OUT_FP32 = 1
+MX_STATIC_WORKSPACE_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gemm.restype = i32
         L.nvfp4_gemm.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp, sz,
                                  vp]
+        L.mxfp4_gemm_static_workspace.restype = i32
+        L.mxfp4_gemm_static_workspace.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32,
+                                                  i32, vp]
         L.mx_device_status.restype = i32
         L.mx_device_status.argtypes = [vp]
         L.mx_selftest_wait_timeout.restype = i32
@@ -166,6 +170,14 @@ def nvfp4_gemm(a_codes, a_scales, b_codes, b_scales, a_tensor_scale, b_tensor_sc
         _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(a_tensor_scale),
         _ptr(b_tensor_scale), _ptr(d), m, n, k, layout, out_dtype, split_k, _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+def mxfp4_gemm_static_workspace(a_codes, a_scales, b_codes, b_scales, d, m, n, k,
+                                layout=MX_LAYOUT_TN, out_dtype=MX_OUT_BF16, split_k=0,
+                                stream=None):
+    return _check("mxfp4_gemm_static_workspace", lib().mxfp4_gemm_static_workspace(
+        _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(d), m, n, k, layout,
+        out_dtype, split_k, _stream(stream)))
 
 
 def mx_device_status(stream=None) -> int:

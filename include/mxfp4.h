@@ -156,6 +156,30 @@ int nvfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
                void *d, int64_t m, int64_t n, int64_t k, int layout, int out_dtype, int split_k,
                void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the fixed device scratch array of mxfp4_gemm_static_workspace. */
+#define MX_STATIC_WORKSPACE_BYTES (16u << 20) /* 16 MiB */
+
+/* mxfp4_gemm without a caller-provided workspace, for callers that cannot
+ * allocate device memory (for instance a plugin inside a host program that
+ * owns all device memory and forbids it cudaMalloc, or a path where a fresh
+ * allocation is not allowed).  The pages have no counterpart of this entry
+ * point; it is this library's own addition.
+ * Arguments and results are those of mxfp4_gemm.  The split-K partial sums go
+ * to a fixed array of MX_STATIC_WORKSPACE_BYTES in the library's device image
+ * (set up by CUDA on each device that loads it and kept until the process
+ * exits); nothing is allocated by the caller or the library.  A shape and
+ * split count whose partials (mx_gemm_workspace_bytes) exceed that size is
+ * rejected with MX_ERR_WORKSPACE before anything is launched.
+ * The first call that uses split-K on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture.  All calls on a device share the array and it keeps the
+ * last call's contents: calls whose kernels overlap on the GPU (for instance
+ * on different streams) race on it, so order them on one stream.  Nothing in
+ * it needs to start at zero: each call writes every partial it reads. */
+int mxfp4_gemm_static_workspace(const void *a_codes, const void *a_scales, const void *b_codes,
+                                const void *b_scales, void *d, int64_t m, int64_t n, int64_t k,
+                                int layout, int out_dtype, int split_k, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns MX_OK, MX_ERR_DEVICE_TIMEOUT when a kernel's
  * bounded wait (on a TMA or tensor-core completion barrier) ran out and the
