@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Set-up above overlaps the previous kernel; global memory only from here.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -366,6 +369,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
                                                             int splits, int64_t mn, void *out,
                                                             int out_fp32, const float *a_ts,
                                                             const float *b_ts) {
+  griddep_launch_dependents();
+  griddep_wait();
   float alpha = 1.0f;
   if (a_ts != nullptr) alpha = __fmul_rn(*a_ts, *b_ts);
   const int64_t n4 = mn >> 2;
@@ -438,9 +443,9 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.partial = g.split_k > 1 ? 1 : 0;
   p.num_units = p.m_tiles * p.n_tiles * p.splits;
   const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
-  gemm_kernel<FMT, BN, OUT_F32>
-      <<<grid, kThreads, C::kSmemBytes, s>>>(*g.tmap_a, *g.tmap_b, *g.tmap_d, p);
-  e = cudaGetLastError();
+  e = launch_pdl(gemm_kernel<FMT, BN, OUT_F32>, dim3(grid), dim3(kThreads), C::kSmemBytes, s,
+                 *g.tmap_a, *g.tmap_b, *g.tmap_d, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || g.split_k <= 1) return e;
   return launch_splitk_reduce(g, s);
 }
@@ -493,10 +498,12 @@ cudaError_t launch_splitk_reduce(const GemmArgs &g, cudaStream_t s) {
   const int64_t mn = g.m * g.n;
   int64_t rgrid = (mn / 4 + 255) / 256;
   if (rgrid > 4 * g.num_sms) rgrid = 4 * g.num_sms;
-  splitk_reduce_kernel<<<static_cast<unsigned>(rgrid), 256, 0, s>>>(
-      g.workspace, g.split_k, mn, g.d, g.out_fp32, g.fmt == 1 ? g.a_ts : nullptr,
-      g.fmt == 1 ? g.b_ts : nullptr);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(
+      splitk_reduce_kernel, dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s,
+      static_cast<const float *>(g.workspace), g.split_k, mn, g.d, g.out_fp32,
+      g.fmt == 1 ? g.a_ts : static_cast<const float *>(nullptr),
+      g.fmt == 1 ? g.b_ts : static_cast<const float *>(nullptr));
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t s) {

@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Set-up above overlaps the previous kernel; global memory only from here.
+  griddep_launch_dependents();
+  griddep_wait();
   const int cluster = static_cast<int>(cluster_id_x());
   const int nclusters = static_cast<int>(num_clusters_x());
 
@@ -360,11 +363,13 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
@@ -396,6 +401,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.num_units = p.pm_tiles * p.n_tiles * p.splits;
   const int clusters = p.num_units < max_clusters[dev] ? p.num_units : max_clusters[dev];
   cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.numAttrs = 2;  // cluster shape + programmatic stream serialization
   e = cudaLaunchKernelEx(&cfg, kernel, *g.tmap_a, *g.tmap_b, *g.tmap_sfa, *g.tmap_sfb, *g.tmap_d,
                          p);
   if (e != cudaSuccess) return e;

@@ -28,6 +28,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch: every kernel of the library is launched so
+// that the next kernel in the stream may start while this one finishes.  A
+// kernel lets its dependents launch as soon as all of its CTAs have started
+// (griddep_launch_dependents at the top), and waits for its predecessor to
+// complete, memory included, before touching any global memory the
+// predecessor may read or write (griddep_wait).
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

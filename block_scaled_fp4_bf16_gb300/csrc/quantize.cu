@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(
     const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, int64_t ld,
     uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, uint32_t total,
     FastDiv kbdiv, uint32_t katoms) {
+  griddep_launch_dependents();
+  griddep_wait();
   const uint32_t b = blockIdx.x * kThreads + threadIdx.x;
   if (b >= total) return;
   const uint32_t kb = kbdiv.d;
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const uint16_t *__
                                                               int64_t ld, uint32_t total,
                                                               FastDiv kbdiv,
                                                               uint32_t *__restrict__ partials) {
+  griddep_launch_dependents();
+  griddep_wait();
   uint32_t m = 0;
   for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < total; b += gridDim.x * kThreads) {
     const uint32_t r = fast_div(b, kbdiv);
@@ -274,6 +278,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
     uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, uint32_t total,
     FastDiv kbdiv, uint32_t katoms, const uint32_t *__restrict__ partials,
     float *__restrict__ tensor_scale) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ uint32_t warp_max[kThreads / 32];
   __shared__ float s_t_shared;
   {
@@ -334,6 +340,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
 __global__ void __launch_bounds__(kThreads) scale_relayout_kernel(
     const uint8_t *__restrict__ plain, int64_t rows, int64_t kb, uint8_t *__restrict__ tiled,
     int64_t total) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t katoms = (kb + 3) >> 2;
   for (int64_t o = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; o < total;
        o += static_cast<int64_t>(gridDim.x) * kThreads) {
@@ -358,11 +366,12 @@ cudaError_t launch_mx_quantize(const QuantizeArgs &a, cudaStream_t s) {
   const uint32_t total = rows_pad * kb;
   const uint32_t grid = (total + kThreads - 1) / kThreads;
   auto kern = wide_ok(a.x, a.ld) ? mx_quantize_kernel<true> : mx_quantize_kernel<false>;
-  kern<<<grid, kThreads, 0, s>>>(
-      static_cast<const uint16_t *>(a.x), static_cast<uint32_t>(a.rows),
-      static_cast<uint32_t>(a.cols), a.ld, static_cast<uint8_t *>(a.codes),
-      static_cast<uint8_t *>(a.scales), a.tiled, total, make_fastdiv(kb), (kb + 3) / 4);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(
+      kern, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint16_t *>(a.x),
+      static_cast<uint32_t>(a.rows), static_cast<uint32_t>(a.cols), a.ld,
+      static_cast<uint8_t *>(a.codes), static_cast<uint8_t *>(a.scales), a.tiled, total,
+      make_fastdiv(kb), (kb + 3) / 4);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_nvfp4_quantize(const QuantizeArgs &a, cudaStream_t s) {
@@ -371,20 +380,21 @@ cudaError_t launch_nvfp4_quantize(const QuantizeArgs &a, cudaStream_t s) {
   const uint32_t real_total = static_cast<uint32_t>(a.rows) * kb;
   const bool wide = wide_ok(a.x, a.ld);
   auto amax_kern = wide ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>;
-  amax_kern<<<kAmaxPartials, kThreads, 0, s>>>(static_cast<const uint16_t *>(a.x), a.ld,
-                                               real_total, kbdiv, a.partials);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(amax_kern, dim3(kAmaxPartials), dim3(kThreads), 0, s,
+                             static_cast<const uint16_t *>(a.x), a.ld, real_total, kbdiv,
+                             a.partials);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const uint32_t rows_pad = static_cast<uint32_t>(a.tiled ? (a.rows + 127) / 128 * 128 : a.rows);
   const uint32_t total = rows_pad * kb;
   const uint32_t grid = (total + kThreads - 1) / kThreads;
   auto quant_kern = wide ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>;
-  quant_kern<<<grid, kThreads, 0, s>>>(
-      static_cast<const uint16_t *>(a.x), static_cast<uint32_t>(a.rows),
-      static_cast<uint32_t>(a.cols), a.ld, static_cast<uint8_t *>(a.codes),
-      static_cast<uint8_t *>(a.scales), a.tiled, total, kbdiv, (kb + 3) / 4, a.partials,
-      a.tensor_scale);
-  return cudaGetLastError();
+  e = launch_pdl(quant_kern, dim3(grid), dim3(kThreads), 0, s,
+                 static_cast<const uint16_t *>(a.x), static_cast<uint32_t>(a.rows),
+                 static_cast<uint32_t>(a.cols), a.ld, static_cast<uint8_t *>(a.codes),
+                 static_cast<uint8_t *>(a.scales), a.tiled, total, kbdiv, (kb + 3) / 4,
+                 static_cast<const uint32_t *>(a.partials), a.tensor_scale);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
@@ -392,9 +402,11 @@ cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, v
   const int64_t total = (rows + 127) / 128 * 128 * ((kb + 3) / 4 * 4);
   int64_t grid = (total + kThreads - 1) / kThreads;
   if (grid > 65536) grid = 65536;
-  scale_relayout_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
-      static_cast<const uint8_t *>(plain), rows, kb, static_cast<uint8_t *>(tiled), total);
-  return cudaGetLastError();
+  const cudaError_t e =
+      launch_pdl(scale_relayout_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                 static_cast<const uint8_t *>(plain), rows, kb, static_cast<uint8_t *>(tiled),
+                 total);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mx
