@@ -168,8 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (the whole warp waits; one elected lane issues the copies)
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
@@ -183,22 +184,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = k0; ks < k1; ++ks, ++it) {
         const uint32_t s = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort, p.status)) {
+        if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u, abort, p.status)) {
           ok = false;
           break;
         }
-        uint8_t *st = smem + s * C::kStageBytes;
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, bytes);
-        tma_load_2d(smem_u32(st), &tmap_a, ks * kStageKBytes, mt * kBM, fb);
-        tma_load_2d(smem_u32(st + C::kABytes), &tmap_b, ks * kStageKBytes, nt * BN, fb);
-        bulk_load(smem_u32(st + C::kABytes + C::kBBytes),
-                  p.sfa + (static_cast<size_t>(mt) * p.sfa_katoms + ks * C::kAtomsK) * 512,
-                  C::kSfaBytes, fb);
-        for (int ra = 0; ra < rb_valid; ++ra)
-          bulk_load(smem_u32(st + C::kABytes + C::kBBytes + C::kSfaBytes + ra * C::kAtomsK * 512),
-                    p.sfb + (static_cast<size_t>(rb0 + ra) * p.sfb_katoms + ks * C::kAtomsK) * 512,
-                    C::kAtomsK * 512, fb);
+        if (elect_one()) {
+          uint8_t *st = smem + s * C::kStageBytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_2d(smem_u32(st), &tmap_a, ks * kStageKBytes, mt * kBM, fb);
+          tma_load_2d(smem_u32(st + C::kABytes), &tmap_b, ks * kStageKBytes, nt * BN, fb);
+          bulk_load(smem_u32(st + C::kABytes + C::kBBytes),
+                    p.sfa + (static_cast<size_t>(mt) * p.sfa_katoms + ks * C::kAtomsK) * 512,
+                    C::kSfaBytes, fb);
+          for (int ra = 0; ra < rb_valid; ++ra)
+            bulk_load(smem_u32(st + C::kABytes + C::kBBytes + C::kSfaBytes + ra * C::kAtomsK * 512),
+                      p.sfb + (static_cast<size_t>(rb0 + ra) * p.sfb_katoms + ks * C::kAtomsK) * 512,
+                      C::kAtomsK * 512, fb);
+        }
+        __syncwarp();
       }
     }
     if (!ok) {
@@ -207,8 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t j = first; j < it; ++j)
         mbar_drain(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1u);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // (the whole warp waits; one elected lane issues the tcgen05 operations)
     uint32_t it = 0, tile = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++tile) {
@@ -218,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k1 = min(k0 + p.stages_per_split, p.k_stages);
       const uint32_t acc = tile % C::kNumAcc;
       const uint32_t aph = (tile / C::kNumAcc) & 1u;
-      if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1u, abort, p.status)) {
+      if (!mbar_wait_warp(smem_u32(&tempty[acc]), aph ^ 1u, abort, p.status)) {
         ok = false;
         break;
       }
@@ -227,44 +232,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = k0; ks < k1; ++ks, ++it) {
         const uint32_t s = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&full[s]), ph, abort, p.status)) {
+        if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
-        const uint32_t sfb_s = sfa_s + C::kSfaBytes;
-        const uint32_t sfa_t = tmem + C::kSfCol + s * C::kSfSetCols;
-        const uint32_t sfb_t = sfa_t + C::kSfaCols;
-#pragma unroll
-        for (int a = 0; a < C::kAtomsK; ++a)
-          tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_scale_block(sfa_s + a * 512));
-#pragma unroll
-        for (int ra = 0; ra < C::kRowAtomsB; ++ra)
+        if (elect_one()) {
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
+          const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+          const uint32_t sfa_t = tmem + C::kSfCol + s * C::kSfSetCols;
+          const uint32_t sfb_t = sfa_t + C::kSfaCols;
 #pragma unroll
           for (int a = 0; a < C::kAtomsK; ++a)
-            tc_cp_32x128b_warpx4(sfb_t + a * (BN / 32) + ra * 4,
-                                 smem_desc_scale_block(sfb_s + (ra * C::kAtomsK + a) * 512));
-        const uint64_t a_desc = smem_desc_sw128_kmajor(st);
-        const uint64_t b_desc = smem_desc_sw128_kmajor(st + C::kABytes);
+            tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_scale_block(sfa_s + a * 512));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // K = 64 per MMA = 32 bytes along the swizzled row (>> 4 = 2).
-          const int ka = FMT == 0 ? (kk >> 1) : kk;
-          const uint32_t sf_id = FMT == 0 ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
-          tc_mma_block_scaled<FMT>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk,
-                                   mma_idesc<FMT>(kBM, BN, sf_id), sfa_t + ka * 4,
-                                   sfb_t + ka * (BN / 32), (ks > k0 || kk > 0) ? 1u : 0u);
+          for (int ra = 0; ra < C::kRowAtomsB; ++ra)
+#pragma unroll
+            for (int a = 0; a < C::kAtomsK; ++a)
+              tc_cp_32x128b_warpx4(sfb_t + a * (BN / 32) + ra * 4,
+                                   smem_desc_scale_block(sfb_s + (ra * C::kAtomsK + a) * 512));
+          const uint64_t a_desc = smem_desc_sw128_kmajor(st);
+          const uint64_t b_desc = smem_desc_sw128_kmajor(st + C::kABytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // K = 64 per MMA = 32 bytes along the swizzled row (>> 4 = 2).
+            const int ka = FMT == 0 ? (kk >> 1) : kk;
+            const uint32_t sf_id = FMT == 0 ? static_cast<uint32_t>(kk & 1) * 2u : 0u;
+            tc_mma_block_scaled<FMT>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk,
+                                     mma_idesc<FMT>(kBM, BN, sf_id), sfa_t + ka * 4,
+                                     sfb_t + ka * (BN / 32), (ks > k0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[s]));
         }
-        tc_commit(smem_u32(&empty[s]));
+        __syncwarp();
       }
       if (!ok) break;
-      tc_commit(smem_u32(&tfull[acc]));
+      if (elect_one()) tc_commit(smem_u32(&tfull[acc]));
+      __syncwarp();
     }
     if (!ok) {
       // Let the MMAs already issued finish before tensor memory is freed.
-      tc_commit(smem_u32(&tfull[0]));
+      if (elect_one()) tc_commit(smem_u32(&tfull[0]));
+      __syncwarp();
       mbar_drain(smem_u32(&tfull[0]), 0u);
       mbar_drain(smem_u32(&tfull[0]), 1u);
     }

@@ -158,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cluster = static_cast<int>(cluster_id_x());
   const int nclusters = static_cast<int>(num_clusters_x());
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (the whole warp waits; one elected lane issues the copies)
     uint32_t it = 0;
     bool ok = true;
     for (int u = cluster; u < p.num_units && ok; u += nclusters) {
@@ -173,26 +174,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = k0; ks < k1; ++ks, ++it) {
         const uint32_t s = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort, p.status)) {
+        if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u, abort, p.status)) {
           ok = false;
           break;
         }
-        const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-        // The leader announces the bytes of both CTAs; the peer's loads only
-        // complete bytes on the leader's barrier.  (A peer-side remote arrive
-        // would be a cluster-scope release, which waits for this thread's
-        // earlier loads and serialises the peer's stages.)
-        if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::kStageBytes);
-        tma_load_2d_pair(st, &tmap_a, ks * kStageKBytes, row_a, fb);
-        tma_load_2d_pair(st + C::kABytes, &tmap_b, ks * kStageKBytes, row_b, fb);
-        // scale atoms: one 512-byte row per atom (zero past the end)
-        tma_load_2d_pair(st + C::kABytes + C::kBBytes, &tmap_sfa, 0, sfa_row + ks * C::kAtomsK,
-                         fb);
+        if (elect_one()) {
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+          // The leader announces the bytes of both CTAs; the peer's loads only
+          // complete bytes on the leader's barrier.  (A peer-side remote arrive
+          // would be a cluster-scope release, which waits for this thread's
+          // earlier loads and serialises the peer's stages.)
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::kStageBytes);
+          tma_load_2d_pair(st, &tmap_a, ks * kStageKBytes, row_a, fb);
+          tma_load_2d_pair(st + C::kABytes, &tmap_b, ks * kStageKBytes, row_b, fb);
+          // scale atoms: one 512-byte row per atom (zero past the end)
+          tma_load_2d_pair(st + C::kABytes + C::kBBytes, &tmap_sfa, 0, sfa_row + ks * C::kAtomsK,
+                           fb);
 #pragma unroll
-        for (int ra = 0; ra < 2; ++ra)
-          tma_load_2d_pair(st + C::kABytes + C::kBBytes + C::kSfaBytes + ra * C::kAtomsK * 512,
-                           &tmap_sfb, 0, (nt * 2 + ra) * p.katoms + ks * C::kAtomsK, fb);
+          for (int ra = 0; ra < 2; ++ra)
+            tma_load_2d_pair(st + C::kABytes + C::kBBytes + C::kSfaBytes + ra * C::kAtomsK * 512,
+                             &tmap_sfb, 0, (nt * 2 + ra) * p.katoms + ks * C::kAtomsK, fb);
+        }
+        __syncwarp();
       }
     }
     // Wait (bounded) until the leader has released every stage this CTA
@@ -200,8 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t first = it > static_cast<uint32_t>(C::kStages) ? it - C::kStages : 0u;
     for (uint32_t j = first; j < it; ++j)
       mbar_drain(smem_u32(&empty[j % C::kStages]), (j / C::kStages) & 1u);
-  } else if (warp == 1 && lane == 0 && leader) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------ MMA issuer
+    // (the whole warp waits; one elected lane issues the tcgen05 operations)
     uint32_t it = 0, tile = 0;
     bool ok = true;
     const uint32_t idesc0 = mma_idesc<FMT>(256, 256, 0);
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_unit(p, u, pm, nt, sp);
       const int k0 = sp * p.stages_per_split;
       const int k1 = min(k0 + p.stages_per_split, p.k_stages);
-      if (!mbar_wait(smem_u32(tempty), (tile & 1u) ^ 1u, abort, p.status)) {
+      if (!mbar_wait_warp(smem_u32(tempty), (tile & 1u) ^ 1u, abort, p.status)) {
         ok = false;
         break;
       }
@@ -219,43 +224,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = k0; ks < k1; ++ks, ++it) {
         const uint32_t s = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1u;
-        if (!mbar_wait(smem_u32(&full[s]), ph, abort, p.status)) {
+        if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
-        const uint32_t sfb_s = sfa_s + C::kSfaBytes;
-        const uint32_t sfa_t = tmem + C::kSfCol + s * C::kSfSetCols;
-        const uint32_t sfb_t = sfa_t + C::kAtomsK * 4;
-#pragma unroll
-        for (int a = 0; a < C::kAtomsK; ++a)
-          tc_cp_pair_32x128b_warpx4(sfa_t + a * 4, smem_desc_scale_block(sfa_s + a * 512));
-#pragma unroll
-        for (int ra = 0; ra < 2; ++ra)
+        if (elect_one()) {
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
+          const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+          const uint32_t sfa_t = tmem + C::kSfCol + s * C::kSfSetCols;
+          const uint32_t sfb_t = sfa_t + C::kAtomsK * 4;
 #pragma unroll
           for (int a = 0; a < C::kAtomsK; ++a)
-            tc_cp_pair_32x128b_warpx4(sfb_t + a * 8 + ra * 4,
-                                      smem_desc_scale_block(sfb_s + (ra * C::kAtomsK + a) * 512));
-        const uint64_t a_desc = smem_desc_sw128_kmajor(st);
-        const uint64_t b_desc = smem_desc_sw128_kmajor(st + C::kABytes);
+            tc_cp_pair_32x128b_warpx4(sfa_t + a * 4, smem_desc_scale_block(sfa_s + a * 512));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int ka = FMT == 0 ? (kk >> 1) : kk;
-          const uint32_t idesc = (FMT == 0 && (kk & 1)) ? idesc2 : idesc0;
-          tc_mma_pair_block_scaled<FMT>(tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
-                                        sfa_t + ka * 4, sfb_t + ka * 8,
-                                        (ks > k0 || kk > 0) ? 1u : 0u);
+          for (int ra = 0; ra < 2; ++ra)
+#pragma unroll
+            for (int a = 0; a < C::kAtomsK; ++a)
+              tc_cp_pair_32x128b_warpx4(sfb_t + a * 8 + ra * 4,
+                                        smem_desc_scale_block(sfb_s + (ra * C::kAtomsK + a) * 512));
+          const uint64_t a_desc = smem_desc_sw128_kmajor(st);
+          const uint64_t b_desc = smem_desc_sw128_kmajor(st + C::kABytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int ka = FMT == 0 ? (kk >> 1) : kk;
+            const uint32_t idesc = (FMT == 0 && (kk & 1)) ? idesc2 : idesc0;
+            tc_mma_pair_block_scaled<FMT>(tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+                                          sfa_t + ka * 4, sfb_t + ka * 8,
+                                          (ks > k0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_mc(smem_u32(&empty[s]), 0x3);
         }
-        tc_commit_pair_mc(smem_u32(&empty[s]), 0x3);
+        __syncwarp();
       }
       if (!ok) break;
-      tc_commit_pair_mc(smem_u32(tfull), 0x3);
+      if (elect_one()) tc_commit_pair_mc(smem_u32(tfull), 0x3);
+      __syncwarp();
     }
     if (!ok) {
       // Let the MMAs already issued finish before tensor memory is freed.
-      tc_commit_pair_mc(smem_u32(tfull), 0x3);
+      if (elect_one()) tc_commit_pair_mc(smem_u32(tfull), 0x3);
+      __syncwarp();
       mbar_drain(smem_u32(tfull), 0u);
       mbar_drain(smem_u32(tfull), 1u);
     }

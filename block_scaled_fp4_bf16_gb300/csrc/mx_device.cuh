@@ -97,6 +97,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The producer and MMA roles run their loops with the whole warp converged:
+// all lanes wait on the barriers together and one elected lane issues the
+// TMA copies and tcgen05 operations.  (Measured on GB300: when one lane runs
+// the MMA loop alone, every barrier wait in it stalls the issue of the next
+// stage's MMAs by about 180 cycles, a third of a stage of 256 K; with the
+// warp converged the waits cost nothing and the tensor core stays busy.)
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// mbar_wait by every lane of a converged warp; true only if it succeeded in
+// all of them, so the warp takes the same branch afterwards.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile uint32_t *abort, uint32_t *status) {
+  const bool ok = mbar_wait(bar, parity, abort, status);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Clean-up wait: bounded, ignores the abort flag, records nothing.
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
