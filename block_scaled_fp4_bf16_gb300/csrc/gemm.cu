@@ -164,9 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Set-up above overlaps the previous kernel; global memory only from here.
+  // Set-up above overlaps the previous kernel.  Each role waits for it
+  // (griddep_wait) just before its own first global-memory access: the
+  // producer before its first load, the epilogue before it reads the
+  // tensor scales or stores; the MMA warp touches no global memory.
   griddep_launch_dependents();
-  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        if (it == 0) griddep_wait();
         if (elect_one()) {
           uint8_t *st = smem + s * C::kStageBytes;
           const uint32_t fb = smem_u32(&full[s]);
@@ -280,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
+    griddep_wait();
     const int q = warp & 3;  // this warp may access tensor-memory lanes 32q..32q+31
     uint8_t *stage_base = smem + C::kStagingOff + (warp - 2) * C::kStagingBufs * kStagingBytes;
     uint32_t nbox = 0;  // boxes this warp has stored (selects the staging buffer)
@@ -360,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_group0();
+    // Before the CTA (and its staging buffers) goes away the stores must
+    // have read their sources; their global writes complete with the grid.
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
 

@@ -52,11 +52,17 @@ struct PairCfg {
   static constexpr int kSfCol = 256;  // after the 256-column accumulator
   static constexpr int kTmemCols = 512;
   static_assert(kSfCol + kStages * kSfSetCols <= kTmemCols, "tensor memory budget");
+  // the last tile's output boxes are staged in the idle stage ring
+  static_assert(kEpiWarps * 8 * 2048 <= kStages * kStageBytes, "ring holds the last tile's boxes");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static constexpr int kStagingOff = kStages * kStageBytes;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2) + 16;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 3) + 16;
+  // staging buffers per epilogue warp: as many (up to 3) as shared memory
+  // allows, so that a warp's box stores overlap instead of waiting in turn
   static constexpr int kStagingBufs =
-      (kStagingOff + 2 * kEpiWarps * kStagingBytes + kBarBytes <= 232448) ? 2 : 1;
+      (kStagingOff + 3 * kEpiWarps * kStagingBytes + kBarBytes <= 232448)   ? 3
+      : (kStagingOff + 2 * kEpiWarps * kStagingBytes + kBarBytes <= 232448) ? 2
+                                                                            : 1;
   static constexpr int kBarOff = kStagingOff + kStagingBufs * kEpiWarps * kStagingBytes;
   static constexpr int kSmemBytes = kBarOff + kBarBytes;  // base is 1024-byte aligned
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -120,8 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *full = bars;                   // leader: its arrival + both CTAs' bytes
   uint64_t *empty = bars + C::kStages;     // both: the leader's stage commit
   uint64_t *tfull = bars + 2 * C::kStages; // both: the leader's accumulator commit
-  uint64_t *tempty = tfull + 1;            // leader: 8 epilogue warps x 2 CTAs
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 1);
+  uint64_t *tempty = tfull + 1;            // leader: one arrival per CTA
+  uint64_t *eload = tempty + 1;            // both: the CTA's 8 epilogue warps
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(eload + 1);
   volatile uint32_t *abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -135,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(tfull), 1);
-    mbar_init(smem_u32(tempty), 2 * kEpiWarps);
+    mbar_init(smem_u32(tempty), 2);
+    mbar_init(smem_u32(eload), kEpiWarps);
     *abort = 0u;
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
@@ -152,9 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Set-up above overlaps the previous kernel; global memory only from here.
+  // Set-up above overlaps the previous kernel.  Each role waits for it
+  // (griddep_wait) just before its own first global-memory access: the
+  // producer before its first load, the epilogue before it reads the
+  // tensor scales or stores; the MMA warp touches no global memory.
   griddep_launch_dependents();
-  griddep_wait();
   const int cluster = static_cast<int>(cluster_id_x());
   const int nclusters = static_cast<int>(num_clusters_x());
 
@@ -178,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        if (it == 0) griddep_wait();
         if (elect_one()) {
           const uint32_t st = smem_u32(smem + s * C::kStageBytes);
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
@@ -271,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
+    griddep_wait();
     const int q = warp & 3;          // tensor-memory lane quarter of this warp
     const int h = (warp - 2) >> 2;   // which 128 of the 256 columns
     uint8_t *stage_base = smem + C::kStagingOff + (warp - 2) * C::kStagingBufs * kStagingBytes;
@@ -291,15 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
       tc_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
       tc_wait_ld();
-      // The accumulator is in registers: release it to the leader's MMA warp.
+      // The accumulator is in registers.  The CTA's epilogue warps meet
+      // (bounded) before any of them starts converting, so that no warp's
+      // release waits behind another warp's conversion work; then one thread
+      // per CTA hands the accumulator back to the leader's MMA warp.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0) mbar_arrive(smem_u32(eload));
+      if (!mbar_wait_warp(smem_u32(eload), tile & 1u, abort, p.status)) break;
+      if (warp == 2 && lane == 0) {
         if (leader)
           mbar_arrive(smem_u32(tempty));
         else
-          mbar_arrive_cluster(tempty_leader);
+          mbar_arrive_cluster_relaxed(tempty_leader);
       }
+      // After the last tile's accumulator is full the producer has issued
+      // its final load and every stage has been consumed, so the stage ring
+      // is idle: that tile's boxes are staged there, one buffer each, and
+      // none of them waits for an earlier store to release its buffer.
+      const bool last = u + nclusters >= p.num_units;
       const int row0 = pm * 256 + static_cast<int>(rank) * 128 + q * 32;
       const bool rows_ok = row0 < p.m;  // M % 32 == 0: a warp's 32 rows are all in or all out
       const int y = p.partial ? sp * p.m + row0 : row0;
@@ -307,10 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kBoxes; ++c) {
         const int col0 = nt * 256 + h * 128 + c * kBoxCols;
         if (!rows_ok || col0 >= p.n) continue;  // warp-uniform
-        uint8_t *stage_buf = stage_base + (nbox % C::kStagingBufs) * kStagingBytes;
-        ++nbox;
-        if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
-        __syncwarp();
+        uint8_t *stage_buf;
+        if (last) {
+          stage_buf = smem + ((warp - 2) * kBoxes + c) * kStagingBytes;
+        } else {
+          stage_buf = stage_base + (nbox % C::kStagingBufs) * kStagingBytes;
+          ++nbox;
+          if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
+          __syncwarp();
+        }
         uint4 v[4];
         if constexpr (OUT_F32) {
 #pragma unroll
@@ -349,7 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_group0();
+    // Before the CTA (and its staging buffers) goes away the stores must
+    // have read their sources; their global writes complete with the grid.
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
 
