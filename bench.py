@@ -208,9 +208,8 @@ class DeviceWorkload:
                 if self.fmt == mx.MX_FMT_NVFP4:
                     s["ts_a"] = torch.zeros(1, dtype=torch.float32, device=dev)
                     s["ts_b"] = torch.zeros(1, dtype=torch.float32, device=dev)
-                    qws = mx.mx_quantize_workspace_bytes(m, k, self.fmt)
-                    s["qws_a"] = torch.empty(qws, dtype=u8, device=dev)
-                    s["qws_b"] = torch.empty(qws, dtype=u8, device=dev)
+                    qws = mx.mx_quantize_group_workspace_bytes(2, self.fmt)
+                    s["qws"] = torch.empty(qws, dtype=u8, device=dev)
             else:
                 s["codes_a"] = torch.from_numpy(host_inputs["a_codes"]).to(dev)
                 s["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).to(dev)
@@ -229,14 +228,13 @@ class DeviceWorkload:
         m, n, k, fmt = self.m, self.n, self.k, self.fmt
         out = []
         if self.kind == "bf16":
-            def qa(s, st):
-                mx.mx_quantize_bf16(s["x_a"], m, k, k, fmt, mx.MX_SCALE_TCGEN05, s["codes_a"],
-                                    s["sf_a"], s.get("ts_a"), s.get("qws_a"), stream=st)
-
-            def qb(s, st):
-                mx.mx_quantize_bf16(s["x_b"], n, k, k, fmt, mx.MX_SCALE_TCGEN05, s["codes_b"],
-                                    s["sf_b"], s.get("ts_b"), s.get("qws_b"), stream=st)
-            out += [("quantize_a", qa), ("quantize_w", qb)]
+            # the activation and the weight in one grouped quantize call
+            def q(s, st):
+                mx.mx_quantize_bf16_group(
+                    [(s["x_a"], m, k, k, s["codes_a"], s["sf_a"], s.get("ts_a")),
+                     (s["x_b"], n, k, k, s["codes_b"], s["sf_b"], s.get("ts_b"))],
+                    fmt, mx.MX_SCALE_TCGEN05, s.get("qws"), stream=st)
+            out.append(("quantize", q))
 
         def gemm(s, st):
             if fmt == mx.MX_FMT_MXFP4:
@@ -256,7 +254,7 @@ class DeviceWorkload:
         g = 1 + (1 if mx.mx_gemm_workspace_bytes(self.m, self.n, self.k, self.split_k) else 0)
         res = {"gemm": g}
         if self.kind == "bf16":
-            res.update({"quantize_a": q, "quantize_w": q})
+            res["quantize"] = q
         return res
 
     def algorithmic(self):
@@ -269,8 +267,7 @@ class DeviceWorkload:
         gemm_bytes = (m + n) * k * (0.5 + 1.0 / blk) + m * n * out_b
         res = {"gemm": (gemm_bytes, 2.0 * m * n * k)}
         if self.kind == "bf16":
-            res["quantize_a"] = (qbytes(m), 0.0)
-            res["quantize_w"] = (qbytes(n), 0.0)
+            res["quantize"] = (qbytes(m) + qbytes(n), 0.0)
         return res
 
     def step(self, i, stream):
@@ -470,8 +467,7 @@ def cpu_baseline(name, host, target_s):
 # Source files that define the kernels of each call of the step.
 CALL_SOURCES = {
     "gemm": ["gemm.cu", "gemm_pair.cu", "mx_device.cuh", "mx_internal.h"],
-    "quantize_a": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
-    "quantize_w": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
+    "quantize": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
 }
 
 

@@ -34,9 +34,17 @@ MX_LAYOUT_TN = 0
 MX_OUT_BF16 = 0
 MX_OUT_FP32 = 1
 MX_STATIC_WORKSPACE_BYTES = 16 << 20
+MX_QUANTIZE_GROUP_MAX = 8
 
 _lock = threading.Lock()
 _lib = None
+
+
+class mx_quantize_tensor(ctypes.Structure):
+    """One tensor of mx_quantize_bf16_group (the C struct of the same name)."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ld_x", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
 
 
 class MXError(RuntimeError):
@@ -67,6 +75,11 @@ def lib() -> ctypes.CDLL:
         L.mx_quantize_workspace_bytes.argtypes = [i64, i64, i32]
         L.mx_quantize_bf16.restype = i32
         L.mx_quantize_bf16.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.mx_quantize_group_workspace_bytes.restype = sz
+        L.mx_quantize_group_workspace_bytes.argtypes = [i32, i32]
+        L.mx_quantize_bf16_group.restype = i32
+        L.mx_quantize_bf16_group.argtypes = [ctypes.POINTER(mx_quantize_tensor), i32, i32, i32, vp,
+                                             sz, vp]
         L.mx_scale_relayout.restype = i32
         L.mx_scale_relayout.argtypes = [vp, i64, i64, i32, vp, vp]
         L.mx_gemm_workspace_bytes.restype = sz
@@ -144,6 +157,23 @@ def mx_quantize_bf16(x, rows, cols, ld_x, fmt, scale_layout, codes, scales, tens
     return _check("mx_quantize_bf16", lib().mx_quantize_bf16(
         _ptr(x), rows, cols, ld_x, fmt, scale_layout, _ptr(codes), _ptr(scales),
         _ptr(tensor_scale), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def mx_quantize_group_workspace_bytes(count: int, fmt: int) -> int:
+    return lib().mx_quantize_group_workspace_bytes(count, fmt)
+
+
+def mx_quantize_bf16_group(tensors, fmt, scale_layout, workspace=None, workspace_bytes=None,
+                           stream=None):
+    """tensors: sequence of (x, rows, cols, ld_x, codes, scales, tensor_scale) tuples."""
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    arr = (mx_quantize_tensor * max(1, len(tensors)))()
+    for i, (x, rows, cols, ld_x, codes, scales, tensor_scale) in enumerate(tensors):
+        arr[i] = mx_quantize_tensor(_ptr(x), rows, cols, ld_x, _ptr(codes), _ptr(scales),
+                                    _ptr(tensor_scale))
+    return _check("mx_quantize_bf16_group", lib().mx_quantize_bf16_group(
+        arr, len(tensors), fmt, scale_layout, _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def mx_scale_relayout(plain, rows, cols, fmt, tiled, stream=None):

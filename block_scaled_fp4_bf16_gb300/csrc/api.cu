@@ -274,9 +274,13 @@ MX_API size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, int format
   return format == MX_FMT_NVFP4 ? static_cast<size_t>(mx::kAmaxPartials) * sizeof(uint32_t) : 0;
 }
 
-MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
-                            int scale_layout, void *codes, void *scales, float *tensor_scale,
-                            void *workspace, size_t workspace_bytes, void *stream) {
+namespace {
+
+// Checks one tensor of a quantize call (everything but the workspace) and
+// fills its launch arguments.
+int quantize_tensor_args(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
+                         int scale_layout, void *codes, void *scales, float *tensor_scale,
+                         mx::QuantizeArgs *a) {
   if (!x || !codes || !scales) return MX_ERR_INVALID_ARG;
   if (!valid_format(format)) return MX_ERR_INVALID_ARG;
   if (scale_layout != MX_SCALE_PLAIN && scale_layout != MX_SCALE_TCGEN05) return MX_ERR_INVALID_ARG;
@@ -290,29 +294,107 @@ MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t l
     return MX_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || (ld_x % 8) != 0 || !aligned16(codes) || !aligned16(scales))
     return MX_ERR_ALIGNMENT;
+  if (format == MX_FMT_NVFP4 && (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return MX_ERR_ALIGNMENT;
+  *a = mx::QuantizeArgs{};
+  a->x = x;
+  a->rows = rows;
+  a->cols = cols;
+  a->ld = ld_x;
+  a->tiled = scale_layout == MX_SCALE_TCGEN05;
+  a->codes = codes;
+  a->scales = scales;
+  a->tensor_scale = tensor_scale;
+  return MX_OK;
+}
+
+// Byte range [lo, hi) of a buffer, for the overlap check of grouped calls.
+struct Range {
+  uintptr_t lo, hi;
+};
+
+bool overlap(const Range &p, const Range &q) { return p.lo < q.hi && q.lo < p.hi; }
+
+}  // namespace
+
+MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
+                            int scale_layout, void *codes, void *scales, float *tensor_scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  mx::QuantizeArgs a;
+  int rc = quantize_tensor_args(x, rows, cols, ld_x, format, scale_layout, codes, scales,
+                                tensor_scale, &a);
+  if (rc != MX_OK) return rc;
   if (format == MX_FMT_NVFP4) {
-    if ((reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0) return MX_ERR_ALIGNMENT;
     if (!workspace || workspace_bytes < mx_quantize_workspace_bytes(rows, cols, format))
       return MX_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+    a.partials = static_cast<uint32_t *>(workspace);
+  }
+  DeviceInfo *dev = nullptr;
+  rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  a.num_sms = dev->num_sms;
+  return launch_rc(mx::launch_quantize_group(format == MX_FMT_MXFP4 ? 0 : 1, &a, 1,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+MX_API size_t mx_quantize_group_workspace_bytes(int count, int format) {
+  if (count < 1 || count > MX_QUANTIZE_GROUP_MAX || !valid_format(format)) return 0;
+  return static_cast<size_t>(count) * mx_quantize_workspace_bytes(1, block_of(format), format);
+}
+
+MX_API int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, int format,
+                                  int scale_layout, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+  static_assert(MX_QUANTIZE_GROUP_MAX == mx::kQuantizeGroupMax, "group size");
+  if (!tensors || count < 1 || count > MX_QUANTIZE_GROUP_MAX) return MX_ERR_INVALID_ARG;
+  mx::QuantizeArgs a[MX_QUANTIZE_GROUP_MAX];
+  Range in[MX_QUANTIZE_GROUP_MAX], out[3 * MX_QUANTIZE_GROUP_MAX];
+  int nout = 0;
+  for (int i = 0; i < count; ++i) {
+    const mx_quantize_tensor &t = tensors[i];
+    const int rc = quantize_tensor_args(t.x, t.rows, t.cols, t.ld_x, format, scale_layout, t.codes,
+                                        t.scales, t.tensor_scale, &a[i]);
+    if (rc != MX_OK) return rc;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(t.x);
+    in[i] = Range{x, x + static_cast<uintptr_t>(((t.rows - 1) * t.ld_x + t.cols) * 2)};
+    const uintptr_t c = reinterpret_cast<uintptr_t>(t.codes);
+    out[nout++] = Range{c, c + static_cast<uintptr_t>(t.rows * t.cols / 2)};
+    const uintptr_t sc = reinterpret_cast<uintptr_t>(t.scales);
+    out[nout++] = Range{sc, sc + mx_scale_bytes(t.rows, t.cols, format, scale_layout)};
+    if (t.tensor_scale) {
+      const uintptr_t ts = reinterpret_cast<uintptr_t>(t.tensor_scale);
+      out[nout++] = Range{ts, ts + sizeof(float)};
+    }
+  }
+  // The tensors are quantized concurrently: no output may overlap an input
+  // or another output.
+  for (int o = 0; o < nout; ++o) {
+    for (int i = 0; i < count; ++i)
+      if (overlap(out[o], in[i])) return MX_ERR_INVALID_ARG;
+    for (int p = o + 1; p < nout; ++p)
+      if (overlap(out[o], out[p])) return MX_ERR_INVALID_ARG;
+  }
+  if (format == MX_FMT_NVFP4) {
+    if (!workspace || workspace_bytes < mx_quantize_group_workspace_bytes(count, format))
+      return MX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+    const Range ws{reinterpret_cast<uintptr_t>(workspace),
+                   reinterpret_cast<uintptr_t>(workspace) +
+                       mx_quantize_group_workspace_bytes(count, format)};
+    for (int o = 0; o < nout; ++o)
+      if (overlap(ws, out[o])) return MX_ERR_INVALID_ARG;
+    for (int i = 0; i < count; ++i) {
+      if (overlap(ws, in[i])) return MX_ERR_INVALID_ARG;
+      a[i].partials = static_cast<uint32_t *>(workspace) + static_cast<size_t>(i) * mx::kAmaxPartials;
+    }
   }
   DeviceInfo *dev = nullptr;
   const int rc = device_info(&dev);
   if (rc != MX_OK) return rc;
-  mx::QuantizeArgs a{};
-  a.x = x;
-  a.rows = rows;
-  a.cols = cols;
-  a.ld = ld_x;
-  a.tiled = scale_layout == MX_SCALE_TCGEN05;
-  a.codes = codes;
-  a.scales = scales;
-  a.tensor_scale = tensor_scale;
-  a.partials = static_cast<uint32_t *>(workspace);
-  a.num_sms = dev->num_sms;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return launch_rc(format == MX_FMT_MXFP4 ? mx::launch_mx_quantize(a, s)
-                                          : mx::launch_nvfp4_quantize(a, s));
+  for (int i = 0; i < count; ++i) a[i].num_sms = dev->num_sms;
+  return launch_rc(mx::launch_quantize_group(format == MX_FMT_MXFP4 ? 0 : 1, a, count,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format,

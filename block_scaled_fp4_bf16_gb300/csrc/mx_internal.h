@@ -27,8 +27,14 @@ struct QuantizeArgs {
   int num_sms;
 };
 
-cudaError_t launch_mx_quantize(const QuantizeArgs &a, cudaStream_t s);
-cudaError_t launch_nvfp4_quantize(const QuantizeArgs &a, cudaStream_t s);
+// Most tensors one quantize launch takes (MX_QUANTIZE_GROUP_MAX).
+constexpr int kQuantizeGroupMax = 8;
+
+// Quantizes `count` independent tensors (1..kQuantizeGroupMax) of one format
+// in one launch (NVFP4: one amax launch, then one quantize launch).  fmt: 0
+// MXFP4, 1 NVFP4.  Each NVFP4 tensor has its own kAmaxPartials partials.
+cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int count,
+                                  cudaStream_t s);
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
                                   cudaStream_t s);
 

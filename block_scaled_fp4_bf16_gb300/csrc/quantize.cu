@@ -16,7 +16,9 @@
 // instructions (no shuffles), scales with packed FP32x2 multiplies, converts
 // two elements per cvt instruction and writes its codes with one store.  No
 // shared memory, 32-bit index arithmetic, and a multiply-high division for
-// (row, block).
+// (row, block).  One launch may quantize several independent tensors: each
+// tensor's blocks are padded to whole CTAs and the CTAs of all tensors form
+// one grid, so a CTA belongs to exactly one tensor.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -56,6 +58,39 @@ __device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
 // Byte offset of scale (row r, scale column c) in the 128x4 tile order.
 __device__ __forceinline__ uint32_t tiled_offset(uint32_t r, uint32_t c, uint32_t katoms) {
   return ((r >> 7) * katoms + (c >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (c & 3u);
+}
+
+// One tensor of a quantize launch.  Its scale blocks (rows padded to 128 in
+// the tiled order) are numbered b = 0..total-1 and handled by the CTAs
+// first_cta .. first_cta + ceil(total / kThreads) - 1 of the grid.
+struct QTensor {
+  const uint16_t *x;            // BF16 bits [rows, cols], row stride ld
+  uint8_t *codes;               // [rows, cols / 2]
+  uint8_t *scales;              // plain [rows, kb] or tiled
+  uint32_t *partials;           // NVFP4: this tensor's kAmaxPartials maxima
+  float *tensor_scale;          // NVFP4: s_t out
+  int64_t ld;
+  uint32_t rows, cols;
+  uint32_t total;               // scale blocks incl. row padding
+  uint32_t real_total;          // rows * kb
+  uint32_t first_cta;
+  uint32_t katoms;
+  FastDiv kbdiv;                // kb = cols / block
+  int tiled;
+};
+
+struct QGroup {
+  int count;
+  QTensor t[kQuantizeGroupMax];
+};
+
+// The tensor of this CTA: the last one whose first CTA is <= blockIdx.x.
+__device__ __forceinline__ const QTensor &group_member(const QGroup &g) {
+  int i = 0;
+#pragma unroll
+  for (int k = 1; k < kQuantizeGroupMax; ++k)
+    if (k < g.count && blockIdx.x >= g.t[k].first_cta) i = k;
+  return g.t[i];
 }
 
 // 32 bytes from global memory (read-only path): one 32-byte load when the
@@ -127,25 +162,23 @@ __device__ __forceinline__ uint32_t scale_to_e2m1x8(const uint32_t *w, float sca
   return out;
 }
 
-// MXFP4 quantize: thread b owns block b of the [rows_pad, kb] block grid.
-// x: BF16 bits [rows, cols] stride ld.  codes [rows, cols/2].
-// scales: plain [rows, kb] or tiled (rows padded to rows_pad with 0 bytes).
-// WIDE: x is 32-byte aligned and ld % 16 == 0.
+// MXFP4 quantize: thread b of a tensor's CTAs owns block b of its
+// [rows_pad, kb] block grid.  Scales plain [rows, kb] or tiled (rows padded
+// to rows_pad with 0 bytes).  WIDE: every x is 32-byte aligned, ld % 16 == 0.
 template <bool WIDE>
-__global__ void __launch_bounds__(kThreads) mx_quantize_kernel(
-    const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, int64_t ld,
-    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, uint32_t total,
-    FastDiv kbdiv, uint32_t katoms) {
+__global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
-  const uint32_t b = blockIdx.x * kThreads + threadIdx.x;
-  if (b >= total) return;
-  const uint32_t kb = kbdiv.d;
-  const uint32_t r = fast_div(b, kbdiv);
+  const QTensor &t = group_member(g);
+  const uint32_t b = (blockIdx.x - t.first_cta) * kThreads + threadIdx.x;
+  if (b >= t.total) return;
+  const uint32_t kb = t.kbdiv.d;
+  const uint32_t r = fast_div(b, t.kbdiv);
   const uint32_t j = b - r * kb;
+  uint8_t *__restrict__ scales = t.scales;
   uint32_t sbyte = 0;
-  if (r < rows) {
-    const uint16_t *src = x + static_cast<int64_t>(r) * ld + j * 32u;
+  if (r < t.rows) {
+    const uint16_t *src = t.x + static_cast<int64_t>(r) * t.ld + j * 32u;
     uint32_t w[16];
     load32<WIDE>(src, &w[0]);
     load32<WIDE>(src + 16, &w[8]);
@@ -157,13 +190,13 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(
     out.y = scale_to_e2m1x8(&w[4], inv);
     out.z = scale_to_e2m1x8(&w[8], inv);
     out.w = scale_to_e2m1x8(&w[12], inv);
-    *reinterpret_cast<uint4 *>(codes + static_cast<int64_t>(r) * (cols >> 1) + j * 16u) = out;
+    *reinterpret_cast<uint4 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 16u) = out;
     sbyte = static_cast<uint32_t>(e + 127);
   }
-  if (tiled) {
-    scales[tiled_offset(r, j, katoms)] = static_cast<uint8_t>(sbyte);
+  if (t.tiled) {
+    scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sbyte);
     if (j == kb - 1)
-      for (uint32_t jj = kb; jj < katoms * 4u; ++jj) scales[tiled_offset(r, jj, katoms)] = 0;
+      for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
   } else {
     scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sbyte);
   }
@@ -171,20 +204,19 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(
 
 // NVFP4 pass 1: per-CTA partial amax (as the 15-bit BF16 magnitude
 // pattern, whose integer order is the order of the values), grid-stride over
-// the 16-element blocks.
+// the 16-element blocks of tensor blockIdx.y.
 template <bool WIDE>
-__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const uint16_t *__restrict__ x,
-                                                              int64_t ld, uint32_t total,
-                                                              FastDiv kbdiv,
-                                                              uint32_t *__restrict__ partials) {
+__global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
+  const QTensor &t = g.t[blockIdx.y];
   uint32_t m = 0;
-  for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < total; b += gridDim.x * kThreads) {
-    const uint32_t r = fast_div(b, kbdiv);
-    const uint32_t j = b - r * kbdiv.d;
+  for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < t.real_total;
+       b += gridDim.x * kThreads) {
+    const uint32_t r = fast_div(b, t.kbdiv);
+    const uint32_t j = b - r * t.kbdiv.d;
     uint32_t w[8];
-    load32<WIDE>(x + static_cast<int64_t>(r) * ld + j * 16u, w);
+    load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + j * 16u, w);
     m = max(m, block_amax<8>(w));
   }
 #pragma unroll
@@ -193,10 +225,10 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const uint16_t *__
   if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t t = 0;
+    uint32_t v = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) t = max(t, warp_max[w]);
-    partials[blockIdx.x] = t;
+    for (int w = 0; w < kThreads / 32; ++w) v = max(v, warp_max[w]);
+    t.partials[blockIdx.x] = v;
   }
 }
 
@@ -269,48 +301,47 @@ __device__ __forceinline__ uint32_t div_to_e2m1x8_ieee(const uint32_t *w, float 
   return out;
 }
 
-// NVFP4 pass 2: every CTA reduces the partial maxima to s_t, then thread b
-// quantizes 16-element block b.  Each binary32 step of the definition is one
-// round-to-nearest operation (correctly rounded divisions where it divides).
+// NVFP4 pass 2: every CTA reduces its tensor's partial maxima to s_t, then
+// thread b quantizes 16-element block b.  Each binary32 step of the
+// definition is one round-to-nearest operation (correctly rounded divisions
+// where it divides).
 template <bool WIDE>
-__global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
-    const uint16_t *__restrict__ x, uint32_t rows, uint32_t cols, int64_t ld,
-    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int tiled, uint32_t total,
-    FastDiv kbdiv, uint32_t katoms, const uint32_t *__restrict__ partials,
-    float *__restrict__ tensor_scale) {
+__global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
+  const QTensor &t = group_member(g);
   __shared__ uint32_t warp_max[kThreads / 32];
   __shared__ float s_t_shared;
   {
     uint32_t m = 0;
-    for (int i = threadIdx.x; i < kAmaxPartials; i += kThreads) m = max(m, partials[i]);
+    for (int i = threadIdx.x; i < kAmaxPartials; i += kThreads) m = max(m, t.partials[i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
     if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-      uint32_t t = 0;
-      for (int w = 0; w < kThreads / 32; ++w) t = max(t, warp_max[w]);
-      const float amax_t = __uint_as_float(t << 16);
+      uint32_t v = 0;
+      for (int w = 0; w < kThreads / 32; ++w) v = max(v, warp_max[w]);
+      const float amax_t = __uint_as_float(v << 16);
       const float s_t = __fdiv_rn(amax_t, 2688.0f);
       s_t_shared = s_t;
-      if (blockIdx.x == 0) *tensor_scale = s_t;
+      if (blockIdx.x == t.first_cta) *t.tensor_scale = s_t;
     }
     __syncthreads();
   }
   const float s_t = s_t_shared;
   const float six_s_t = __fmul_rn(6.0f, s_t);
 
-  const uint32_t b = blockIdx.x * kThreads + threadIdx.x;
-  if (b >= total) return;
-  const uint32_t kb = kbdiv.d;
-  const uint32_t r = fast_div(b, kbdiv);
+  const uint32_t b = (blockIdx.x - t.first_cta) * kThreads + threadIdx.x;
+  if (b >= t.total) return;
+  const uint32_t kb = t.kbdiv.d;
+  const uint32_t r = fast_div(b, t.kbdiv);
   const uint32_t j = b - r * kb;
+  uint8_t *__restrict__ scales = t.scales;
   uint32_t sb = 0;
-  if (r < rows) {
+  if (r < t.rows) {
     uint32_t w[8];
-    load32<WIDE>(x + static_cast<int64_t>(r) * ld + j * 16u, w);
+    load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + j * 16u, w);
     const uint32_t amax = block_amax<8>(w);
     if (s_t > 0.0f) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(amax << 16), six_s_t));
     uint2 out = make_uint2(0u, 0u);
@@ -325,12 +356,12 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(
         out.y = div_to_e2m1x8_ieee(&w[4], den);
       }
     }
-    *reinterpret_cast<uint2 *>(codes + static_cast<int64_t>(r) * (cols >> 1) + j * 8u) = out;
+    *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
   }
-  if (tiled) {
-    scales[tiled_offset(r, j, katoms)] = static_cast<uint8_t>(sb);
+  if (t.tiled) {
+    scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sb);
     if (j == kb - 1)
-      for (uint32_t jj = kb; jj < katoms * 4u; ++jj) scales[tiled_offset(r, jj, katoms)] = 0;
+      for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
   } else {
     scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
   }
@@ -360,40 +391,49 @@ bool wide_ok(const void *x, int64_t ld) {
 
 }  // namespace
 
-cudaError_t launch_mx_quantize(const QuantizeArgs &a, cudaStream_t s) {
-  const uint32_t kb = static_cast<uint32_t>(a.cols / 32);
-  const uint32_t rows_pad = static_cast<uint32_t>(a.tiled ? (a.rows + 127) / 128 * 128 : a.rows);
-  const uint32_t total = rows_pad * kb;
-  const uint32_t grid = (total + kThreads - 1) / kThreads;
-  auto kern = wide_ok(a.x, a.ld) ? mx_quantize_kernel<true> : mx_quantize_kernel<false>;
-  const cudaError_t e = launch_pdl(
-      kern, dim3(grid), dim3(kThreads), 0, s, static_cast<const uint16_t *>(a.x),
-      static_cast<uint32_t>(a.rows), static_cast<uint32_t>(a.cols), a.ld,
-      static_cast<uint8_t *>(a.codes), static_cast<uint8_t *>(a.scales), a.tiled, total,
-      make_fastdiv(kb), (kb + 3) / 4);
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-cudaError_t launch_nvfp4_quantize(const QuantizeArgs &a, cudaStream_t s) {
-  const uint32_t kb = static_cast<uint32_t>(a.cols / 16);
-  const FastDiv kbdiv = make_fastdiv(kb);
-  const uint32_t real_total = static_cast<uint32_t>(a.rows) * kb;
-  const bool wide = wide_ok(a.x, a.ld);
-  auto amax_kern = wide ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>;
-  cudaError_t e = launch_pdl(amax_kern, dim3(kAmaxPartials), dim3(kThreads), 0, s,
-                             static_cast<const uint16_t *>(a.x), a.ld, real_total, kbdiv,
-                             a.partials);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const uint32_t rows_pad = static_cast<uint32_t>(a.tiled ? (a.rows + 127) / 128 * 128 : a.rows);
-  const uint32_t total = rows_pad * kb;
-  const uint32_t grid = (total + kThreads - 1) / kThreads;
-  auto quant_kern = wide ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>;
-  e = launch_pdl(quant_kern, dim3(grid), dim3(kThreads), 0, s,
-                 static_cast<const uint16_t *>(a.x), static_cast<uint32_t>(a.rows),
-                 static_cast<uint32_t>(a.cols), a.ld, static_cast<uint8_t *>(a.codes),
-                 static_cast<uint8_t *>(a.scales), a.tiled, total, kbdiv, (kb + 3) / 4,
-                 static_cast<const uint32_t *>(a.partials), a.tensor_scale);
+cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int count,
+                                  cudaStream_t s) {
+  if (count < 1 || count > kQuantizeGroupMax) return cudaErrorInvalidValue;
+  const uint32_t block = fmt == 0 ? 32u : 16u;
+  QGroup g{};
+  g.count = count;
+  bool wide = true;
+  uint32_t ctas = 0;
+  for (int i = 0; i < count; ++i) {
+    const QuantizeArgs &a = tensors[i];
+    QTensor &t = g.t[i];
+    const uint32_t kb = static_cast<uint32_t>(a.cols) / block;
+    const uint32_t rows_pad =
+        static_cast<uint32_t>(a.tiled ? (a.rows + 127) / 128 * 128 : a.rows);
+    t.x = static_cast<const uint16_t *>(a.x);
+    t.codes = static_cast<uint8_t *>(a.codes);
+    t.scales = static_cast<uint8_t *>(a.scales);
+    t.partials = a.partials;
+    t.tensor_scale = a.tensor_scale;
+    t.ld = a.ld;
+    t.rows = static_cast<uint32_t>(a.rows);
+    t.cols = static_cast<uint32_t>(a.cols);
+    t.total = rows_pad * kb;
+    t.real_total = t.rows * kb;
+    t.first_cta = ctas;
+    t.katoms = (kb + 3) / 4;
+    t.kbdiv = make_fastdiv(kb);
+    t.tiled = a.tiled;
+    ctas += (t.total + kThreads - 1) / kThreads;
+    wide = wide && wide_ok(a.x, a.ld);
+  }
+  cudaError_t e;
+  if (fmt == 0) {
+    e = launch_pdl(wide ? mx_quantize_kernel<true> : mx_quantize_kernel<false>, dim3(ctas),
+                   dim3(kThreads), 0, s, g);
+  } else {
+    e = launch_pdl(wide ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>,
+                   dim3(kAmaxPartials, count), dim3(kThreads), 0, s, g);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(wide ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>, dim3(ctas),
+                   dim3(kThreads), 0, s, g);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -118,6 +118,45 @@ int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t ld_x, in
                      int scale_layout, void *codes, void *scales, float *tensor_scale,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- grouped quantize ---------------------------------------------------
+ * The pages quantize one tensor per call and have no grouped form.  This
+ * library adds one: several independent tensors of one format (typically
+ * the activation and the weight of one GEMM) in a single launch (NVFP4: one
+ * amax launch and one quantize launch), which saves the ramp-up and tail of
+ * a launch per tensor on inputs of a few tens of MB.  Each tensor's codes,
+ * scales and tensor scale are byte for byte those of mx_quantize_bf16 on the
+ * same arguments (the quantize rules above). */
+
+/* Most tensors one mx_quantize_bf16_group call takes. */
+#define MX_QUANTIZE_GROUP_MAX 8
+
+/* One tensor of a grouped call; the fields mean what the arguments of the
+ * same names of mx_quantize_bf16 mean (all pointers are device pointers). */
+typedef struct mx_quantize_tensor {
+  const void *x;       /* BF16 [rows, cols], row stride ld_x elements */
+  int64_t rows, cols, ld_x;
+  void *codes;         /* out, rows * cols / 2 bytes                  */
+  void *scales;        /* out, mx_scale_bytes(rows, cols, ...) bytes  */
+  float *tensor_scale; /* NVFP4: out s_t; MXFP4: NULL                 */
+} mx_quantize_tensor;
+
+/* Workspace bytes of a grouped call of `count` tensors: count times the
+ * per-tensor NVFP4 buffer of partial maxima, 0 for MXFP4 (0 as well for an
+ * invalid count or format). */
+size_t mx_quantize_group_workspace_bytes(int count, int format);
+
+/* Quantizes tensors[0 .. count-1] (count in 1..MX_QUANTIZE_GROUP_MAX; the
+ * array itself is host memory, read before the call returns) with one
+ * format and one scale layout.  Every tensor is validated as by
+ * mx_quantize_bf16 before anything is launched; in addition no output
+ * buffer (codes, scales, tensor scale, workspace) may overlap any input or
+ * another output (MX_ERR_INVALID_ARG), since the tensors are processed
+ * concurrently.  workspace: mx_quantize_group_workspace_bytes(count, format)
+ * bytes (NULL if 0). */
+int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, int format,
+                           int scale_layout, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
 /* Plain scales [rows, cols / block] -> MX_SCALE_TCGEN05 order (see
  * mx_scale_bytes).  `tiled` receives mx_scale_bytes(rows, cols, format,
  * MX_SCALE_TCGEN05) bytes, padding included ("Integrate MXFP4 hipblaslt GEMM

@@ -52,6 +52,33 @@ def gpu_quantize(x_bits: np.ndarray, fmt: int, layout: int, ld: int | None = Non
     return codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(), s_t
 
 
+def gpu_quantize_group(xs, fmt: int, layout: int, lds=None):
+    """Quantize several BF16-bit arrays in one mx_quantize_bf16_group call;
+    returns a list of host (codes, scales, s_t).  Outputs are pre-filled with
+    0xAB so that any byte the kernel fails to write shows up."""
+    lds = lds or [None] * len(xs)
+    keep, tensors, outs = [], [], []
+    for x_bits, ld in zip(xs, lds):
+        rows, cols = x_bits.shape
+        ld = cols if ld is None else ld
+        padded = np.zeros((rows, ld), np.uint16)
+        padded[:, :cols] = x_bits
+        x = dev_bf16(padded)
+        codes = torch.full((rows * cols // 2,), 0xAB, dtype=torch.uint8, device="cuda")
+        scales = torch.full((mx.mx_scale_bytes(rows, cols, fmt, layout),), 0xAB,
+                            dtype=torch.uint8, device="cuda")
+        ts = torch.full((1,), -1.0, dtype=torch.float32, device="cuda") if fmt == mx.MX_FMT_NVFP4 else None
+        keep.append(x)
+        tensors.append((x, rows, cols, ld, codes, scales, ts))
+        outs.append((rows, cols, codes, scales, ts))
+    wsb = mx.mx_quantize_group_workspace_bytes(len(xs), fmt)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    mx.mx_quantize_bf16_group(tensors, fmt, layout, ws)
+    torch.cuda.synchronize()
+    return [(codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(),
+             None if ts is None else np.float32(ts.item())) for rows, cols, codes, scales, ts in outs]
+
+
 def gpu_relayout(plain: np.ndarray, rows: int, cols: int, fmt: int) -> torch.Tensor:
     tiled = torch.full((mx.mx_scale_bytes(rows, cols, fmt, mx.MX_SCALE_TCGEN05),), 0xAB,
                        dtype=torch.uint8, device="cuda")

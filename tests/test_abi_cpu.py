@@ -113,6 +113,48 @@ def test_quantize_argument_validation(lib):
     assert q(FAKE, 4, 32, 32, 1, 0, FAKE, FAKE, FAKE, None, 0, None) == mx.MX_ERR_WORKSPACE
 
 
+def _group(lib, tensors, fmt=0, layout=0, ws=None, wsb=0):
+    arr = (mx.mx_quantize_tensor * max(1, len(tensors)))()
+    for i, t in enumerate(tensors):
+        arr[i] = mx.mx_quantize_tensor(*t)
+    return lib.mx_quantize_bf16_group(arr, len(tensors), fmt, layout, ws, wsb, None)
+
+
+def test_group_workspace_bytes(lib):
+    per = mx.mx_quantize_workspace_bytes(1, 16, mx.MX_FMT_NVFP4)
+    assert mx.mx_quantize_group_workspace_bytes(3, mx.MX_FMT_NVFP4) == 3 * per
+    assert mx.mx_quantize_group_workspace_bytes(3, mx.MX_FMT_MXFP4) == 0
+    assert mx.mx_quantize_group_workspace_bytes(0, mx.MX_FMT_NVFP4) == 0
+    assert mx.mx_quantize_group_workspace_bytes(mx.MX_QUANTIZE_GROUP_MAX + 1, 1) == 0
+
+
+def test_group_quantize_argument_validation(lib):
+    MB = 1 << 20
+    # (x, rows, cols, ld_x, codes, scales, tensor_scale): disjoint buffers 1 MiB apart
+    t0 = (FAKE, 64, 256, 256, FAKE + 1 * MB, FAKE + 2 * MB, None)
+    t1 = (FAKE + 3 * MB, 32, 512, 512, FAKE + 4 * MB, FAKE + 5 * MB, None)
+    assert _group(lib, []) == mx.MX_ERR_INVALID_ARG                      # count 0
+    assert _group(lib, [t0] * (mx.MX_QUANTIZE_GROUP_MAX + 1)) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_quantize_bf16_group(None, 1, 0, 0, None, 0, None) == mx.MX_ERR_INVALID_ARG
+    # every tensor is checked as by mx_quantize_bf16
+    assert _group(lib, [t0, t1[:1] + (32, 48, 48) + t1[4:]]) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _group(lib, [t0, (FAKE_ODD,) + t1[1:]]) == mx.MX_ERR_ALIGNMENT
+    assert _group(lib, [t0, t1[:6] + (FAKE + 6 * MB,)]) == mx.MX_ERR_INVALID_ARG  # MX tensor scale
+    # outputs overlapping an input or another output are refused
+    assert _group(lib, [t0, t1[:4] + (FAKE + 1 * MB,) + t1[5:]]) == mx.MX_ERR_INVALID_ARG
+    assert _group(lib, [t0, t1[:4] + (FAKE + 16,) + t1[5:]]) == mx.MX_ERR_INVALID_ARG
+    assert _group(lib, [t0[:5] + (FAKE + 1 * MB + 4096,) + t0[6:]]) == mx.MX_ERR_INVALID_ARG
+    # NVFP4: tensor scales and a workspace of count x the per-tensor size
+    n0 = t0[:6] + (FAKE + 6 * MB,)
+    n1 = t1[:6] + (FAKE + 6 * MB + 64,)
+    wsb = mx.mx_quantize_group_workspace_bytes(2, mx.MX_FMT_NVFP4)
+    assert _group(lib, [n0, n1], fmt=1) == mx.MX_ERR_WORKSPACE
+    assert _group(lib, [n0, n1], fmt=1, ws=FAKE + 7 * MB, wsb=wsb - 16) == mx.MX_ERR_WORKSPACE
+    assert _group(lib, [n0, n0[:6] + (FAKE + 6 * MB,)], fmt=1, ws=FAKE + 7 * MB,
+                  wsb=wsb) == mx.MX_ERR_INVALID_ARG                    # one shared tensor scale
+    assert _group(lib, [n0, n1], fmt=1, ws=FAKE + 2 * MB, wsb=wsb) == mx.MX_ERR_INVALID_ARG
+
+
 def test_relayout_and_selftest_validation(lib):
     assert lib.mx_scale_relayout(None, 4, 32, 0, FAKE, None) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_scale_relayout(FAKE, 4, 40, 0, FAKE, None) == mx.MX_ERR_UNSUPPORTED_SHAPE

@@ -6,7 +6,7 @@ import pytest
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import gpu_quantize, gpu_relayout
+from tests.gpu_helpers import gpu_quantize, gpu_quantize_group, gpu_relayout
 
 pytestmark = pytest.mark.gpu
 
@@ -182,3 +182,61 @@ def test_leading_dim_not_32_byte_aligned():
     _check_mx(x, TILED, ld=520)
     _check_nv(x, TILED, ld=520)
     _check_nv(x, PLAIN, ld=528)
+
+
+# ---- grouped quantize: one launch, each tensor byte-equal to the oracle ----
+
+def _group_inputs(shapes, seed):
+    return [synth.bf16_normal(r, c, 0.5 + i, seed=seed + i) for i, (r, c) in enumerate(shapes)]
+
+
+@pytest.mark.parametrize("layout", [PLAIN, TILED])
+def test_mx_quantize_group_matches_oracle(layout):
+    shapes = [(129, 4096), (3, 96), (256, 512), (1, 32), (517, 1024)]
+    xs = _group_inputs(shapes, 700)
+    xs[2][5, :32] = 0                      # a zero block inside the group
+    got = gpu_quantize_group(xs, MX, layout, lds=[None, 104, None, 40, 1032])
+    for x, (codes, scales, s_t) in zip(xs, got):
+        rc, rs = oracle.mx_quantize(x)
+        assert s_t is None
+        assert np.array_equal(codes, rc), _explain(x, codes, rc, scales, rs, 32)
+        want = rs.ravel() if layout == PLAIN else oracle.scale_tile(rs)
+        assert np.array_equal(scales, want)
+
+
+@pytest.mark.parametrize("layout", [PLAIN, TILED])
+def test_nvfp4_quantize_group_matches_oracle(layout):
+    """Each tensor gets its own amax and s_t although the group shares launches."""
+    shapes = [(300, 1024), (5, 48), (128, 256)]
+    xs = _group_inputs(shapes, 800)
+    xs[1] = xs[1] * 0                     # an all-zero tensor: s_t = 0, codes 0
+    xs[2][7, 3] = synth.f32_to_bf16_bits(np.array([1000.0], np.float32))[0]
+    got = gpu_quantize_group(xs, NV, layout)
+    for x, (codes, scales, s_t) in zip(xs, got):
+        rc, rs, rt = oracle.nvfp4_quantize(x)
+        assert np.float32(s_t).view(np.uint32) == np.float32(rt).view(np.uint32)
+        assert np.array_equal(codes, rc), _explain(x, codes, rc, scales, rs, 16)
+        want = rs.ravel() if layout == PLAIN else oracle.scale_tile(rs)
+        assert np.array_equal(scales, want)
+
+
+def test_quantize_group_of_the_largest_size_matches_single_calls():
+    n = mx.MX_QUANTIZE_GROUP_MAX
+    xs = _group_inputs([(64 + 32 * i, 256 + 128 * i) for i in range(n)], 900)
+    for fmt in (MX, NV):
+        got = gpu_quantize_group(xs, fmt, TILED)
+        for x, (codes, scales, s_t) in zip(xs, got):
+            c1, s1, t1 = gpu_quantize(x, fmt, TILED)
+            assert np.array_equal(codes, c1) and np.array_equal(scales, s1)
+            assert (s_t is None and t1 is None) or s_t.view(np.uint32) == t1.view(np.uint32)
+
+
+def test_quantize_group_at_the_quantize_gemm_workload_size():
+    """The activation 2048x4096 and weight 4096x4096 of the quantize+GEMM
+    workload in one call, as the benchmark issues them."""
+    w = synth.workload_inputs("quant_gemm_2048x4096x4096")
+    got = gpu_quantize_group([w["a"], w["b"]], MX, TILED)
+    for x, (codes, scales, _) in zip([w["a"], w["b"]], got):
+        rc, rs = oracle.mx_quantize(x)
+        assert np.array_equal(codes, rc)
+        assert np.array_equal(scales, oracle.scale_tile(rs))
