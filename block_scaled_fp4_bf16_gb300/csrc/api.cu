@@ -190,7 +190,9 @@ int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *
     if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
   }
   CUtensorMap tma, tmb, tmd, tmsa, tmsb;
-  if (encode_codes_map(&tma, a_codes, m, k, 128) != MX_OK) return MX_ERR_CUDA;
+  // the single-CTA kernel (M <= 128) loads the M rows of A, the pair kernel 128 per CTA
+  if (encode_codes_map(&tma, a_codes, m, k, pair ? 128 : static_cast<int>(m)) != MX_OK)
+    return MX_ERR_CUDA;
   // the pair kernel stages half of each 256-row B tile per CTA
   if (encode_codes_map(&tmb, b_codes, n, k, pair ? 128 : bn) != MX_OK) return MX_ERR_CUDA;
   if (pair) {

@@ -9,11 +9,14 @@
 // Split-K with a separate fixed-order reduction follows the linear split
 // count of "Initial integration of a4w4 GEMM" (ROCm/TransformerEngine #663).
 //
+// Used for M <= 128 (larger M runs on CTA pairs, gemm_pair.cu).
 // Structure (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: A tile (128 x 256 codes), B tile (BN x 256),
-//               and the scale atoms of the stage, into an S-stage ring of
-//               shared memory, completion tracked by mbarriers.
-//   warp 1      allocates tensor memory; one lane issues, per stage,
+//   warp 0      TMA producer (whole warp waits, one elected lane issues): the
+//               M rows of A (rows M..127 of the 128-row tile stay 0), a B tile
+//               (BN x 256 codes) and the scale atoms of the stage, into an
+//               S-stage ring of shared memory, completion tracked by mbarriers.
+//   warp 1      allocates tensor memory; the converged warp waits and one
+//               elected lane issues, per stage,
 //               tcgen05.cp of the stage's scale atoms into that stage's own
 //               set of tensor-memory columns (so copies never wait on the
 //               MMAs of earlier stages) and four K=64 block-scaled MMAs into
@@ -63,6 +66,8 @@ struct Cfg {
   static constexpr int kTmemCols = 512;
   static_assert(kSfCol + kStages * kSfSetCols <= kTmemCols, "tensor memory budget");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+  // the last tile's output boxes (up to BN / 16 per epilogue warp) fit in the ring
+  static_assert(kEpilogueWarps * (BN / 16) * 2048 <= kStages * kStageBytes, "ring holds a tile's boxes");
   static constexpr int kStagingOff = kStages * kStageBytes;
   // barriers: full[S], empty[S], tfull[A], tempty[A]; then tmem slot, abort
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNumAcc) + 16;
@@ -87,6 +92,7 @@ struct Params {
   int n_row_atoms;             // ceil(N / 128)
   int partial;                 // 1: write FP32 partials of split s at rows s*M + m
   int num_units;
+  int a_rows;                  // rows of A loaded per stage (= M, a multiple of 32, <= 128)
 };
 
 // Unit -> (m tile, n tile, split); tiles are walked in groups of 8 M tiles
@@ -148,8 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmap_b);
     prefetch_tmap(&tmap_d);
   }
-  // B scale atoms past the end of N are never loaded: make them 0 (2^-127
-  // or 0.0, both finite) once, for every stage.
+  // The kernel runs for M <= 128, and only the M rows of A are loaded: the
+  // rest of every stage's 128-row A tile is made 0 once (the MMA then adds
+  // zero rows, whose outputs are not stored).  B scale atoms past the end of
+  // N are never loaded either: they are made 0 (2^-127 or 0.0, both finite).
+  for (int s = 0; s < C::kStages; ++s) {
+    uint32_t *a_tail = reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + p.a_rows * kStageKBytes);
+    for (int i = threadIdx.x; i < (kBM - p.a_rows) * kStageKBytes / 4; i += kThreads) a_tail[i] = 0u;
+  }
   for (int s = 0; s < C::kStages; ++s) {
     uint32_t *sfb = reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + C::kABytes +
                                                  C::kBBytes + C::kSfaBytes);
@@ -182,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k1 = min(k0 + p.stages_per_split, p.k_stages);
       const int rb0 = nt * C::kRowAtomsB;
       const int rb_valid = min(C::kRowAtomsB, p.n_row_atoms - rb0);
-      const uint32_t bytes = C::kABytes + C::kBBytes + C::kSfaBytes + rb_valid * C::kAtomsK * 512;
+      const uint32_t bytes = p.a_rows * kStageKBytes + C::kBBytes + C::kSfaBytes +
+                             rb_valid * C::kAtomsK * 512;
       for (int ks = k0; ks < k1; ++ks, ++it) {
         const uint32_t s = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1u;
@@ -299,6 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ready = mbar_wait(smem_u32(&tfull[acc]), aph, abort, p.status);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
+      // The last tile is stored after the final MMA: the stage ring is idle
+      // then and holds one staging buffer per box, so no box waits for the
+      // store of an earlier one.
+      const bool last = u + static_cast<int>(gridDim.x) >= p.num_units;
       const int row0 = mt * kBM + q * 32;          // first row of this warp's box
       const bool rows_ok = row0 < p.m;             // M % 32 == 0: all or none
       const int y = p.partial ? sp * p.m + row0 : row0;
@@ -332,11 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kChunk; ++j) f[j] = __fmul_rn(f[j], alpha);
         }
-        // The box stored from this staging buffer last time must have left it.
-        uint8_t *stage_buf = stage_base + (nbox % C::kStagingBufs) * kStagingBytes;
-        ++nbox;
-        if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
-        __syncwarp();
+        uint8_t *stage_buf;
+        if (last) {
+          stage_buf = smem + ((warp - 2) * kChunks + c) * kStagingBytes;
+        } else {
+          // The box stored from this staging buffer last time must have left it.
+          stage_buf = stage_base + (nbox % C::kStagingBufs) * kStagingBytes;
+          ++nbox;
+          if (lane == 0) bulk_wait_group_read<C::kStagingBufs - 1>();
+          __syncwarp();
+        }
         uint4 v[4];
         if constexpr (kChunk == 32) {
 #pragma unroll
@@ -458,6 +480,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.n_row_atoms = static_cast<int>((g.n + 127) / 128);
   p.partial = g.split_k > 1 ? 1 : 0;
   p.num_units = p.m_tiles * p.n_tiles * p.splits;
+  p.a_rows = static_cast<int>(g.m);  // the A map's box is M rows (M <= 128 here)
   const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
   e = launch_pdl(gemm_kernel<FMT, BN, OUT_F32>, dim3(grid), dim3(kThreads), C::kSmemBytes, s,
                  *g.tmap_a, *g.tmap_b, *g.tmap_d, p);

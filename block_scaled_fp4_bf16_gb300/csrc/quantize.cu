@@ -30,6 +30,10 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 256;
+// NVFP4 pass 2: 16-element blocks per thread (loaded together, then
+// quantized), so that each CTA's reduction of the partial maxima to s_t is
+// shared by 2 x 256 blocks.
+constexpr int kNvBlocksPerThread = 2;
 
 // q = n / d for 32-bit n, by a 64-bit multiply-high: m = floor((2^64-1)/d) + 1.
 struct FastDiv {
@@ -62,7 +66,8 @@ __device__ __forceinline__ uint32_t tiled_offset(uint32_t r, uint32_t c, uint32_
 
 // One tensor of a quantize launch.  Its scale blocks (rows padded to 128 in
 // the tiled order) are numbered b = 0..total-1 and handled by the CTAs
-// first_cta .. first_cta + ceil(total / kThreads) - 1 of the grid.
+// first_cta .. first_cta + ceil(total / (kThreads * blocks per thread)) - 1
+// of the grid (1 block per thread for MXFP4, kNvBlocksPerThread for NVFP4).
 struct QTensor {
   const uint16_t *x;            // BF16 bits [rows, cols], row stride ld
   uint8_t *codes;               // [rows, cols / 2]
@@ -84,29 +89,31 @@ struct QGroup {
   QTensor t[kQuantizeGroupMax];
 };
 
-// The tensor of this CTA: the last one whose first CTA is <= blockIdx.x.
-__device__ __forceinline__ const QTensor &group_member(const QGroup &g) {
+// The tensor of grid CTA `cta`: the last one whose first CTA is <= cta.
+__device__ __forceinline__ const QTensor &group_member(const QGroup &g, uint32_t cta) {
   int i = 0;
 #pragma unroll
   for (int k = 1; k < kQuantizeGroupMax; ++k)
-    if (k < g.count && blockIdx.x >= g.t[k].first_cta) i = k;
+    if (k < g.count && cta >= g.t[k].first_cta) i = k;
   return g.t[i];
 }
 
 // 32 bytes from global memory (read-only path): one 32-byte load when the
-// address is 32-byte aligned (WIDE), else two 16-byte loads.
+// address is 32-byte aligned (WIDE), else two 16-byte loads.  Not volatile:
+// the input does not change while a kernel runs, and the compiler may then
+// issue a thread's loads together before their data is used.
 template <bool WIDE>
 __device__ __forceinline__ void load32(const void *p, uint32_t *w) {
   if constexpr (WIDE) {
-    asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
                    "=r"(w[6]), "=r"(w[7])
                  : "l"(p));
   } else {
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                  : "l"(p));
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
                  : "l"(static_cast<const uint8_t *>(p) + 16));
   }
@@ -169,7 +176,7 @@ template <bool WIDE>
 __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
-  const QTensor &t = group_member(g);
+  const QTensor &t = group_member(g, blockIdx.x);
   const uint32_t b = (blockIdx.x - t.first_cta) * kThreads + threadIdx.x;
   if (b >= t.total) return;
   const uint32_t kb = t.kbdiv.d;
@@ -211,12 +218,24 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const __grid_const
   griddep_wait();
   const QTensor &t = g.t[blockIdx.y];
   uint32_t m = 0;
-  for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < t.real_total;
-       b += gridDim.x * kThreads) {
+  const uint32_t stride = gridDim.x * kThreads;
+  uint32_t b = blockIdx.x * kThreads + threadIdx.x;
+  // four loads in flight per thread, then the remainder one by one
+  for (; b + 3 * stride < t.real_total; b += 4 * stride) {
+    uint32_t w[4][8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t bq = b + q * stride;
+      const uint32_t r = fast_div(bq, t.kbdiv);
+      load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + (bq - r * t.kbdiv.d) * 16u, w[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = max(m, block_amax<8>(w[q]));
+  }
+  for (; b < t.real_total; b += stride) {
     const uint32_t r = fast_div(b, t.kbdiv);
-    const uint32_t j = b - r * t.kbdiv.d;
     uint32_t w[8];
-    load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + j * 16u, w);
+    load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + (b - r * t.kbdiv.d) * 16u, w);
     m = max(m, block_amax<8>(w));
   }
 #pragma unroll
@@ -304,14 +323,35 @@ __device__ __forceinline__ uint32_t div_to_e2m1x8_ieee(const uint32_t *w, float 
 // NVFP4 pass 2: every CTA reduces its tensor's partial maxima to s_t, then
 // thread b quantizes 16-element block b.  Each binary32 step of the
 // definition is one round-to-nearest operation (correctly rounded divisions
-// where it divides).
+// where it divides).  The CTAs take the blocks in the reverse of the order in
+// which pass 1 swept them, so the first blocks quantized are the ones pass 1
+// read last, which are still in L2.
 template <bool WIDE>
-__global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const __grid_constant__ QGroup g) {
+__global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
-  const QTensor &t = group_member(g);
+  const uint32_t cta = gridDim.x - 1 - blockIdx.x;
+  const QTensor &t = group_member(g, cta);
+  // The thread's blocks are loaded first: their latency then overlaps the
+  // reduction of the partial maxima below, which they do not depend on.
+  const uint32_t kb = t.kbdiv.d;
+  const uint32_t base = (cta - t.first_cta) * (kThreads * kNvBlocksPerThread) + threadIdx.x;
+  uint8_t *__restrict__ scales = t.scales;
+  uint32_t w[kNvBlocksPerThread][8];
+  uint32_t rq[kNvBlocksPerThread], jq[kNvBlocksPerThread];
+#pragma unroll
+  for (int q = 0; q < kNvBlocksPerThread; ++q) {
+    const uint32_t b = base + q * kThreads;
+    rq[q] = fast_div(b, t.kbdiv);
+    jq[q] = b - rq[q] * kb;
+    if (b < t.total && rq[q] < t.rows)
+      load32<WIDE>(t.x + static_cast<int64_t>(rq[q]) * t.ld + jq[q] * 16u, w[q]);
+  }
   __shared__ uint32_t warp_max[kThreads / 32];
   __shared__ float s_t_shared;
+  // den = E4M3(sb) * s_t and RN(1 / den) for every scale byte sb (0 marks a
+  // den outside [2^-100, 2^100], where the IEEE division is used instead)
+  __shared__ float den_tab[128], rcp_tab[128];
   {
     uint32_t m = 0;
     for (int i = threadIdx.x; i < kAmaxPartials; i += kThreads) m = max(m, t.partials[i]);
@@ -325,45 +365,64 @@ __global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const __grid_c
       const float amax_t = __uint_as_float(v << 16);
       const float s_t = __fdiv_rn(amax_t, 2688.0f);
       s_t_shared = s_t;
-      if (blockIdx.x == t.first_cta) *t.tensor_scale = s_t;
+      if (cta == t.first_cta) *t.tensor_scale = s_t;
     }
     __syncthreads();
   }
   const float s_t = s_t_shared;
   const float six_s_t = __fmul_rn(6.0f, s_t);
-
-  const uint32_t b = (blockIdx.x - t.first_cta) * kThreads + threadIdx.x;
-  if (b >= t.total) return;
-  const uint32_t kb = t.kbdiv.d;
-  const uint32_t r = fast_div(b, t.kbdiv);
-  const uint32_t j = b - r * kb;
-  uint8_t *__restrict__ scales = t.scales;
-  uint32_t sb = 0;
-  if (r < t.rows) {
-    uint32_t w[8];
-    load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + j * 16u, w);
-    const uint32_t amax = block_amax<8>(w);
-    if (s_t > 0.0f) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(amax << 16), six_s_t));
-    uint2 out = make_uint2(0u, 0u);
-    if (sb != 0) {
-      const float den = __fmul_rn(e4m3_to_f32(sb), s_t);
-      if (den >= 0x1p-100f && den <= 0x1p+100f) {
-        const float rc = rcp_rn(den);
-        out.x = div_to_e2m1x8(&w[0], den, rc);
-        out.y = div_to_e2m1x8(&w[4], den, rc);
-      } else {
-        out.x = div_to_e2m1x8_ieee(&w[0], den);
-        out.y = div_to_e2m1x8_ieee(&w[4], den);
-      }
-    }
-    *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
+  if (threadIdx.x < 128) {
+    const float den = __fmul_rn(e4m3_to_f32(threadIdx.x), s_t);
+    den_tab[threadIdx.x] = den;
+    rcp_tab[threadIdx.x] = (den >= 0x1p-100f && den <= 0x1p+100f) ? rcp_rn(den) : 0.0f;
   }
-  if (t.tiled) {
-    scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sb);
-    if (j == kb - 1)
-      for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
-  } else {
-    scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
+  // amax_b / (6 s_t) is taken the same way: RN(amax_b * r6) and one FMA
+  // correction give the correctly rounded quotient (Markstein) while 6 s_t
+  // stays in [2^-100, 2^100].  A quotient small enough for the correction to
+  // be inexact (fp32 subnormal) gives sb = 0 either way.
+  const bool six_ok = six_s_t >= 0x1p-100f && six_s_t <= 0x1p+100f;
+  const float r6 = six_ok ? rcp_rn(six_s_t) : 0.0f;
+  __syncthreads();
+
+#pragma unroll
+  for (int q = 0; q < kNvBlocksPerThread; ++q) {
+    if (base + q * kThreads >= t.total) continue;
+    const uint32_t r = rq[q], j = jq[q];
+    uint32_t sb = 0;
+    if (r < t.rows) {
+      const uint32_t amax = block_amax<8>(w[q]);
+      if (s_t > 0.0f) {
+        const float a = __uint_as_float(amax << 16);
+        float q6;
+        if (six_ok) {
+          const float q0 = __fmul_rn(a, r6);
+          q6 = __fmaf_rn(__fmaf_rn(-q0, six_s_t, a), r6, q0);
+        } else {
+          q6 = __fdiv_rn(a, six_s_t);
+        }
+        sb = cvt_e4m3(q6);
+      }
+      uint2 out = make_uint2(0u, 0u);
+      if (sb != 0) {
+        const float den = den_tab[sb];
+        const float rc = rcp_tab[sb];
+        if (rc != 0.0f) {
+          out.x = div_to_e2m1x8(&w[q][0], den, rc);
+          out.y = div_to_e2m1x8(&w[q][4], den, rc);
+        } else {
+          out.x = div_to_e2m1x8_ieee(&w[q][0], den);
+          out.y = div_to_e2m1x8_ieee(&w[q][4], den);
+        }
+      }
+      *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
+    }
+    if (t.tiled) {
+      scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sb);
+      if (j == kb - 1)
+        for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
+    } else {
+      scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
+    }
   }
 }
 
@@ -419,7 +478,8 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
     t.katoms = (kb + 3) / 4;
     t.kbdiv = make_fastdiv(kb);
     t.tiled = a.tiled;
-    ctas += (t.total + kThreads - 1) / kThreads;
+    const uint32_t per_cta = kThreads * (fmt == 0 ? 1u : static_cast<uint32_t>(kNvBlocksPerThread));
+    ctas += (t.total + per_cta - 1) / per_cta;
     wide = wide && wide_ok(a.x, a.ld);
   }
   cudaError_t e;

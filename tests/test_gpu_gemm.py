@@ -118,6 +118,17 @@ def test_single_cta_wide_tile_path():
     _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=False, split_k=1)
 
 
+@pytest.mark.parametrize("m,n,k,split_k,out_fp32", [
+    (32, 2304, 4096, 1, True), (32, 2304, 4096, 3, False), (32, 640, 1024, 0, True),
+    (64, 1024, 1024, 2, False), (96, 640, 768, 1, True), (32, 78848, 256, 1, False)])
+def test_mxfp4_m_up_to_128_partial_a_tile(m, n, k, split_k, out_fp32):
+    """The single-CTA kernel (M <= 128) loads only the M rows of A per stage and
+    keeps rows M..127 of its tile at zero: M = 32, 64 and 96, with and without
+    split-K, both output types, and the 256-column tile (N = 78848)."""
+    a, sa, b, sb = _codes_case(m, n, k, seed=m * 7 + n + k)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32, split_k=split_k)
+
+
 def test_skinny_32x8192x8192_split_k_full():
     """Decode-shaped skinny GEMM with split-K: every output against the oracle,
     and bit-identical across runs (fixed reduction order)."""
@@ -164,7 +175,8 @@ def test_mlp_up_16384x28672x8192_bf16_sampled():
 
 @pytest.mark.parametrize("m,n,k,split_k", [(128, 128, 256, 1), (256, 320, 1024, 1),
                                            (160, 4096, 512, 1), (64, 512, 2048, 3),
-                                           (416, 352, 2048, 3)])
+                                           (416, 352, 2048, 3), (32, 640, 1024, 1),
+                                           (32, 640, 1024, 3)])
 def test_nvfp4_gemm_small(m, n, k, split_k):
     xa = synth.bf16_normal(m, k, 1.0, seed=m * 3 + k)
     xb = synth.bf16_normal(n, k, 1.0, seed=n * 5 + k)
