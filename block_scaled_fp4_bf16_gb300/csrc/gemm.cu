@@ -93,22 +93,29 @@ struct Params {
   int partial;                 // 1: write FP32 partials of split s at rows s*M + m
   int num_units;
   int a_rows;                  // rows of A loaded per stage (= M, a multiple of 32, <= 128)
+  FastDiv div_tiles;           // by m_tiles * n_tiles
+  FastDiv div_group;           // by 8 * n_tiles
+  FastDiv div_last;            // by m_tiles % 8
 };
 
 // Unit -> (m tile, n tile, split); tiles are walked in groups of 8 M tiles
 // so that concurrently running CTAs share A and B panels in L2.
 __device__ __forceinline__ void decode_unit(const Params &p, int u, int &mt, int &nt, int &sp) {
+  // (multiply-high divisions: this runs before every tile in three roles)
   const int tiles = p.m_tiles * p.n_tiles;
-  sp = u / tiles;
+  sp = static_cast<int>(fast_div(static_cast<uint32_t>(u), p.div_tiles));
   const int t = u - sp * tiles;
   constexpr int kGroup = 8;
-  const int per_group = kGroup * p.n_tiles;
-  const int g = t / per_group;
+  const int g = static_cast<int>(fast_div(static_cast<uint32_t>(t), p.div_group));
   const int first_m = g * kGroup;
-  const int gsize = min(kGroup, p.m_tiles - first_m);
-  const int r = t - g * per_group;
-  mt = first_m + r % gsize;
-  nt = r / gsize;
+  const int r = t - g * kGroup * p.n_tiles;
+  if (p.m_tiles - first_m >= kGroup) {
+    mt = first_m + (r & (kGroup - 1));
+    nt = r / kGroup;
+  } else {
+    nt = static_cast<int>(fast_div(static_cast<uint32_t>(r), p.div_last));
+    mt = first_m + r - nt * (p.m_tiles - first_m);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -159,8 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // zero rows, whose outputs are not stored).  B scale atoms past the end of
   // N are never loaded either: they are made 0 (2^-127 or 0.0, both finite).
   for (int s = 0; s < C::kStages; ++s) {
-    uint32_t *a_tail = reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + p.a_rows * kStageKBytes);
-    for (int i = threadIdx.x; i < (kBM - p.a_rows) * kStageKBytes / 4; i += kThreads) a_tail[i] = 0u;
+    uint4 *a_tail = reinterpret_cast<uint4 *>(smem + s * C::kStageBytes + p.a_rows * kStageKBytes);
+    for (int i = threadIdx.x; i < (kBM - p.a_rows) * kStageKBytes / 16; i += kThreads)
+      a_tail[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   for (int s = 0; s < C::kStages; ++s) {
     uint32_t *sfb = reinterpret_cast<uint32_t *>(smem + s * C::kStageBytes + C::kABytes +
@@ -480,6 +488,9 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.n_row_atoms = static_cast<int>((g.n + 127) / 128);
   p.partial = g.split_k > 1 ? 1 : 0;
   p.num_units = p.m_tiles * p.n_tiles * p.splits;
+  p.div_tiles = make_fastdiv(static_cast<uint32_t>(p.m_tiles * p.n_tiles));
+  p.div_group = make_fastdiv(static_cast<uint32_t>(8 * p.n_tiles));
+  p.div_last = make_fastdiv(static_cast<uint32_t>(p.m_tiles % 8));
   p.a_rows = static_cast<int>(g.m);  // the A map's box is M rows (M <= 128 here)
   const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
   e = launch_pdl(gemm_kernel<FMT, BN, OUT_F32>, dim3(grid), dim3(kThreads), C::kSmemBytes, s,

@@ -78,6 +78,9 @@ struct PairParams {
   int katoms;                  // scale atoms along K per 128-row tile
   int partial;                 // 1: FP32 partials of split s at rows s*M + m
   int num_units;
+  FastDiv div_tiles;           // by pm_tiles * n_tiles
+  FastDiv div_group;           // by 16 * n_tiles (the units of a group of 16 M tiles)
+  FastDiv div_last;            // by pm_tiles % 16 (the size of a last, partial group)
 };
 
 // Unit -> (256-row tile of M, 256-column tile of N, split), in groups of 16
@@ -86,17 +89,21 @@ struct PairParams {
 // per group.
 __device__ __forceinline__ void decode_unit(const PairParams &p, int u, int &pm, int &nt,
                                             int &sp) {
+  // (multiply-high divisions: this runs before every tile in three roles)
   const int tiles = p.pm_tiles * p.n_tiles;
-  sp = u / tiles;
+  sp = static_cast<int>(fast_div(static_cast<uint32_t>(u), p.div_tiles));
   const int t = u - sp * tiles;
   constexpr int kGroup = 16;
-  const int per_group = kGroup * p.n_tiles;
-  const int g = t / per_group;
+  const int g = static_cast<int>(fast_div(static_cast<uint32_t>(t), p.div_group));
   const int first = g * kGroup;
-  const int gsize = min(kGroup, p.pm_tiles - first);
-  const int r = t - g * per_group;
-  pm = first + r % gsize;
-  nt = r / gsize;
+  const int r = t - g * kGroup * p.n_tiles;
+  if (p.pm_tiles - first >= kGroup) {
+    pm = first + (r & (kGroup - 1));
+    nt = r / kGroup;
+  } else {
+    nt = static_cast<int>(fast_div(static_cast<uint32_t>(r), p.div_last));
+    pm = first + r - nt * (p.pm_tiles - first);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -438,6 +445,9 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.katoms = static_cast<int>(g.k / (FMT == 0 ? 128 : 64));
   p.partial = g.split_k > 1 ? 1 : 0;
   p.num_units = p.pm_tiles * p.n_tiles * p.splits;
+  p.div_tiles = make_fastdiv(static_cast<uint32_t>(p.pm_tiles * p.n_tiles));
+  p.div_group = make_fastdiv(static_cast<uint32_t>(16 * p.n_tiles));
+  p.div_last = make_fastdiv(static_cast<uint32_t>(p.pm_tiles % 16));
   const int clusters = p.num_units < max_clusters[dev] ? p.num_units : max_clusters[dev];
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.numAttrs = 2;  // cluster shape + programmatic stream serialization

@@ -10,6 +10,28 @@
 
 namespace mx {
 
+// q = n / d for 32-bit n by a 64-bit multiply-high, m = floor((2^64 - 1) / d)
+// + 1 (exact for every n < 2^32): the kernels divide by run-time constants
+// this way instead of by a 32-bit integer division, whose dependent
+// instruction chain costs a few hundred cycles.
+struct FastDiv {
+  uint32_t d;
+  unsigned long long m;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.m = d <= 1 ? 0ull : (~0ull / d) + 1ull;
+  return f;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
+  return f.d <= 1 ? n : static_cast<uint32_t>(__umul64hi(static_cast<unsigned long long>(n), f.m));
+}
+#endif
+
 // Number of partial maxima the NVFP4 amax pass writes (one per CTA).
 constexpr int kAmaxPartials = 512;
 

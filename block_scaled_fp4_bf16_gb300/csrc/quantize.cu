@@ -35,23 +35,6 @@ constexpr int kThreads = 256;
 // shared by 2 x 256 blocks.
 constexpr int kNvBlocksPerThread = 2;
 
-// q = n / d for 32-bit n, by a 64-bit multiply-high: m = floor((2^64-1)/d) + 1.
-struct FastDiv {
-  uint32_t d;
-  unsigned long long m;
-};
-
-FastDiv make_fastdiv(uint32_t d) {
-  FastDiv f;
-  f.d = d;
-  f.m = d <= 1 ? 0ull : (~0ull / d) + 1ull;
-  return f;
-}
-
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &f) {
-  return f.d <= 1 ? n : static_cast<uint32_t>(__umul64hi(static_cast<unsigned long long>(n), f.m));
-}
-
 // floor(log2 |x|) of a non-zero BF16 magnitude (15-bit pattern).
 __device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
   const uint32_t e = (mag >> 7) & 0xFFu;
