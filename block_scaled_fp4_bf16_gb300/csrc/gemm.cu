@@ -386,10 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<uint4 *>(stage_buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) = v[i];
+        if (last) continue;  // the last tile's boxes are stored together below
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_store_2d(&tmap_d, smem_u32(stage_buf), col0, y);
+          bulk_commit_group();
+        }
+      }
+      if (last && rows_ok) {
+        // One proxy fence for all the boxes of the last tile (a fence per box
+        // costs several hundred cycles, and here nothing waits in between).
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int c = 0; c < kChunks; ++c) {
+            const int col0 = nt * BN + c * kChunk;
+            if (col0 < p.n)
+              tma_store_2d(&tmap_d, smem_u32(smem + ((warp - 2) * kChunks + c) * kStagingBytes), col0, y);
+          }
           bulk_commit_group();
         }
       }
