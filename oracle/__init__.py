@@ -154,6 +154,24 @@ def mx_quantize(x_bits: np.ndarray):
     return codes, scales
 
 
+def mx_quantize_2d(x_bits: np.ndarray):
+    """Bidimensional MXFP4 quantize of BF16 bits [rows, cols] (rows, cols % 32 == 0).
+
+    Returns (codes, scales, codes_t, scales_t): the rowwise quantize of x
+    (blocks of 32 along a row) and the rowwise quantize of x transposed
+    (blocks of 32 down a column of x), the latter stored as [cols, rows/2]
+    codes and [cols, rows/32] scales.  This is the definition of the
+    "rowwise + columnwise" output of NVIDIA/TransformerEngine #3809
+    (NVFP4QuantizeBidimensionalG2RKernel: the columnwise result is the
+    transposed output, passed as (cols, rows)), applied to the MX rule.
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    assert x.shape[0] % 32 == 0 and x.shape[1] % 32 == 0
+    codes, scales = mx_quantize(x)
+    codes_t, scales_t = mx_quantize(np.ascontiguousarray(x.T))
+    return codes, scales, codes_t, scales_t
+
+
 def bf16_amax(x_bits: np.ndarray) -> float:
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     rows, cols = x.shape

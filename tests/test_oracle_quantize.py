@@ -116,6 +116,47 @@ def test_mx_nibble_order(oracle):
     assert codes[0, 0] == (15 << 4) | 2
 
 
+# ----------------------------------------------------------------- bidimensional MXFP4
+
+def test_mx_quantize_2d_columnwise_brute_force(oracle):
+    """The columnwise half against the independent brute-force quantizer run on
+    the columns (blocks of 32 down a column), stored transposed."""
+    x = synth.bf16_normal(96, 160, 1.0, seed=21)
+    x[32:64, 7] = 0                     # an all-zero column block
+    x[0:32, 9] = 0x8000                 # a column block of -0
+    codes, scales, codes_t, scales_t = oracle.mx_quantize_2d(x)
+    rc, rs = _brute_force_mx(x)
+    assert np.array_equal(_unpack(codes, 160), rc) and np.array_equal(scales, rs)
+    cc, cs = _brute_force_mx(np.ascontiguousarray(x.T))
+    assert codes_t.shape == (160, 48) and scales_t.shape == (160, 3)
+    assert np.array_equal(_unpack(codes_t, 96), cc) and np.array_equal(scales_t, cs)
+    assert scales_t[7, 1] == 0 and np.all(_unpack(codes_t, 96)[7, 32:64] == 0)
+    assert np.all(_unpack(codes_t, 96)[9, 0:32] == 8)
+
+
+def test_mx_quantize_2d_orientation(oracle):
+    """One non-zero element at (r, c): the rowwise code sits at row r, column c;
+    the columnwise code at row c, column r of the transposed output."""
+    r, c = 45, 70
+    x = np.zeros((64, 96), dtype=np.uint16)
+    x[r, c] = synth.f32_to_bf16_bits(np.array([-3.0], np.float32))[0]
+    codes, scales, codes_t, scales_t = oracle.mx_quantize_2d(x)
+    u, ut = _unpack(codes, 96), _unpack(codes_t, 64)
+    # amax 3 -> exponent floor(log2 3) - 2 = -1 -> scale 126; -3 * 2 = -6 -> code 15
+    assert u[r, c] == 15 and np.count_nonzero(u) == 1
+    assert ut[c, r] == 15 and np.count_nonzero(ut) == 1
+    assert scales[r, c // 32] == 126 and scales_t[c, r // 32] == 126
+    assert np.count_nonzero(scales) == 1 and np.count_nonzero(scales_t) == 1
+
+
+def test_mx_quantize_2d_symmetric_input(oracle):
+    """For a symmetric matrix the two directions give the same bytes."""
+    x = synth.bf16_normal(128, 128, 2.0, seed=22)
+    x = np.triu(x) + np.triu(x, 1).T
+    codes, scales, codes_t, scales_t = oracle.mx_quantize_2d(x)
+    assert np.array_equal(codes, codes_t) and np.array_equal(scales, scales_t)
+
+
 # ----------------------------------------------------------------- NVFP4
 
 def test_nvfp4_exact_regime_reduces_to_nearest_grid(oracle):
