@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.mx_quantize_bf16_group.restype = i32
         L.mx_quantize_bf16_group.argtypes = [ctypes.POINTER(mx_quantize_tensor), i32, i32, i32, vp,
                                              sz, vp]
+        L.mx_quantize_bf16_2d.restype = i32
+        L.mx_quantize_bf16_2d.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
         L.mx_scale_relayout.restype = i32
         L.mx_scale_relayout.argtypes = [vp, i64, i64, i32, vp, vp]
         L.mx_gemm_workspace_bytes.restype = sz
@@ -174,6 +176,13 @@ def mx_quantize_bf16_group(tensors, fmt, scale_layout, workspace=None, workspace
                                     _ptr(tensor_scale))
     return _check("mx_quantize_bf16_group", lib().mx_quantize_bf16_group(
         arr, len(tensors), fmt, scale_layout, _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def mx_quantize_bf16_2d(x, rows, cols, ld_x, fmt, scale_layout, codes, scales, codes_t, scales_t,
+                        stream=None):
+    return _check("mx_quantize_bf16_2d", lib().mx_quantize_bf16_2d(
+        _ptr(x), rows, cols, ld_x, fmt, scale_layout, _ptr(codes), _ptr(scales), _ptr(codes_t),
+        _ptr(scales_t), _stream(stream)))
 
 
 def mx_scale_relayout(plain, rows, cols, fmt, tiled, stream=None):

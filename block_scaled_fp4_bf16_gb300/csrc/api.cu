@@ -399,6 +399,44 @@ MX_API int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, 
                                              static_cast<cudaStream_t>(stream)));
 }
 
+MX_API int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                               int format, int scale_layout, void *codes, void *scales,
+                               void *codes_t, void *scales_t, void *stream) {
+  if (!x || !codes || !scales || !codes_t || !scales_t) return MX_ERR_INVALID_ARG;
+  if (!valid_format(format)) return MX_ERR_INVALID_ARG;
+  if (scale_layout != MX_SCALE_PLAIN && scale_layout != MX_SCALE_TCGEN05) return MX_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld_x < cols) return MX_ERR_INVALID_ARG;
+  if (format != MX_FMT_MXFP4) return MX_ERR_UNSUPPORTED_FEATURE;
+  if (rows % 32 != 0 || cols % 32 != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED_SHAPE;
+  if ((rows + 127) / 128 * 128 * (cols / 32) >= (int64_t(1) << 31) ||
+      (cols + 127) / 128 * 128 * (rows / 32) >= (int64_t(1) << 31))
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || (ld_x % 8) != 0 || !aligned16(codes) || !aligned16(scales) ||
+      !aligned16(codes_t) || !aligned16(scales_t))
+    return MX_ERR_ALIGNMENT;
+  // The two outputs are written concurrently from the same input: no output
+  // may overlap the input or another output.
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
+  const Range in{xb, xb + static_cast<uintptr_t>(((rows - 1) * ld_x + cols) * 2)};
+  const Range out[4] = {
+      {reinterpret_cast<uintptr_t>(codes), reinterpret_cast<uintptr_t>(codes) + static_cast<uintptr_t>(rows * cols / 2)},
+      {reinterpret_cast<uintptr_t>(scales), reinterpret_cast<uintptr_t>(scales) + mx_scale_bytes(rows, cols, format, scale_layout)},
+      {reinterpret_cast<uintptr_t>(codes_t), reinterpret_cast<uintptr_t>(codes_t) + static_cast<uintptr_t>(rows * cols / 2)},
+      {reinterpret_cast<uintptr_t>(scales_t), reinterpret_cast<uintptr_t>(scales_t) + mx_scale_bytes(cols, rows, format, scale_layout)}};
+  for (int o = 0; o < 4; ++o) {
+    if (overlap(out[o], in)) return MX_ERR_INVALID_ARG;
+    for (int p = o + 1; p < 4; ++p)
+      if (overlap(out[o], out[p])) return MX_ERR_INVALID_ARG;
+  }
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  return launch_rc(mx::launch_mx_quantize_2d(x, rows, cols, ld_x, scale_layout == MX_SCALE_TCGEN05,
+                                             codes, scales, codes_t, scales_t,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format,
                              void *tiled, void *stream) {
   if (!plain || !tiled || !valid_format(format)) return MX_ERR_INVALID_ARG;

@@ -57,6 +57,11 @@ constexpr int kQuantizeGroupMax = 8;
 // MXFP4, 1 NVFP4.  Each NVFP4 tensor has its own kAmaxPartials partials.
 cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int count,
                                   cudaStream_t s);
+// Bidimensional MXFP4 quantize: rowwise codes/scales of x and of x^T (rows,
+// cols % 32 == 0).
+cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld, int tiled,
+                                  void *codes, void *scales, void *codes_t, void *scales_t,
+                                  cudaStream_t s);
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
                                   cudaStream_t s);
 

@@ -157,6 +157,26 @@ int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, int for
                            int scale_layout, void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/* ---- bidimensional quantize ----------------------------------------------
+ * Rowwise + columnwise MXFP4 quantize in one pass (NVIDIA/TransformerEngine
+ * #3809: the bidimensional quantize kernel, whose columnwise result is the
+ * transposed output, passed as (cols, rows)).  The columnwise codes of x are
+ * the rowwise codes of x^T, i.e. the B operand that a TN GEMM needs to
+ * multiply by x^T (a weight's transpose, or the other operand of a backward
+ * GEMM).
+ *   x:        BF16 [rows, cols], row stride ld_x elements (ld_x >= cols,
+ *             ld_x % 8 == 0); rows % 32 == 0 and cols % 32 == 0.
+ *   codes, scales:     out, exactly what mx_quantize_bf16 writes for x.
+ *   codes_t, scales_t: out, exactly what mx_quantize_bf16 writes for x^T:
+ *             codes_t [cols, rows / 2] bytes, scales_t
+ *             mx_scale_bytes(cols, rows, format, scale_layout) bytes.
+ * format: MX_FMT_MXFP4 only (MX_FMT_NVFP4 -> MX_ERR_UNSUPPORTED_FEATURE).
+ * No output may overlap the input or another output (MX_ERR_INVALID_ARG).
+ * Launches one kernel; each element of x is read from memory once. */
+int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
+                        int scale_layout, void *codes, void *scales, void *codes_t,
+                        void *scales_t, void *stream);
+
 /* Plain scales [rows, cols / block] -> MX_SCALE_TCGEN05 order (see
  * mx_scale_bytes).  `tiled` receives mx_scale_bytes(rows, cols, format,
  * MX_SCALE_TCGEN05) bytes, padding included ("Integrate MXFP4 hipblaslt GEMM

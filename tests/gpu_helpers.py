@@ -79,6 +79,25 @@ def gpu_quantize_group(xs, fmt: int, layout: int, lds=None):
              None if ts is None else np.float32(ts.item())) for rows, cols, codes, scales, ts in outs]
 
 
+def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None):
+    """Bidimensional MXFP4 quantize on the GPU; returns host (codes, scales,
+    codes_t, scales_t), outputs pre-filled with 0xAB."""
+    rows, cols = x_bits.shape
+    ld = cols if ld is None else ld
+    padded = np.zeros((rows, ld), np.uint16)
+    padded[:, :cols] = x_bits
+    x = dev_bf16(padded)
+    fill = lambda n: torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")
+    fmt = mx.MX_FMT_MXFP4
+    codes, codes_t = fill(rows * cols // 2), fill(rows * cols // 2)
+    scales = fill(mx.mx_scale_bytes(rows, cols, fmt, layout))
+    scales_t = fill(mx.mx_scale_bytes(cols, rows, fmt, layout))
+    mx.mx_quantize_bf16_2d(x, rows, cols, ld, fmt, layout, codes, scales, codes_t, scales_t)
+    torch.cuda.synchronize()
+    return (codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(),
+            codes_t.cpu().numpy().reshape(cols, rows // 2), scales_t.cpu().numpy())
+
+
 def gpu_relayout(plain: np.ndarray, rows: int, cols: int, fmt: int) -> torch.Tensor:
     tiled = torch.full((mx.mx_scale_bytes(rows, cols, fmt, mx.MX_SCALE_TCGEN05),), 0xAB,
                        dtype=torch.uint8, device="cuda")

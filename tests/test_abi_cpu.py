@@ -155,6 +155,30 @@ def test_group_quantize_argument_validation(lib):
     assert _group(lib, [n0, n1], fmt=1, ws=FAKE + 2 * MB, wsb=wsb) == mx.MX_ERR_INVALID_ARG
 
 
+def test_quantize_2d_argument_validation(lib):
+    MB = 1 << 20
+    q = lib.mx_quantize_bf16_2d
+    ok = dict(x=FAKE, rows=64, cols=96, ld=96, fmt=0, lay=1, c=FAKE + MB, s=FAKE + 2 * MB,
+              ct=FAKE + 3 * MB, st=FAKE + 4 * MB)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return q(a["x"], a["rows"], a["cols"], a["ld"], a["fmt"], a["lay"], a["c"], a["s"], a["ct"],
+                 a["st"], None)
+    assert call(x=None) == mx.MX_ERR_INVALID_ARG
+    assert call(ct=None) == mx.MX_ERR_INVALID_ARG
+    assert call(ld=64) == mx.MX_ERR_INVALID_ARG
+    assert call(lay=3) == mx.MX_ERR_INVALID_ARG
+    assert call(fmt=1) == mx.MX_ERR_UNSUPPORTED_FEATURE          # NVFP4 not provided
+    assert call(rows=48) == mx.MX_ERR_UNSUPPORTED_SHAPE           # rows % 32
+    assert call(cols=80, ld=80) == mx.MX_ERR_UNSUPPORTED_SHAPE    # cols % 32
+    assert call(st=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
+    assert call(ld=100) == mx.MX_ERR_ALIGNMENT                    # ld % 8
+    assert call(ct=FAKE + MB + 64) == mx.MX_ERR_INVALID_ARG       # codes_t overlaps codes
+    assert call(c=FAKE + 1024) == mx.MX_ERR_INVALID_ARG           # codes overlap the input
+
+
 def test_relayout_and_selftest_validation(lib):
     assert lib.mx_scale_relayout(None, 4, 32, 0, FAKE, None) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_scale_relayout(FAKE, 4, 40, 0, FAKE, None) == mx.MX_ERR_UNSUPPORTED_SHAPE

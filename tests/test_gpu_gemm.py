@@ -10,6 +10,7 @@ import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
 from tests.gpu_helpers import (bf16_bits_to_f64, check_bf16, check_fp32, dev_u8, gpu_gemm,
+                               gpu_quantize_2d,
                                gpu_quantize, gpu_relayout, sample_indices)
 
 pytestmark = pytest.mark.gpu
@@ -140,6 +141,23 @@ def test_skinny_32x8192x8192_split_k_full():
                   oracle.scale_tile(w["b_scales"]), m, n, k, out_fp32=False, split_k=0)
     assert np.array_equal(d1, d2)
     assert mx.mx_gemm_workspace_bytes(m, n, k, 0) > 0   # split-K is in use
+
+
+def test_backward_gemm_with_columnwise_codes():
+    """dX = dY . W through the TN GEMM: A = rowwise codes of dY [M, N], B = the
+    columnwise codes of W [N, K] (the rowwise codes of W^T) from the
+    bidimensional quantize; against the oracle GEMM on the oracle's codes."""
+    m, n, k = 256, 512, 768
+    dy = synth.bf16_normal(m, n, 1.0, seed=51)
+    w = synth.bf16_normal(n, k, 0.02, seed=52)
+    ca, sa_t, _ = gpu_quantize(dy, MX, TILED)
+    _, _, cwt, swt = gpu_quantize_2d(w, TILED)
+    ra, rsa = oracle.mx_quantize(dy)
+    _, _, rwt, rswt = oracle.mx_quantize_2d(w)
+    assert np.array_equal(ca, ra) and np.array_equal(cwt, rwt)
+    d = gpu_gemm(MX, ca, sa_t, cwt, swt, m, k, n, out_fp32=False)
+    ref, s_abs = oracle.mx_gemm(ra, rsa, rwt, rswt, m, k, n)
+    check_bf16(d, ref, s_abs, "dgrad with columnwise codes")
 
 
 def _quant_gemm_check(name, n_rows, n_cols):

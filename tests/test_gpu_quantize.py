@@ -6,7 +6,7 @@ import pytest
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import gpu_quantize, gpu_quantize_group, gpu_relayout
+from tests.gpu_helpers import gpu_quantize, gpu_quantize_2d, gpu_quantize_group, gpu_relayout
 
 pytestmark = pytest.mark.gpu
 
@@ -240,3 +240,43 @@ def test_quantize_group_at_the_quantize_gemm_workload_size():
         rc, rs = oracle.mx_quantize(x)
         assert np.array_equal(codes, rc)
         assert np.array_equal(scales, oracle.scale_tile(rs))
+
+
+# ---- bidimensional quantize: rowwise and columnwise outputs byte-equal ------
+
+def _check_2d(x, layout, ld=None):
+    codes, scales, codes_t, scales_t = gpu_quantize_2d(x, layout, ld=ld)
+    rc, rs, rct, rst = oracle.mx_quantize_2d(x)
+    assert np.array_equal(codes, rc), "rowwise codes: " + _explain(x, codes, rc, scales, rs, 32)
+    assert np.array_equal(codes_t, rct), "columnwise codes: " + _explain(
+        np.ascontiguousarray(x.T), codes_t, rct, scales_t, rst, 32)
+    if layout == PLAIN:
+        assert np.array_equal(scales, rs.ravel()) and np.array_equal(scales_t, rst.ravel())
+    else:
+        assert np.array_equal(scales, oracle.scale_tile(rs))
+        assert np.array_equal(scales_t, oracle.scale_tile(rst))
+
+
+@pytest.mark.parametrize("rows,cols", [(32, 32), (64, 96), (96, 256), (128, 512), (160, 288),
+                                       (544, 1024), (256, 4096), (4096, 288)])
+@pytest.mark.parametrize("layout", [PLAIN, TILED])
+def test_mx_quantize_2d_matches_oracle(rows, cols, layout):
+    x = synth.bf16_normal(rows, cols, 1.0, seed=rows * 7 + cols)
+    x[0, :32] = 0                                     # zero row block
+    x[:32, min(5, cols - 1)] = 0x8000                 # column block of -0
+    _check_2d(x, layout)
+
+
+def test_mx_quantize_2d_leading_dim_and_special_values():
+    x = synth.bf16_normal(96, 160, 3.0, seed=41)
+    x[2, :] = synth.f32_to_bf16_bits(np.full(160, 1e-40, np.float32))   # subnormals
+    x[:, 3] = 0x7F7F                                                   # largest finite
+    x[40:64, 70] = 0x0001
+    _check_2d(x, TILED, ld=168)                      # 16-byte (not 32-byte) aligned rows
+    _check_2d(x, PLAIN, ld=256)
+
+
+def test_mx_quantize_2d_full_size_weight():
+    """The 4096 x 4096 weight of the quantize+GEMM workload."""
+    w = synth.workload_inputs("quant_gemm_2048x4096x4096")
+    _check_2d(w["b"], TILED)
