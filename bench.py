@@ -6,11 +6,12 @@
 
 A step is one pass of the whole hot path over one batch of synthetic input.
 For the default workload (BF16 activations 2048x4096 and weights 4096x4096,
-quantized to MXFP4 and multiplied, BF16 out) a step is: quantize A, quantize
-W (scales written straight into the tcgen05 tile order), GEMM.  `value` is
-2*M*N*K per step over the device time of the step, in TFLOP/s; the GEMM
-kernel alone and the quantizer's GB/s are reported beside it with their
-roofline fractions.
+quantized to MXFP4 and multiplied, BF16 out) a step is: one grouped quantize
+of A and W (scales written straight into the tcgen05 tile order), then the
+GEMM.  `value` is 2*M*N*K per step over the device time of the step, in
+TFLOP/s; the GEMM kernel alone and the quantizer's GB/s are reported beside it
+with their roofline fractions.  The quant2d workload (a bidimensional quantize,
+no GEMM) reports GB/s of algorithmic bytes instead.
 
 Timing: inputs are resident in HBM; the K steps are replayed from CUDA graphs
 (each holding one step per rotating input set) between two CUDA events on the
@@ -182,12 +183,14 @@ class DeviceWorkload:
         dev = "cuda"
         u8 = torch.uint8
         sa_bytes = mx.mx_scale_bytes(m, k, self.fmt, mx.MX_SCALE_TCGEN05)
-        sb_bytes = mx.mx_scale_bytes(n, k, self.fmt, mx.MX_SCALE_TCGEN05)
-        wsb = mx.mx_gemm_workspace_bytes(m, n, k, self.split_k)
+        sb_bytes = mx.mx_scale_bytes(n, k, self.fmt, mx.MX_SCALE_TCGEN05) if n else 0
+        wsb = mx.mx_gemm_workspace_bytes(m, n, k, self.split_k) if n else 0
         out_dt = torch.bfloat16 if self.out == mx.MX_OUT_BF16 else torch.float32
         if self.kind == "bf16":
             ha = torch.from_numpy(host_inputs["a"].view(np.int16)).view(torch.bfloat16)
             hb = torch.from_numpy(host_inputs["b"].view(np.int16)).view(torch.bfloat16)
+        elif self.kind == "quant2d":
+            ha = torch.from_numpy(host_inputs["a"].view(np.int16)).view(torch.bfloat16)
         else:
             tiled = {}
             for key, rows in (("a", m), ("b", n)):
@@ -198,6 +201,15 @@ class DeviceWorkload:
                 tiled[key] = t
         for _ in range(nsets):
             s = {}
+            if self.kind == "quant2d":
+                s["x_a"] = ha.to(dev)
+                s["codes_a"] = torch.empty(m * k // 2, dtype=u8, device=dev)
+                s["sf_a"] = torch.empty(sa_bytes, dtype=u8, device=dev)
+                s["codes_t"] = torch.empty(m * k // 2, dtype=u8, device=dev)
+                s["sf_t"] = torch.empty(mx.mx_scale_bytes(k, m, self.fmt, mx.MX_SCALE_TCGEN05),
+                                        dtype=u8, device=dev)
+                self.sets.append(s)
+                continue
             if self.kind == "bf16":
                 s["x_a"] = ha.to(dev)
                 s["x_b"] = hb.to(dev)
@@ -227,6 +239,11 @@ class DeviceWorkload:
         mx = self.mx
         m, n, k, fmt = self.m, self.n, self.k, self.fmt
         out = []
+        if self.kind == "quant2d":
+            def q2d(s, st):
+                mx.mx_quantize_bf16_2d(s["x_a"], m, k, k, fmt, mx.MX_SCALE_TCGEN05, s["codes_a"],
+                                       s["sf_a"], s["codes_t"], s["sf_t"], stream=st)
+            return [("quantize_2d", q2d)]
         if self.kind == "bf16":
             # the activation and the weight in one grouped quantize call
             def q(s, st):
@@ -250,6 +267,8 @@ class DeviceWorkload:
     def kernels_per_call(self):
         """Kernel launches of each call of the step (matches the library's launches)."""
         mx = self.mx
+        if self.kind == "quant2d":
+            return {"quantize_2d": 1}
         q = 1 if self.fmt == mx.MX_FMT_MXFP4 else 2
         g = 1 + (1 if mx.mx_gemm_workspace_bytes(self.m, self.n, self.k, self.split_k) else 0)
         res = {"gemm": g}
@@ -261,6 +280,9 @@ class DeviceWorkload:
         """Algorithmic work of each call: (bytes, flops)."""
         m, n, k = self.m, self.n, self.k
         blk = 32 if self.fmt == self.mx.MX_FMT_MXFP4 else 16
+        if self.kind == "quant2d":
+            # BF16 read once, codes and scales written for x and for x^T
+            return {"quantize_2d": (m * k * (2 + 2 * (0.5 + 1.0 / blk)), 0.0)}
         amax_pass = 0 if self.fmt == self.mx.MX_FMT_MXFP4 else 2
         qbytes = lambda r: r * k * (2 + amax_pass + 0.5 + 1.0 / blk)
         out_b = 2 if self.out == self.mx.MX_OUT_BF16 else 4
@@ -368,17 +390,21 @@ def time_e2e(wl, host_inputs, steps):
     torch = wl.torch
     s0 = wl.sets[0]
     pinned = {}
-    if wl.kind == "bf16":
+    if wl.kind in ("bf16", "quant2d"):
         pinned["x_a"] = torch.from_numpy(host_inputs["a"].view(np.int16)).view(
             torch.bfloat16).pin_memory()
+    if wl.kind == "bf16":
         pinned["x_b"] = torch.from_numpy(host_inputs["b"].view(np.int16)).view(
             torch.bfloat16).pin_memory()
-    else:
+    elif wl.kind == "codes":
         pinned["codes_a"] = torch.from_numpy(host_inputs["a_codes"]).pin_memory()
         pinned["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).pin_memory()
-    d_host = torch.empty(s0["d"].shape, dtype=s0["d"].dtype).pin_memory()
+    # the step's result read back: D, or both code outputs of the quant2d step
+    result_keys = ["codes_a", "codes_t"] if wl.kind == "quant2d" else ["d"]
+    results = {key: torch.empty(s0[key].shape, dtype=s0[key].dtype).pin_memory()
+               for key in result_keys}
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = d_host.numel() * d_host.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in results.values())
     stream = torch.cuda.Stream()
 
     def one(i):
@@ -387,7 +413,8 @@ def time_e2e(wl, host_inputs, steps):
             s[key].view(-1).copy_(t.view(-1), non_blocking=True)
         for _, fn in wl.calls():
             fn(s, stream.cuda_stream)
-        d_host.copy_(s["d"], non_blocking=True)
+        for key, t in results.items():
+            t.copy_(s[key], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -413,6 +440,10 @@ def oracle_step_sample(name, host, frac, prepared):
     mr = max(1, int(round(m * frac)))
     nr = max(1, int(round(n * frac)))
     t0 = time.perf_counter()
+    if w["kind"] == "quant2d":
+        mr = max(32, mr // 32 * 32)
+        oracle.mx_quantize_2d(host["a"][:mr])
+        return time.perf_counter() - t0, mr / m
     if w["kind"] == "bf16":
         if w["fmt"] == "mxfp4":
             oracle.mx_quantize(host["a"][:mr])
@@ -433,7 +464,7 @@ def oracle_step_sample(name, host, frac, prepared):
 def oracle_prepare(name, host):
     import oracle
     w = synth.WORKLOADS[name]
-    if w["kind"] != "bf16":
+    if w["kind"] not in ("bf16",):
         return None
     if w["fmt"] == "mxfp4":
         qa, sa = oracle.mx_quantize(host["a"])
@@ -456,6 +487,11 @@ def cpu_baseline(name, host, target_s):
     pilot, f0 = oracle_step_sample(name, host, 1.0 / 64, prepared)
     frac = min(1.0, f0 * target_s / max(pilot, 1e-6))
     t, f = oracle_step_sample(name, host, frac, prepared)
+    if synth.WORKLOADS[name]["kind"] == "quant2d":
+        gbs = m * k * (2 + 2 * (0.5 + 1.0 / 32)) * f / t / 1e9
+        return {"value": gbs, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+                "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} rows, both "
+                          f"directions), {t:.1f} s on the host CPU"}
     value = 2.0 * m * n * k * f / t / 1e12
     return {"value": value, "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
             "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} output rows with "
@@ -467,6 +503,7 @@ def cpu_baseline(name, host, target_s):
 # Source files that define the kernels of each call of the step.
 CALL_SOURCES = {
     "gemm": ["gemm.cu", "gemm_pair.cu", "mx_device.cuh", "mx_internal.h"],
+    "quantize_2d": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
 }
 
@@ -565,7 +602,11 @@ def main_ours(args):
     fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
     flops = 2.0 * m * n * k
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    quant2d = wl.kind == "quant2d"
+    # the quant2d step has no GEMM: its value is algorithmic GB/s
+    step_work = sum(b for b, _ in wl.algorithmic().values()) / 1e9 if quant2d else flops / 1e12
+    unit = "GB/s" if quant2d else "TFLOPS"
+    value = world * step_work / (ms_per_step * 1e-3)
     alg = wl.algorithmic()
     kpc = wl.kernels_per_call()
     kernels = {}
@@ -592,10 +633,11 @@ def main_ours(args):
                                                   "dense ratio)" if kd["bound"] == "tensor"
                                                   else "hbm_gbs"))}
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e2m1 (fp32 accumulate)", "data": "synthetic",
+        "dtype": "bf16 -> e2m1 (quantize only)" if quant2d else "e2m1 (fp32 accumulate)",
+        "data": "synthetic",
         "config": {"workload": name, "m": m, "n": n, "k": k, "format": w["fmt"],
                    "out": w["out"], "rotating_sets": nsets,
                    "l2": f"rotating input sets, {nsets} x {wl.set_bytes / 2**20:.0f} MiB "
@@ -605,7 +647,7 @@ def main_ours(args):
         "roofline": roofline,
         "kernels": kernels,
         "sum_of_calls_ms": sum(per_call.values()),
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+        "e2e": {"value": world * step_work / (e2e_ms * 1e-3), "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps * sum(kpc.values()),
         "clocks": clocks,
@@ -650,18 +692,21 @@ def main_reference(args):
         t, f = oracle_step_sample(name, host, frac, prepared)
         times.append(t)
     mean_t = statistics.fmean(times)
-    value = 2.0 * m * n * k * f / mean_t / 1e12
+    quant2d = synth.WORKLOADS[name]["kind"] == "quant2d"
+    unit = "GB/s" if quant2d else "TFLOPS"
+    value = (m * k * (2 + 2 * (0.5 + 1.0 / 32)) * f / mean_t / 1e9 if quant2d
+             else 2.0 * m * n * k * f / mean_t / 1e12)
     sample = (f"{f:.5f} of one step per step ({int(round(f * m))} of {m} output rows with the "
               f"matching share of the quantize work)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": mean_t * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
         "config": {"workload": name, "m": m, "n": n, "k": k},
-        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle_threads(),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle_threads(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -82,6 +82,10 @@ WORKLOADS = {
     # NVFP4 variant, FP32 out.
     "nvfp4_4096x4096x4096": dict(kind="bf16", fmt="nvfp4", m=4096, n=4096, k=4096,
                                  sigma_a=1.0, sigma_b=1.0, out="fp32", split_k=1),
+    # Bidimensional MXFP4 quantize (rowwise + columnwise) of the MLP weight
+    # 28672 x 8192: no GEMM (n = 0), HBM bound.
+    "quant2d_28672x8192": dict(kind="quant2d", fmt="mxfp4", m=28672, n=0, k=8192,
+                               sigma_a=0.015, out="codes", split_k=1),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -96,6 +100,7 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
 
     kind == "bf16": {"a": BF16 bits [m, k], "b": BF16 bits [n, k]}
     kind == "codes": {"a_codes", "a_scales", "b_codes", "b_scales"} (plain scales)
+    kind == "quant2d": {"a": BF16 bits [m, k]}
     """
     w = WORKLOADS[name]
     m = w["m"] if m is None else m
@@ -105,6 +110,8 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
     if w["kind"] == "bf16":
         return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1),
                 "b": bf16_normal(n, k, w["sigma_b"], seed + 2)}
+    if w["kind"] == "quant2d":
+        return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1)}
     kb = k // 32
     return {"a_codes": fp4_codes(m, k, seed + 1),
             "a_scales": scale_bytes(m, kb, w["scale_lo"], w["scale_hi"], seed + 2),
