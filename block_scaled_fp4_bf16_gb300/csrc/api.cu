@@ -402,7 +402,9 @@ MX_API int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, 
 MX_API int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
                                int format, int scale_layout, void *codes, void *scales,
                                void *codes_t, void *scales_t, void *stream) {
-  if (!x || !codes || !scales || !codes_t || !scales_t) return MX_ERR_INVALID_ARG;
+  // codes and scales may both be null (columnwise output only)
+  const bool rowwise = codes != nullptr || scales != nullptr;
+  if (!x || !codes_t || !scales_t || (rowwise && (!codes || !scales))) return MX_ERR_INVALID_ARG;
   if (!valid_format(format)) return MX_ERR_INVALID_ARG;
   if (scale_layout != MX_SCALE_PLAIN && scale_layout != MX_SCALE_TCGEN05) return MX_ERR_INVALID_ARG;
   if (rows <= 0 || cols <= 0 || ld_x < cols) return MX_ERR_INVALID_ARG;
@@ -414,7 +416,7 @@ MX_API int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_
     return MX_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || (ld_x % 8) != 0 || !aligned16(codes) || !aligned16(scales) ||
       !aligned16(codes_t) || !aligned16(scales_t))
-    return MX_ERR_ALIGNMENT;
+    return MX_ERR_ALIGNMENT;  // (a null pointer is aligned)
   // The two outputs are written concurrently from the same input: no output
   // may overlap the input or another output.
   const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
@@ -424,7 +426,7 @@ MX_API int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_
       {reinterpret_cast<uintptr_t>(scales), reinterpret_cast<uintptr_t>(scales) + mx_scale_bytes(rows, cols, format, scale_layout)},
       {reinterpret_cast<uintptr_t>(codes_t), reinterpret_cast<uintptr_t>(codes_t) + static_cast<uintptr_t>(rows * cols / 2)},
       {reinterpret_cast<uintptr_t>(scales_t), reinterpret_cast<uintptr_t>(scales_t) + mx_scale_bytes(cols, rows, format, scale_layout)}};
-  for (int o = 0; o < 4; ++o) {
+  for (int o = rowwise ? 0 : 2; o < 4; ++o) {
     if (overlap(out[o], in)) return MX_ERR_INVALID_ARG;
     for (int p = o + 1; p < 4; ++p)
       if (overlap(out[o], out[p])) return MX_ERR_INVALID_ARG;

@@ -433,7 +433,7 @@ struct Q2dArgs {
   const uint16_t *x;
   int64_t ld;
   uint32_t rows, cols;
-  uint8_t *codes, *scales;      // x: [rows, cols / 2], scales of x
+  uint8_t *codes, *scales;      // x: [rows, cols / 2], scales of x (null: columnwise only)
   uint8_t *codes_t, *scales_t;  // x^T: [cols, rows / 2], scales of x^T
   int tiled;
   uint32_t kb, kbt;             // scale columns of x and of x^T (cols / 32, rows / 32)
@@ -480,6 +480,7 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_2d_kernel(const __grid_c
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       dst[i ^ ((lb >> 1) & 3)] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    if (a.codes == nullptr) continue;  // columnwise only (uniform across the grid)
     uint32_t sbyte = 0;
     if (inside) {
       uint4 out;

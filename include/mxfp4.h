@@ -166,13 +166,24 @@ int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, int for
  * GEMM).
  *   x:        BF16 [rows, cols], row stride ld_x elements (ld_x >= cols,
  *             ld_x % 8 == 0); rows % 32 == 0 and cols % 32 == 0.
- *   codes, scales:     out, exactly what mx_quantize_bf16 writes for x.
+ *   codes, scales:     out, exactly what mx_quantize_bf16 writes for x; both
+ *             NULL for the columnwise output alone.
  *   codes_t, scales_t: out, exactly what mx_quantize_bf16 writes for x^T:
  *             codes_t [cols, rows / 2] bytes, scales_t
  *             mx_scale_bytes(cols, rows, format, scale_layout) bytes.
  * format: MX_FMT_MXFP4 only (MX_FMT_NVFP4 -> MX_ERR_UNSUPPORTED_FEATURE).
  * No output may overlap the input or another output (MX_ERR_INVALID_ARG).
- * Launches one kernel; each element of x is read from memory once. */
+ * Launches one kernel; each element of x is read from memory once.
+ *
+ * Operand layouts.  The GEMMs below take K-contiguous codes (TN) only; the
+ * other layouts of the pages' GEMMs are formed when the operands are
+ * quantized.  An operand stored with K as its row index (A as [K, M] or B
+ * as [K, N] in BF16) is quantized with this call's columnwise output, which
+ * is K-contiguous:
+ *   D = A . B^T  (TN):  A [M, K], B [N, K]  -> both rowwise (mx_quantize_bf16);
+ *   D = A . B    (NN):  B [K, N]            -> B's columnwise output;
+ *   D = A^T . B^T (TT): A [K, M]            -> A's columnwise output;
+ *   D = A^T . B  (NT):  A [K, M], B [K, N]  -> both columnwise outputs. */
 int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
                         int scale_layout, void *codes, void *scales, void *codes_t,
                         void *scales_t, void *stream);

@@ -79,9 +79,11 @@ def gpu_quantize_group(xs, fmt: int, layout: int, lds=None):
              None if ts is None else np.float32(ts.item())) for rows, cols, codes, scales, ts in outs]
 
 
-def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None):
+def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
+                    columnwise_only: bool = False):
     """Bidimensional MXFP4 quantize on the GPU; returns host (codes, scales,
-    codes_t, scales_t), outputs pre-filled with 0xAB."""
+    codes_t, scales_t), outputs pre-filled with 0xAB (codes and scales None
+    when only the columnwise output is asked for)."""
     rows, cols = x_bits.shape
     ld = cols if ld is None else ld
     padded = np.zeros((rows, ld), np.uint16)
@@ -92,9 +94,12 @@ def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None):
     codes, codes_t = fill(rows * cols // 2), fill(rows * cols // 2)
     scales = fill(mx.mx_scale_bytes(rows, cols, fmt, layout))
     scales_t = fill(mx.mx_scale_bytes(cols, rows, fmt, layout))
+    if columnwise_only:
+        codes = scales = None
     mx.mx_quantize_bf16_2d(x, rows, cols, ld, fmt, layout, codes, scales, codes_t, scales_t)
     torch.cuda.synchronize()
-    return (codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(),
+    return (None if codes is None else codes.cpu().numpy().reshape(rows, cols // 2),
+            None if scales is None else scales.cpu().numpy(),
             codes_t.cpu().numpy().reshape(cols, rows // 2), scales_t.cpu().numpy())
 
 

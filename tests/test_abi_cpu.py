@@ -177,6 +177,8 @@ def test_quantize_2d_argument_validation(lib):
     assert call(ld=100) == mx.MX_ERR_ALIGNMENT                    # ld % 8
     assert call(ct=FAKE + MB + 64) == mx.MX_ERR_INVALID_ARG       # codes_t overlaps codes
     assert call(c=FAKE + 1024) == mx.MX_ERR_INVALID_ARG           # codes overlap the input
+    assert call(c=None) == mx.MX_ERR_INVALID_ARG                  # rowwise codes without scales
+    assert call(s=None) == mx.MX_ERR_INVALID_ARG
 
 
 def test_relayout_and_selftest_validation(lib):

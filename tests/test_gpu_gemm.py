@@ -160,6 +160,39 @@ def test_backward_gemm_with_columnwise_codes():
     check_bf16(d, ref, s_abs, "dgrad with columnwise codes")
 
 
+@pytest.mark.parametrize("layout", ["TN", "NN", "TT", "NT"])
+def test_four_operand_layouts_through_the_quantizer(layout):
+    """D = op(A) . op(B)^T for the four layouts of BF16 inputs: an operand stored
+    K-major is quantized rowwise, one stored with K as its row index
+    columnwise (the bidimensional quantize, columnwise output only); the
+    GEMM is the TN kernel.  Its output must equal, bit for bit, the TN GEMM
+    of the explicitly transposed inputs, and match the oracle."""
+    m, n, k = 160, 288, 512
+    a_km = synth.bf16_normal(m, k, 1.0, seed=61)          # A as [M, K]
+    b_kn = synth.bf16_normal(n, k, 0.05, seed=62)         # B as [N, K]
+    # A is stored [M, K] for TN and NN, [K, M] for TT and NT; B [N, K] for TN and TT, [K, N] otherwise
+    a_stored = a_km if layout in ("TN", "NN") else np.ascontiguousarray(a_km.T)
+    b_stored = b_kn if layout in ("TN", "TT") else np.ascontiguousarray(b_kn.T)
+
+    def k_major(x_stored, is_k_major):
+        if is_k_major:
+            c, s_t, _ = gpu_quantize(x_stored, MX, TILED)
+            return c, s_t
+        _, _, ct, st = gpu_quantize_2d(x_stored, TILED, columnwise_only=True)
+        return ct, st
+    ca, sa = k_major(a_stored, layout in ("TN", "NN"))
+    cb, sb = k_major(b_stored, layout in ("TN", "TT"))
+    d = gpu_gemm(MX, ca, sa, cb, sb, m, n, k, out_fp32=False)
+    ra, rsa = oracle.mx_quantize(a_km)
+    rb, rsb = oracle.mx_quantize(b_kn)
+    assert np.array_equal(ca, ra) and np.array_equal(cb, rb)
+    d_tn = gpu_gemm(MX, ra, oracle.scale_tile(rsa), rb, oracle.scale_tile(rsb), m, n, k,
+                    out_fp32=False)
+    assert np.array_equal(d, d_tn)
+    ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k)
+    check_bf16(d, ref, s_abs, f"layout {layout}")
+
+
 def _quant_gemm_check(name, n_rows, n_cols):
     wl = synth.WORKLOADS[name]
     m, n, k = wl["m"], wl["n"], wl["k"]

@@ -280,3 +280,14 @@ def test_mx_quantize_2d_full_size_weight():
     """The 4096 x 4096 weight of the quantize+GEMM workload."""
     w = synth.workload_inputs("quant_gemm_2048x4096x4096")
     _check_2d(w["b"], TILED)
+
+
+def test_mx_quantize_2d_columnwise_only():
+    """Rowwise outputs omitted (null): the columnwise output is unchanged."""
+    x = synth.bf16_normal(192, 320, 1.0, seed=43)
+    _, _, rct, rst = oracle.mx_quantize_2d(x)
+    for layout in (PLAIN, TILED):
+        codes, scales, codes_t, scales_t = gpu_quantize_2d(x, layout, columnwise_only=True)
+        assert codes is None and scales is None
+        assert np.array_equal(codes_t, rct)
+        assert np.array_equal(scales_t, rst.ravel() if layout == PLAIN else oracle.scale_tile(rst))
