@@ -14,7 +14,9 @@ file's header comment and at each function.
 Pinned by the ``-m "not gpu"`` tests (``tests/test_oracle_*.py``): exhaustive
 E2M1/E4M3/BF16 codec checks against brute-force nearest-value searches and
 library routines, the exhaustive BF16 quantize sweep, GEMM brute force against
-a dequantize-then-fp64 matmul, and the closed-form invariants.
+a dequantize-then-fp64 matmul, the closed-form invariants, and for the
+stochastic-rounding path the published Philox4x32 known answers, exact
+rational rounding and the half-way inputs that expose the draw layout.
 """
 from __future__ import annotations
 
@@ -59,6 +61,7 @@ def _load():
         lib = ctypes.CDLL(build())
         c_u8p = ctypes.POINTER(ctypes.c_uint8)
         c_u16p = ctypes.POINTER(ctypes.c_uint16)
+        c_u32p = ctypes.POINTER(ctypes.c_uint32)
         c_i64 = ctypes.c_int64
         c_i64p = ctypes.POINTER(ctypes.c_int64)
         c_f64p = ctypes.POINTER(ctypes.c_double)
@@ -88,6 +91,14 @@ def _load():
         lib.oracle_nvfp4_quantize.argtypes = [c_u16p, c_i64, c_i64, c_i64, c_u8p, c_u8p,
                                               ctypes.POINTER(ctypes.c_float)]
         lib.oracle_block_gemm.restype = None
+        lib.oracle_philox4x32.argtypes = [c_u32p, c_u32p, ctypes.c_int, c_u32p]
+        lib.oracle_philox4x32.restype = None
+        lib.oracle_e2m1_encode_sr.argtypes = [ctypes.c_double, ctypes.c_uint32]
+        lib.oracle_e2m1_encode_sr.restype = ctypes.c_uint32
+        lib.oracle_nvfp4_quantize_sr.argtypes = [c_u16p, c_i64, c_i64, c_i64, ctypes.c_uint64,
+                                                 ctypes.c_int, ctypes.c_uint32, c_u8p, c_u8p,
+                                                 ctypes.POINTER(ctypes.c_float)]
+        lib.oracle_nvfp4_quantize_sr.restype = None
         lib.oracle_block_gemm.argtypes = [ctypes.c_int, c_u8p, c_u8p, c_u8p, c_u8p,
                                           c_i64, c_i64, c_i64, ctypes.c_float, ctypes.c_float,
                                           c_i64p, c_i64, c_i64p, c_i64, c_f64p, c_f64p]
@@ -189,6 +200,42 @@ def nvfp4_quantize(x_bits: np.ndarray):
     _load().oracle_nvfp4_quantize(_ptr(x, ctypes.c_uint16), rows, cols, cols,
                                   _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
                                   ctypes.byref(s_t))
+    return codes, scales, np.float32(s_t.value)
+
+
+def philox4x32(ctr, key, rounds: int = 10) -> np.ndarray:
+    """Philox4x32-``rounds`` of one 128-bit counter (4 x u32) under a 64-bit key (2 x u32)."""
+    c = np.ascontiguousarray(ctr, dtype=np.uint32).reshape(4)
+    k = np.ascontiguousarray(key, dtype=np.uint32).reshape(2)
+    out = np.zeros(4, dtype=np.uint32)
+    _load().oracle_philox4x32(_ptr(c, ctypes.c_uint32), _ptr(k, ctypes.c_uint32), int(rounds),
+                              _ptr(out, ctypes.c_uint32))
+    return out
+
+
+def e2m1_encode_sr(y: float, u: int) -> int:
+    """Stochastic rounding of y to an E2M1 code with the uniform byte u."""
+    return int(_load().oracle_e2m1_encode_sr(float(y), int(u)))
+
+
+def nvfp4_quantize_sr(x_bits: np.ndarray, seed: int, rounds: int = 10, direction: int = 0):
+    """NVFP4 quantize of BF16 bits [rows, cols] with stochastically rounded codes.
+
+    Same s_t and scales as :func:`nvfp4_quantize`; block (r, j) draws
+    Philox4x32-``rounds`` of counter (j, r, direction, 0) under the key
+    (seed low, seed high) and element i of the block uses byte i of the draw.
+    Returns (codes, scales, s_t).
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    assert cols % 16 == 0
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 16), dtype=np.uint8)
+    s_t = ctypes.c_float(0.0)
+    _load().oracle_nvfp4_quantize_sr(_ptr(x, ctypes.c_uint16), rows, cols, cols,
+                                     int(seed) & 0xFFFFFFFFFFFFFFFF, int(rounds), int(direction),
+                                     _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                                     ctypes.byref(s_t))
     return codes, scales, np.float32(s_t.value)
 
 

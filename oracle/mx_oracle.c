@@ -33,7 +33,13 @@
  *      * NVFP4: s_t = amax_t / 2688 (2688 = 6 * 448), block scale
  *        sb = E4M3_RNE_satfinite(amax_b / (6 * s_t)), code =
  *        E2M1_RNE(x / (E4M3(sb) * s_t)), every step one binary32 RN op;
- *        when s_t == 0 or sb == 0 the codes of the block are 0x0.
+ *        when s_t == 0 or sb == 0 the codes of the block are 0x0;
+ *      * NVFP4 stochastic rounding (the pages: one Philox4x32 draw per
+ *        output block, keyed by block coordinates and direction, with a
+ *        configurable round count): counter (block column j, row r,
+ *        direction, 0), key (seed low, seed high), byte i of the draw for
+ *        element i, round up iff u / 256 < p (oracle_e2m1_encode_sr); the
+ *        scales stay round-to-nearest.
  */
 #include <math.h>
 #include <stdint.h>
@@ -281,6 +287,125 @@ void oracle_nvfp4_quantize(const uint16_t *x, int64_t rows, int64_t cols, int64_
             for (int i = 0; i < 16; ++i) {
                 volatile float y = oracle_bf16_to_float(blk[i]) / den;
                 put_nibble(row_codes, j * 16 + i, oracle_e2m1_encode((double)y));
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Stochastic rounding (NVFP4)                                         */
+/* ------------------------------------------------------------------ */
+
+/* Philox4x32-R, the counter-based generator of Salmon, Moraes, Dror and
+ * Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3" (SC 2011), Philox
+ * section: a 128-bit counter c0..c3 and a 64-bit key k0, k1.  One round
+ * multiplies c0 and c2 by the constants 0xD2511F53 and 0xCD9E8D57 (full
+ * 64-bit products), then forms
+ *   (hi(c2 * M1) ^ c1 ^ k0,  lo(c2 * M1),  hi(c0 * M0) ^ c3 ^ k1,  lo(c0 * M0));
+ * between rounds the key is bumped by the Weyl constants 0x9E3779B9 and
+ * 0xBB67AE85 (the first round uses the key as given).  The output is the
+ * counter after `rounds` rounds (10 is the published default).
+ * NVIDIA/TransformerEngine #3809 (CuTeDSL NVFP4 kernels): each stochastic
+ * rounding draw is plain Philox4x32 of a known counter, with a configurable
+ * round count. */
+void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds, uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int i = 0; i < rounds; ++i) {
+        if (i > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* Stochastic rounding of y to E2M1 with the uniform byte u (0..255): with
+ * lo <= |y| < hi the two neighbouring E2M1 magnitudes and
+ * p = (|y| - lo) / (hi - lo), the magnitude becomes hi when u / 256 < p, else
+ * lo (so it is hi with probability ceil(256 p) / 256, and a value on the grid
+ * never moves).  |y| >= 6 saturates to 6 and the sign of y is kept, as in
+ * oracle_e2m1_encode.  Reading: the pages name stochastic rounding but not
+ * its arithmetic; this is the textbook rule with 8 random bits per element,
+ * the 128 bits of one Philox draw spread over a 16-element block. */
+uint32_t oracle_e2m1_encode_sr(double y, uint32_t u)
+{
+    const uint32_t sign = signbit(y) ? 8u : 0u;
+    const double a = fabs(y);
+    if (a >= 6.0)
+        return 7u | sign;
+    uint32_t c = 0;
+    while (c < 6 && k_e2m1_mag[c + 1] <= a)
+        ++c;
+    const double p = (a - k_e2m1_mag[c]) / (k_e2m1_mag[c + 1] - k_e2m1_mag[c]);
+    return ((double)(u & 0xFFu) / 256.0 < p ? c + 1 : c) | sign;
+}
+
+/* As oracle_nvfp4_quantize (same s_t, same block scales, same quotient
+ * x / den), with the quotient rounded stochastically instead of to nearest.
+ * NVIDIA/TransformerEngine #3809 (CuTeDSL NVFP4 kernels): one Philox draw
+ * per output block, keyed by the block's coordinates and direction.
+ * Reading: block (r, j) (row r of the output, j-th 16-element block along
+ * it) draws Philox4x32-`rounds` of counter (j, r, direction, 0) under the key
+ * (low, high 32 bits of seed); element i of the block (0..15) takes byte
+ * i % 4 (least significant first) of word i / 4 of the draw.  direction is
+ * 0 for the rowwise output and 1 for the columnwise one (the quantize of
+ * x^T, whose rows are the columns of x). */
+void oracle_nvfp4_quantize_sr(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
+                              uint64_t seed, int rounds, uint32_t direction,
+                              uint8_t *codes, uint8_t *scales, float *tensor_scale)
+{
+    const int64_t nb = cols / 16;
+    volatile float amax_t = oracle_bf16_amax(x, rows, cols, ld);
+    volatile float s_t = amax_t / 2688.0f;
+    *tensor_scale = s_t;
+    const float s_t_v = s_t;
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        uint8_t *row_codes = codes + r * (cols / 2);
+        for (int64_t j = 0; j < nb; ++j) {
+            const uint16_t *blk = x + r * ld + j * 16;
+            float amax_b = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                float v = fabsf(oracle_bf16_to_float(blk[i]));
+                if (v > amax_b)
+                    amax_b = v;
+            }
+            uint32_t sb = 0;
+            if (s_t_v > 0.0f) {
+                volatile float t = 6.0f * s_t_v;
+                volatile float ratio = amax_b / t;
+                sb = oracle_e4m3_encode((double)ratio);
+            }
+            scales[r * nb + j] = (uint8_t)sb;
+            if (sb == 0) {
+                for (int i = 0; i < 16; ++i)
+                    put_nibble(row_codes, j * 16 + i, 0u);
+                continue;
+            }
+            const uint32_t ctr[4] = {(uint32_t)j, (uint32_t)r, direction, 0u};
+            uint32_t draw[4];
+            oracle_philox4x32(ctr, key, rounds, draw);
+            volatile float den = (float)oracle_e4m3_decode(sb) * s_t_v;
+            for (int i = 0; i < 16; ++i) {
+                volatile float y = oracle_bf16_to_float(blk[i]) / den;
+                const uint32_t u = (draw[i / 4] >> (8 * (i % 4))) & 0xFFu;
+                put_nibble(row_codes, j * 16 + i, oracle_e2m1_encode_sr((double)y, u));
             }
         }
     }
