@@ -10,8 +10,9 @@ quantized to MXFP4 and multiplied, BF16 out) a step is: one grouped quantize
 of A and W (scales written straight into the tcgen05 tile order), then the
 GEMM.  `value` is 2*M*N*K per step over the device time of the step, in
 TFLOP/s; the GEMM kernel alone and the quantizer's GB/s are reported beside it
-with their roofline fractions.  The quant2d workload (a bidimensional quantize,
-no GEMM) reports GB/s of algorithmic bytes instead.
+with their roofline fractions.  The quantize-only workloads (quant2d_*: a
+bidimensional MXFP4 quantize; nvfp4_sr_*: an NVFP4 quantize with stochastic
+rounding) have no GEMM and report GB/s of algorithmic bytes instead.
 
 Timing: inputs are resident in HBM; the K steps are replayed from CUDA graphs
 (each holding one step per rotating input set) between two CUDA events on the
@@ -57,6 +58,18 @@ from block_scaled_fp4_bf16_gb300 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "quant_gemm_2048x4096x4096"
 METRIC = "MXFP4 GEMM TFLOPS and % of GB300 dense FP4 peak; quantize GB/s vs HBM"
+
+# Steps that are a quantize alone (no GEMM): their metric is algorithmic GB/s.
+QUANT_KINDS = ("quant2d", "quant_sr")
+# Philox seed of the stochastic-rounding quantize step
+SR_SEED = 0x5EED5EED
+
+
+def quant_step_bytes(kind, m, k):
+    """Algorithmic bytes of a quantize-only step over a BF16 [m, k] tensor."""
+    if kind == "quant2d":   # read once; codes + UE8M0 scales of x and of x^T
+        return m * k * (2 + 2 * (0.5 + 1.0 / 32))
+    return m * k * (2 + 2 + 0.5 + 1.0 / 16)  # NVFP4: amax read + quantize read; codes + E4M3 scales
 L2_BYTES = 129 * 1024 * 1024
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 : BF16 tensor ratio on GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -189,7 +202,7 @@ class DeviceWorkload:
         if self.kind == "bf16":
             ha = torch.from_numpy(host_inputs["a"].view(np.int16)).view(torch.bfloat16)
             hb = torch.from_numpy(host_inputs["b"].view(np.int16)).view(torch.bfloat16)
-        elif self.kind == "quant2d":
+        elif self.kind in QUANT_KINDS:
             ha = torch.from_numpy(host_inputs["a"].view(np.int16)).view(torch.bfloat16)
         else:
             tiled = {}
@@ -208,6 +221,15 @@ class DeviceWorkload:
                 s["codes_t"] = torch.empty(m * k // 2, dtype=u8, device=dev)
                 s["sf_t"] = torch.empty(mx.mx_scale_bytes(k, m, self.fmt, mx.MX_SCALE_TCGEN05),
                                         dtype=u8, device=dev)
+                self.sets.append(s)
+                continue
+            if self.kind == "quant_sr":
+                s["x_a"] = ha.to(dev)
+                s["codes_a"] = torch.empty(m * k // 2, dtype=u8, device=dev)
+                s["sf_a"] = torch.empty(sa_bytes, dtype=u8, device=dev)
+                s["ts_a"] = torch.zeros(1, dtype=torch.float32, device=dev)
+                s["qws"] = torch.empty(mx.mx_quantize_workspace_bytes(m, k, self.fmt), dtype=u8,
+                                       device=dev)
                 self.sets.append(s)
                 continue
             if self.kind == "bf16":
@@ -244,6 +266,11 @@ class DeviceWorkload:
                 mx.mx_quantize_bf16_2d(s["x_a"], m, k, k, fmt, mx.MX_SCALE_TCGEN05, s["codes_a"],
                                        s["sf_a"], s["codes_t"], s["sf_t"], stream=st)
             return [("quantize_2d", q2d)]
+        if self.kind == "quant_sr":
+            def qsr(s, st):
+                mx.nvfp4_quantize_bf16_sr(s["x_a"], m, k, k, mx.MX_SCALE_TCGEN05, s["codes_a"],
+                                          s["sf_a"], s["ts_a"], SR_SEED, 10, s["qws"], stream=st)
+            return [("quantize_sr", qsr)]
         if self.kind == "bf16":
             # the activation and the weight in one grouped quantize call
             def q(s, st):
@@ -269,6 +296,8 @@ class DeviceWorkload:
         mx = self.mx
         if self.kind == "quant2d":
             return {"quantize_2d": 1}
+        if self.kind == "quant_sr":
+            return {"quantize_sr": 2}
         q = 1 if self.fmt == mx.MX_FMT_MXFP4 else 2
         g = 1 + (1 if mx.mx_gemm_workspace_bytes(self.m, self.n, self.k, self.split_k) else 0)
         res = {"gemm": g}
@@ -282,7 +311,9 @@ class DeviceWorkload:
         blk = 32 if self.fmt == self.mx.MX_FMT_MXFP4 else 16
         if self.kind == "quant2d":
             # BF16 read once, codes and scales written for x and for x^T
-            return {"quantize_2d": (m * k * (2 + 2 * (0.5 + 1.0 / blk)), 0.0)}
+            return {"quantize_2d": (quant_step_bytes(self.kind, m, k), 0.0)}
+        if self.kind == "quant_sr":
+            return {"quantize_sr": (quant_step_bytes(self.kind, m, k), 0.0)}
         amax_pass = 0 if self.fmt == self.mx.MX_FMT_MXFP4 else 2
         qbytes = lambda r: r * k * (2 + amax_pass + 0.5 + 1.0 / blk)
         out_b = 2 if self.out == self.mx.MX_OUT_BF16 else 4
@@ -390,7 +421,7 @@ def time_e2e(wl, host_inputs, steps):
     torch = wl.torch
     s0 = wl.sets[0]
     pinned = {}
-    if wl.kind in ("bf16", "quant2d"):
+    if wl.kind in ("bf16",) + QUANT_KINDS:
         pinned["x_a"] = torch.from_numpy(host_inputs["a"].view(np.int16)).view(
             torch.bfloat16).pin_memory()
     if wl.kind == "bf16":
@@ -399,8 +430,8 @@ def time_e2e(wl, host_inputs, steps):
     elif wl.kind == "codes":
         pinned["codes_a"] = torch.from_numpy(host_inputs["a_codes"]).pin_memory()
         pinned["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).pin_memory()
-    # the step's result read back: D, or both code outputs of the quant2d step
-    result_keys = ["codes_a", "codes_t"] if wl.kind == "quant2d" else ["d"]
+    # the step's result read back: D, or the code outputs of a quantize step
+    result_keys = {"quant2d": ["codes_a", "codes_t"], "quant_sr": ["codes_a"]}.get(wl.kind, ["d"])
     results = {key: torch.empty(s0[key].shape, dtype=s0[key].dtype).pin_memory()
                for key in result_keys}
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
@@ -443,6 +474,9 @@ def oracle_step_sample(name, host, frac, prepared):
     if w["kind"] == "quant2d":
         mr = max(32, mr // 32 * 32)
         oracle.mx_quantize_2d(host["a"][:mr])
+        return time.perf_counter() - t0, mr / m
+    if w["kind"] == "quant_sr":
+        oracle.nvfp4_quantize_sr(host["a"][:mr], SR_SEED, 10)
         return time.perf_counter() - t0, mr / m
     if w["kind"] == "bf16":
         if w["fmt"] == "mxfp4":
@@ -487,11 +521,13 @@ def cpu_baseline(name, host, target_s):
     pilot, f0 = oracle_step_sample(name, host, 1.0 / 64, prepared)
     frac = min(1.0, f0 * target_s / max(pilot, 1e-6))
     t, f = oracle_step_sample(name, host, frac, prepared)
-    if synth.WORKLOADS[name]["kind"] == "quant2d":
-        gbs = m * k * (2 + 2 * (0.5 + 1.0 / 32)) * f / t / 1e9
+    kind = synth.WORKLOADS[name]["kind"]
+    if kind in QUANT_KINDS:
+        gbs = quant_step_bytes(kind, m, k) * f / t / 1e9
+        what = "both directions" if kind == "quant2d" else "stochastic rounding"
         return {"value": gbs, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
-                "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} rows, both "
-                          f"directions), {t:.1f} s on the host CPU"}
+                "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} rows, {what}), "
+                          f"{t:.1f} s on the host CPU"}
     value = 2.0 * m * n * k * f / t / 1e12
     return {"value": value, "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
             "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} output rows with "
@@ -505,6 +541,7 @@ CALL_SOURCES = {
     "gemm": ["gemm.cu", "gemm_pair.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize_2d": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
+    "quantize_sr": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
 }
 
 
@@ -602,10 +639,10 @@ def main_ours(args):
     fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
     flops = 2.0 * m * n * k
-    quant2d = wl.kind == "quant2d"
-    # the quant2d step has no GEMM: its value is algorithmic GB/s
-    step_work = sum(b for b, _ in wl.algorithmic().values()) / 1e9 if quant2d else flops / 1e12
-    unit = "GB/s" if quant2d else "TFLOPS"
+    quant_only = wl.kind in QUANT_KINDS
+    # a quantize-only step has no GEMM: its value is algorithmic GB/s
+    step_work = sum(b for b, _ in wl.algorithmic().values()) / 1e9 if quant_only else flops / 1e12
+    unit = "GB/s" if quant_only else "TFLOPS"
     value = world * step_work / (ms_per_step * 1e-3)
     alg = wl.algorithmic()
     kpc = wl.kernels_per_call()
@@ -636,7 +673,7 @@ def main_ours(args):
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 -> e2m1 (quantize only)" if quant2d else "e2m1 (fp32 accumulate)",
+        "dtype": "bf16 -> e2m1 (quantize only)" if quant_only else "e2m1 (fp32 accumulate)",
         "data": "synthetic",
         "config": {"workload": name, "m": m, "n": n, "k": k, "format": w["fmt"],
                    "out": w["out"], "rotating_sets": nsets,
@@ -692,9 +729,10 @@ def main_reference(args):
         t, f = oracle_step_sample(name, host, frac, prepared)
         times.append(t)
     mean_t = statistics.fmean(times)
-    quant2d = synth.WORKLOADS[name]["kind"] == "quant2d"
-    unit = "GB/s" if quant2d else "TFLOPS"
-    value = (m * k * (2 + 2 * (0.5 + 1.0 / 32)) * f / mean_t / 1e9 if quant2d
+    kind = synth.WORKLOADS[name]["kind"]
+    quant_only = kind in QUANT_KINDS
+    unit = "GB/s" if quant_only else "TFLOPS"
+    value = (quant_step_bytes(kind, m, k) * f / mean_t / 1e9 if quant_only
              else 2.0 * m * n * k * f / mean_t / 1e12)
     sample = (f"{f:.5f} of one step per step ({int(round(f * m))} of {m} output rows with the "
               f"matching share of the quantize work)")

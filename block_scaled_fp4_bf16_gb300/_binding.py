@@ -35,6 +35,7 @@ MX_OUT_BF16 = 0
 MX_OUT_FP32 = 1
 MX_STATIC_WORKSPACE_BYTES = 16 << 20
 MX_QUANTIZE_GROUP_MAX = 8
+MX_PHILOX_MAX_ROUNDS = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +81,9 @@ def lib() -> ctypes.CDLL:
         L.mx_quantize_bf16_group.restype = i32
         L.mx_quantize_bf16_group.argtypes = [ctypes.POINTER(mx_quantize_tensor), i32, i32, i32, vp,
                                              sz, vp]
+        L.nvfp4_quantize_bf16_sr.restype = i32
+        L.nvfp4_quantize_bf16_sr.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, ctypes.c_uint64,
+                                             i32, vp, sz, vp]
         L.mx_quantize_bf16_2d.restype = i32
         L.mx_quantize_bf16_2d.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
         L.mx_scale_relayout.restype = i32
@@ -159,6 +163,16 @@ def mx_quantize_bf16(x, rows, cols, ld_x, fmt, scale_layout, codes, scales, tens
     return _check("mx_quantize_bf16", lib().mx_quantize_bf16(
         _ptr(x), rows, cols, ld_x, fmt, scale_layout, _ptr(codes), _ptr(scales),
         _ptr(tensor_scale), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def nvfp4_quantize_bf16_sr(x, rows, cols, ld_x, scale_layout, codes, scales, tensor_scale, seed,
+                           philox_rounds=10, workspace=None, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("nvfp4_quantize_bf16_sr", lib().nvfp4_quantize_bf16_sr(
+        _ptr(x), rows, cols, ld_x, scale_layout, _ptr(codes), _ptr(scales), _ptr(tensor_scale),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, philox_rounds, _ptr(workspace), workspace_bytes,
+        _stream(stream)))
 
 
 def mx_quantize_group_workspace_bytes(count: int, fmt: int) -> int:

@@ -340,6 +340,29 @@ MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t l
                                              static_cast<cudaStream_t>(stream)));
 }
 
+static_assert(MX_PHILOX_MAX_ROUNDS == mx::kPhiloxMaxRounds, "Philox round limit");
+
+MX_API int nvfp4_quantize_bf16_sr(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  int scale_layout, void *codes, void *scales,
+                                  float *tensor_scale, uint64_t seed, int philox_rounds,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+  if (philox_rounds < 1 || philox_rounds > MX_PHILOX_MAX_ROUNDS) return MX_ERR_INVALID_ARG;
+  mx::QuantizeArgs a;
+  int rc = quantize_tensor_args(x, rows, cols, ld_x, MX_FMT_NVFP4, scale_layout, codes, scales,
+                                tensor_scale, &a);
+  if (rc != MX_OK) return rc;
+  if (!workspace || workspace_bytes < mx_quantize_workspace_bytes(rows, cols, MX_FMT_NVFP4))
+    return MX_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+  a.partials = static_cast<uint32_t *>(workspace);
+  DeviceInfo *dev = nullptr;
+  rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  a.num_sms = dev->num_sms;
+  const mx::SrArgs sr{seed, philox_rounds, 0u};
+  return launch_rc(mx::launch_quantize_group(1, &a, 1, static_cast<cudaStream_t>(stream), &sr));
+}
+
 MX_API size_t mx_quantize_group_workspace_bytes(int count, int format) {
   if (count < 1 || count > MX_QUANTIZE_GROUP_MAX || !valid_format(format)) return 0;
   return static_cast<size_t>(count) * mx_quantize_workspace_bytes(1, block_of(format), format);

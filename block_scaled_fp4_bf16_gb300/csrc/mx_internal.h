@@ -55,8 +55,19 @@ constexpr int kQuantizeGroupMax = 8;
 // Quantizes `count` independent tensors (1..kQuantizeGroupMax) of one format
 // in one launch (NVFP4: one amax launch, then one quantize launch).  fmt: 0
 // MXFP4, 1 NVFP4.  Each NVFP4 tensor has its own kAmaxPartials partials.
+// NVFP4 stochastic rounding of the codes: one Philox4x32-`rounds` draw per
+// 16-element block, counter (block column, row, direction, 0), key (seed low,
+// seed high).
+struct SrArgs {
+  uint64_t seed;
+  int rounds;          // 1..kPhiloxMaxRounds
+  uint32_t direction;  // 0 rowwise, 1 columnwise
+};
+constexpr int kPhiloxMaxRounds = 16;
+
+// sr: NVFP4 only; null rounds the codes to nearest.
 cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int count,
-                                  cudaStream_t s);
+                                  cudaStream_t s, const SrArgs *sr = nullptr);
 // Bidimensional MXFP4 quantize: rowwise codes/scales of x and of x^T (rows,
 // cols % 32 == 0).
 cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld, int tiled,

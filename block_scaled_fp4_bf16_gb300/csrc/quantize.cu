@@ -69,6 +69,9 @@ struct QTensor {
 
 struct QGroup {
   int count;
+  // NVFP4 stochastic rounding (the kernels instantiated for it read these)
+  uint32_t sr_key0, sr_key1, sr_direction;
+  int sr_rounds;
   QTensor t[kQuantizeGroupMax];
 };
 
@@ -303,13 +306,80 @@ __device__ __forceinline__ uint32_t div_to_e2m1x8_ieee(const uint32_t *w, float 
   return out;
 }
 
+// Philox4x32 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC 2011): per round the 64-bit products of c0 and c2 with
+// 0xD2511F53 and 0xCD9E8D57 give (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0);
+// the key is bumped by 0x9E3779B9, 0xBB67AE85 before every round but the
+// first.  ROUNDS > 0 fixes the count at compile time, else `rounds` (at most
+// kPhiloxMaxRounds) is used.
+template <int ROUNDS>
+__device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, int rounds) {
+#pragma unroll
+  for (int i = 0; i < (ROUNDS > 0 ? ROUNDS : kPhiloxMaxRounds); ++i) {
+    if (ROUNDS <= 0 && i >= rounds) break;
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// The E2M1 value that stochastic rounding of the binary32 quotient q gives
+// with the uniform byte u: with lo <= |q| < hi the neighbouring E2M1
+// magnitudes, hi when u / 256 < (|q| - lo) / (hi - lo), else lo; the sign of
+// q is kept and |q| >= 6 is left >= 6 for the saturating conversion.  Every
+// step is exact: the spacing s = hi - lo is a power of two (1/2 below 2, 1
+// below 4, 2 above), y = |q| / s, lo / s = floor(y), and 256 (y - floor(y))
+// is compared with u.
+__device__ __forceinline__ float sr_e2m1_value(float q, uint32_t u) {
+  const float a = fabsf(q);
+  const uint32_t es = max(__float_as_uint(a) >> 23, 127u);  // biased exponent, at least 2^0
+  const float inv_s = __uint_as_float((255u - es) << 23);   // 2^(128 - es)
+  const float s = __uint_as_float((es - 1u) << 23);         // 2^(es - 128)
+  const float y = __fmul_rn(a, inv_s);
+  const float f = floorf(y);
+  const float frac256 = __fmul_rn(__fsub_rn(y, f), 256.0f);
+  const float v = __fmul_rn(static_cast<float>(u) < frac256 ? __fadd_rn(f, 1.0f) : f, s);
+  return __uint_as_float(__float_as_uint(v) | (__float_as_uint(q) & 0x80000000u));
+}
+
+// The correctly rounded quotient x / den (as in div_to_e2m1x8; r == 0 selects
+// the IEEE division), with the sign of x.
+__device__ __forceinline__ float quotient(float x, float den, float r) {
+  if (r == 0.0f) return __fdiv_rn(x, den);
+  const float q0 = __fmul_rn(x, r);
+  const float q = __fmaf_rn(__fmaf_rn(-q0, den, x), r, q0);
+  return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// As div_to_e2m1x8 with stochastic rounding: element e (0..7) of the eight
+// uses byte e of the 64 bits (u_lo, u_hi), least significant byte first.
+__device__ __forceinline__ uint32_t div_to_e2m1x8_sr(const uint32_t *w, float den, float r,
+                                                     uint32_t u_lo, uint32_t u_hi) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = (i < 2 ? u_lo : u_hi) >> (16 * (i & 1));
+    const float q0 = quotient(__uint_as_float(w[i] << 16), den, r);
+    const float q1 = quotient(__uint_as_float(w[i] & 0xFFFF0000u), den, r);
+    out |= cvt_e2m1x2(sr_e2m1_value(q0, u & 0xFFu), sr_e2m1_value(q1, (u >> 8) & 0xFFu))
+           << (8 * i);
+  }
+  return out;
+}
+
 // NVFP4 pass 2: every CTA reduces its tensor's partial maxima to s_t, then
 // thread b quantizes 16-element block b.  Each binary32 step of the
 // definition is one round-to-nearest operation (correctly rounded divisions
 // where it divides).  The CTAs take the blocks in the reverse of the order in
 // which pass 1 swept them, so the first blocks quantized are the ones pass 1
-// read last, which are still in L2.
-template <bool WIDE>
+// read last, which are still in L2.  SR != 0 rounds the codes stochastically
+// (SR = 10: Philox4x32-10 unrolled; SR < 0: g.sr_rounds rounds).
+template <bool WIDE, int SR>
 __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
@@ -386,7 +456,14 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_kernel(const __gri
         sb = cvt_e4m3(q6);
       }
       uint2 out = make_uint2(0u, 0u);
-      if (sb != 0) {
+      if (sb != 0 && SR != 0) {
+        const float den = den_tab[sb];
+        const float rc = rcp_tab[sb];
+        const uint4 d = philox4x32<SR>(make_uint4(j, r, g.sr_direction, 0u), g.sr_key0, g.sr_key1,
+                                       g.sr_rounds);
+        out.x = div_to_e2m1x8_sr(&w[q][0], den, rc, d.x, d.y);
+        out.y = div_to_e2m1x8_sr(&w[q][4], den, rc, d.z, d.w);
+      } else if (sb != 0) {
         const float den = den_tab[sb];
         const float rc = rcp_tab[sb];
         if (rc != 0.0f) {
@@ -552,11 +629,19 @@ bool wide_ok(const void *x, int64_t ld) {
 }  // namespace
 
 cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int count,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, const SrArgs *sr) {
   if (count < 1 || count > kQuantizeGroupMax) return cudaErrorInvalidValue;
+  if (sr && (fmt != 1 || sr->rounds < 1 || sr->rounds > kPhiloxMaxRounds))
+    return cudaErrorInvalidValue;
   const uint32_t block = fmt == 0 ? 32u : 16u;
   QGroup g{};
   g.count = count;
+  if (sr) {
+    g.sr_key0 = static_cast<uint32_t>(sr->seed);
+    g.sr_key1 = static_cast<uint32_t>(sr->seed >> 32);
+    g.sr_direction = sr->direction;
+    g.sr_rounds = sr->rounds;
+  }
   bool wide = true;
   uint32_t ctas = 0;
   for (int i = 0; i < count; ++i) {
@@ -592,8 +677,12 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
                    dim3(kAmaxPartials, count), dim3(kThreads), 0, s, g);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_pdl(wide ? nvfp4_quantize_kernel<true> : nvfp4_quantize_kernel<false>, dim3(ctas),
-                   dim3(kThreads), 0, s, g);
+    auto kern = wide ? nvfp4_quantize_kernel<true, 0> : nvfp4_quantize_kernel<false, 0>;
+    if (sr && sr->rounds == 10)
+      kern = wide ? nvfp4_quantize_kernel<true, 10> : nvfp4_quantize_kernel<false, 10>;
+    else if (sr)
+      kern = wide ? nvfp4_quantize_kernel<true, -1> : nvfp4_quantize_kernel<false, -1>;
+    e = launch_pdl(kern, dim3(ctas), dim3(kThreads), 0, s, g);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -86,6 +86,10 @@ WORKLOADS = {
     # 28672 x 8192: no GEMM (n = 0), HBM bound.
     "quant2d_28672x8192": dict(kind="quant2d", fmt="mxfp4", m=28672, n=0, k=8192,
                                sigma_a=0.015, out="codes", split_k=1),
+    # NVFP4 quantize with stochastic rounding (Philox4x32-10 per block) of a
+    # 16384 x 8192 gradient-like tensor: no GEMM (n = 0), HBM bound.
+    "nvfp4_sr_16384x8192": dict(kind="quant_sr", fmt="nvfp4", m=16384, n=0, k=8192,
+                                sigma_a=1e-3, out="codes", split_k=1),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -100,7 +104,7 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
 
     kind == "bf16": {"a": BF16 bits [m, k], "b": BF16 bits [n, k]}
     kind == "codes": {"a_codes", "a_scales", "b_codes", "b_scales"} (plain scales)
-    kind == "quant2d": {"a": BF16 bits [m, k]}
+    kind == "quant2d" or "quant_sr": {"a": BF16 bits [m, k]}
     """
     w = WORKLOADS[name]
     m = w["m"] if m is None else m
@@ -110,7 +114,7 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
     if w["kind"] == "bf16":
         return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1),
                 "b": bf16_normal(n, k, w["sigma_b"], seed + 2)}
-    if w["kind"] == "quant2d":
+    if w["kind"] in ("quant2d", "quant_sr"):
         return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1)}
     kb = k // 32
     return {"a_codes": fp4_codes(m, k, seed + 1),

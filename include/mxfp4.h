@@ -118,6 +118,42 @@ int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t ld_x, in
                      int scale_layout, void *codes, void *scales, float *tensor_scale,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- stochastic rounding (NVFP4) ------------------------------------------
+ * NVIDIA/TransformerEngine #3809 (CuTeDSL NVFP4 kernels, commit messages):
+ * stochastic rounding draws Philox once per output block, keyed by the
+ * block's coordinates and direction; each draw is plain Philox4x32 of a known
+ * counter with a configurable round count.  This library's reading:
+ *   - block (r, j) (row r, j-th 16-element block of the row) draws
+ *     Philox4x32-philox_rounds (Salmon et al., "Parallel Random Numbers: As
+ *     Easy as 1, 2, 3", SC 2011) of the counter (j, r, 0, 0) under the key
+ *     (seed & 0xFFFFFFFF, seed >> 32); the third counter word is the
+ *     direction, 0 for this rowwise output;
+ *   - element i (0..15) of the block takes byte i of the 128-bit draw (word
+ *     i / 4, least significant byte first) as a uniform u in 0..255;
+ *   - with q = x / (E4M3(sb) * s_t) the same correctly rounded quotient as
+ *     mx_quantize_bf16 and lo <= |q| < hi the two neighbouring E2M1
+ *     magnitudes, the code's magnitude is hi iff u / 256 < (|q| - lo) /
+ *     (hi - lo) (so hi with probability ceil(256 p) / 256); |q| >= 6 gives 6;
+ *     the sign of x is kept;
+ *   - s_t and the scale bytes are those of mx_quantize_bf16 (round to
+ *     nearest); codes 0 where sb == 0 or s_t == 0.
+ * The result depends only on x, seed and philox_rounds (not on the launch
+ * shape), so it is reproducible. */
+
+/* Largest philox_rounds accepted. */
+#define MX_PHILOX_MAX_ROUNDS 16
+
+/* NVFP4 quantize with stochastically rounded codes.  Arguments as
+ * mx_quantize_bf16 with format MX_FMT_NVFP4; seed: the 64-bit Philox key;
+ * philox_rounds: 1..MX_PHILOX_MAX_ROUNDS (10 is Philox4x32-10, the
+ * generator's published default; MX_ERR_INVALID_ARG otherwise).  workspace:
+ * mx_quantize_workspace_bytes(rows, cols, MX_FMT_NVFP4) bytes.  Launches two
+ * kernels (amax, then quantize). */
+int nvfp4_quantize_bf16_sr(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                           int scale_layout, void *codes, void *scales, float *tensor_scale,
+                           uint64_t seed, int philox_rounds, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
 /* ---- grouped quantize ---------------------------------------------------
  * The pages quantize one tensor per call and have no grouped form.  This
  * library adds one: several independent tensors of one format (typically

@@ -52,6 +52,28 @@ def gpu_quantize(x_bits: np.ndarray, fmt: int, layout: int, ld: int | None = Non
     return codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(), s_t
 
 
+def gpu_quantize_sr(x_bits: np.ndarray, seed: int, rounds: int = 10, layout: int = 0,
+                    ld: int | None = None):
+    """NVFP4 quantize with stochastic rounding on the GPU (nvfp4_quantize_bf16_sr);
+    returns host (codes, scales, s_t).  Outputs are pre-filled with 0xAB."""
+    rows, cols = x_bits.shape
+    ld = cols if ld is None else ld
+    padded = np.zeros((rows, ld), np.uint16)
+    padded[:, :cols] = x_bits
+    x = dev_bf16(padded)
+    fmt = mx.MX_FMT_NVFP4
+    codes = torch.full((rows * cols // 2,), 0xAB, dtype=torch.uint8, device="cuda")
+    scales = torch.full((mx.mx_scale_bytes(rows, cols, fmt, layout),), 0xAB, dtype=torch.uint8,
+                        device="cuda")
+    ts = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(mx.mx_quantize_workspace_bytes(rows, cols, fmt), dtype=torch.uint8,
+                     device="cuda")
+    mx.nvfp4_quantize_bf16_sr(x, rows, cols, ld, layout, codes, scales, ts, seed, rounds, ws)
+    torch.cuda.synchronize()
+    return (codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(),
+            np.float32(ts.item()))
+
+
 def gpu_quantize_group(xs, fmt: int, layout: int, lds=None):
     """Quantize several BF16-bit arrays in one mx_quantize_bf16_group call;
     returns a list of host (codes, scales, s_t).  Outputs are pre-filled with

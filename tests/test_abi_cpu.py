@@ -113,6 +113,26 @@ def test_quantize_argument_validation(lib):
     assert q(FAKE, 4, 32, 32, 1, 0, FAKE, FAKE, FAKE, None, 0, None) == mx.MX_ERR_WORKSPACE
 
 
+def test_quantize_sr_argument_validation(lib):
+    q = lib.nvfp4_quantize_bf16_sr
+    MB = 1 << 20
+
+    def call(x=FAKE, rows=4, cols=32, ld=32, lay=0, c=FAKE + MB, s=FAKE + 2 * MB, ts=FAKE + 3 * MB,
+             rounds=10, ws=FAKE + 4 * MB, wsb=1 << 16):
+        return q(x, rows, cols, ld, lay, c, s, ts, 0x0123456789ABCDEF, rounds, ws, wsb, None)
+    assert call(rounds=0) == mx.MX_ERR_INVALID_ARG
+    assert call(rounds=mx.MX_PHILOX_MAX_ROUNDS + 1) == mx.MX_ERR_INVALID_ARG
+    assert call(x=None) == mx.MX_ERR_INVALID_ARG
+    assert call(ts=None) == mx.MX_ERR_INVALID_ARG                # NVFP4 needs the tensor scale
+    assert call(lay=7) == mx.MX_ERR_INVALID_ARG
+    assert call(cols=40, ld=40) == mx.MX_ERR_UNSUPPORTED_SHAPE    # cols % 16
+    assert call(ld=36) == mx.MX_ERR_ALIGNMENT
+    assert call(ts=FAKE + 3 * MB + 2) == mx.MX_ERR_ALIGNMENT
+    assert call(ws=None) == mx.MX_ERR_WORKSPACE
+    assert call(wsb=4) == mx.MX_ERR_WORKSPACE
+    assert call(ws=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
+
+
 def _group(lib, tensors, fmt=0, layout=0, ws=None, wsb=0):
     arr = (mx.mx_quantize_tensor * max(1, len(tensors)))()
     for i, t in enumerate(tensors):

@@ -6,7 +6,8 @@ import pytest
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import gpu_quantize, gpu_quantize_2d, gpu_quantize_group, gpu_relayout
+from tests.gpu_helpers import (gpu_quantize, gpu_quantize_2d, gpu_quantize_group, gpu_quantize_sr,
+                               gpu_relayout)
 
 pytestmark = pytest.mark.gpu
 
@@ -291,3 +292,89 @@ def test_mx_quantize_2d_columnwise_only():
         assert codes is None and scales is None
         assert np.array_equal(codes_t, rct)
         assert np.array_equal(scales_t, rst.ravel() if layout == PLAIN else oracle.scale_tile(rst))
+
+
+# ---------------------------------------------------------------- stochastic rounding (NVFP4)
+
+def _check_nv_sr(x, seed, rounds=10, layout=PLAIN, ld=None):
+    codes, scales, s_t = gpu_quantize_sr(x, seed, rounds, layout, ld)
+    rc, rs, rt = oracle.nvfp4_quantize_sr(x, seed, rounds)
+    assert np.float32(s_t).view(np.uint32) == np.float32(rt).view(np.uint32)
+    if layout == PLAIN:
+        assert np.array_equal(scales.reshape(rs.shape), rs)
+    else:
+        assert np.array_equal(scales, oracle.scale_tile(rs))
+    assert np.array_equal(codes, rc), _explain(x, codes, rc, scales, rs, 16) + f"\n  seed={seed}"
+    return codes
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (5, 48), (128, 256), (300, 1024), (129, 4096)])
+@pytest.mark.parametrize("layout", [PLAIN, TILED])
+def test_nvfp4_sr_matches_oracle(rows, cols, layout):
+    x = synth.bf16_normal(rows, cols, 1.0, seed=rows * 31 + cols)
+    _check_nv_sr(x, 0x5EED0000 + rows, 10, layout)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 0xFFFFFFFF, 0x100000000, 0xFEDCBA9876543210])
+@pytest.mark.parametrize("rounds", [1, 2, 7, 10, 16])
+def test_nvfp4_sr_seeds_and_round_counts(seed, rounds):
+    x = synth.bf16_normal(64, 512, 0.02, seed=7)
+    _check_nv_sr(x, seed, rounds)
+
+
+def test_nvfp4_sr_full_size():
+    w = synth.workload_inputs("nvfp4_4096x4096x4096")
+    _check_nv_sr(w["a"], 42, 10, TILED)
+    _check_nv_sr(w["b"], 43, 10, TILED)
+
+
+def test_nvfp4_sr_special_cases_and_unaligned_rows():
+    x = synth.bf16_normal(40, 256, 2.0, seed=3)
+    x[0, :16] = 0
+    x[1, 16:32] = 0x8000
+    x[2, :] = synth.f32_to_bf16_bits(np.full(256, 1e-30, np.float32))
+    x[3, 0] = synth.f32_to_bf16_bits(np.array([1000.0], np.float32))[0]
+    _check_nv_sr(x, 11)
+    _check_nv_sr(x, 12, ld=264)          # rows only 16-byte aligned: the two-load path
+    _check_nv_sr(np.zeros((4, 64), np.uint16), 13)
+
+
+@pytest.mark.parametrize("tmax", [1.0, 448.0, 1.5e-3, 7.5e5, 3e30, 2e-30])
+def test_nvfp4_sr_every_bf16_under_many_divisors(tmax):
+    """Every finite BF16 value under many block divisors (including divisors
+    outside the reciprocal's safe range, which take the IEEE division)."""
+    rows = []
+    for k in (0, 1, 3, 6, 9, 13):
+        for mant in (1.0, 1.375, 1.875):
+            bmax = tmax * 2.0 ** -k * mant / 1.875
+            bb = synth.f32_to_bf16_bits(np.array([bmax], np.float32))[0]
+            bval = float(synth.bf16_bits_to_f32(np.array([bb], np.uint16))[0])
+            v = _finite_bf16_upto(bval)
+            y = np.zeros((v.size, 16), np.uint16)
+            y[:, 0] = bb
+            y[:, 7] = v
+            y[:, 12] = v[::-1]
+            rows.append(y)
+    x = np.concatenate(rows)
+    x[0, 15] = synth.f32_to_bf16_bits(np.array([tmax], np.float32))[0]
+    _check_nv_sr(x, int(tmax * 1000) & 0xFFFF)
+
+
+def test_nvfp4_sr_is_deterministic_and_unbiased_on_the_gpu():
+    """Same seed, same bytes; the mean over 128 seeds of the dequantized codes
+    is within 5 standard errors (plus the 1/256-step bias) of x / den."""
+    x = synth.bf16_normal(32, 256, 0.5, seed=21)
+    a = gpu_quantize_sr(x, 99)[0]
+    assert np.array_equal(a, gpu_quantize_sr(x, 99)[0])
+    assert not np.array_equal(a, gpu_quantize_sr(x, 100)[0])
+    _, rs, rt = oracle.nvfp4_quantize(x)
+    e4 = np.array([oracle.e4m3_decode(b) for b in range(256)])
+    den = np.repeat((e4[rs] * np.float64(rt)).astype(np.float32), 16, axis=1)
+    q = (synth.bf16_bits_to_f32(x) / den).astype(np.float64)
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])
+    n, acc = 128, np.zeros_like(q)
+    for seed in range(n):
+        c = _unpack(gpu_quantize_sr(x, 5000 + seed)[0])
+        acc += np.where(c & 8, -1.0, 1.0) * grid[c & 7]
+    step = np.where(np.abs(q) < 2, 0.5, np.where(np.abs(q) < 4, 1.0, 2.0))
+    assert np.all(np.abs(acc / n - q) <= step * (5 * 0.5 / np.sqrt(n) + 1 / 256))
