@@ -329,45 +329,73 @@ __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, i
 }
 
 // The E2M1 value that stochastic rounding of the binary32 quotient q gives
-// with the uniform byte u: with lo <= |q| < hi the neighbouring E2M1
-// magnitudes, hi when u / 256 < (|q| - lo) / (hi - lo), else lo; the sign of
-// q is kept and |q| >= 6 is left >= 6 for the saturating conversion.  Every
-// step is exact: the spacing s = hi - lo is a power of two (1/2 below 2, 1
-// below 4, 2 above), y = |q| / s, lo / s = floor(y), and 256 (y - floor(y))
-// is compared with u.
-__device__ __forceinline__ float sr_e2m1_value(float q, uint32_t u) {
+// with the byte u, passed as nu = ~u (any bits above the low byte ignored):
+// with lo <= |q| < hi the neighbouring E2M1 magnitudes and p = (|q| - lo) /
+// (hi - lo), hi when u / 256 < p, else lo; the sign of q is kept and |q| >= 6
+// is left >= 6 for the saturating conversion.
+// From 1 up, the E2M1 grid is binary32 cut to one mantissa bit, and p is the
+// cut-off 22 bits F / 2^22.  u / 256 < F / 2^22 holds iff F + (256 - u) 2^14
+// - 1 carries into the kept bit, so adding ((255 - u) << 14) | 0x3FFF to the
+// bits and clearing the low 22 gives the result (a carry out of the top
+// mantissa bit moves to the next binade, which is the next grid value).
+// Below 1 the grid (spacing 1/2) is that of [1, 2) shifted by 1: b = |q| + 1
+// rounded up keeps u / 256 < p exact, since u 2^14 is an integer and
+// F(b) = ceil(p 2^22); the 1 is taken off again at the end (exactly).
+__device__ __forceinline__ float sr_e2m1_value(float q, uint32_t nu) {
   const float a = fabsf(q);
-  const uint32_t es = max(__float_as_uint(a) >> 23, 127u);  // biased exponent, at least 2^0
-  const float inv_s = __uint_as_float((255u - es) << 23);   // 2^(128 - es)
-  const float s = __uint_as_float((es - 1u) << 23);         // 2^(es - 128)
-  const float y = __fmul_rn(a, inv_s);
-  const float f = floorf(y);
-  const float frac256 = __fmul_rn(__fsub_rn(y, f), 256.0f);
-  const float v = __fmul_rn(static_cast<float>(u) < frac256 ? __fadd_rn(f, 1.0f) : f, s);
+  const float off = a < 1.0f ? 1.0f : 0.0f;
+  const float b = __fadd_ru(a, off);
+  const uint32_t add = ((nu & 0xFFu) << 14) | 0x3FFFu;
+  const float t = __uint_as_float((__float_as_uint(b) + add) & 0xFFC00000u);
+  const float v = __fsub_rn(t, off);
   return __uint_as_float(__float_as_uint(v) | (__float_as_uint(q) & 0x80000000u));
 }
 
-// The correctly rounded quotient x / den (as in div_to_e2m1x8; r == 0 selects
-// the IEEE division), with the sign of x.
-__device__ __forceinline__ float quotient(float x, float den, float r) {
-  if (r == 0.0f) return __fdiv_rn(x, den);
-  const float q0 = __fmul_rn(x, r);
-  const float q = __fmaf_rn(__fmaf_rn(-q0, den, x), r, q0);
-  return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+// Eight BF16 (four words, element 2i in the low half of word i) divided by
+// den: the correctly rounded quotients with the sign of x (the sequence of
+// div_to_e2m1x8 in packed FP32x2 operations; r == 0 selects the IEEE
+// division).
+__device__ __forceinline__ void quotients8(const uint32_t *w, float den, float r, float *q) {
+  if (r == 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[2 * i] = __fdiv_rn(__uint_as_float(w[i] << 16), den);
+      q[2 * i + 1] = __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), den);
+    }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("{\n"
+        " .reg .b64 rr, nd, x, q0, t;\n"
+        " .reg .f32 nden;\n"
+        " neg.f32 nden, %2;\n"
+        " mov.b64 rr, {%3, %3};\n mov.b64 nd, {nden, nden};\n"
+        " mov.b64 x, {%4, %5};\n"
+        " mul.rn.f32x2 q0, x, rr;\n"
+        " fma.rn.f32x2 t, q0, nd, x;\n"
+        " fma.rn.f32x2 q0, t, rr, q0;\n"
+        " and.b64 t, x, 0x8000000080000000;\n or.b64 q0, q0, t;\n"
+        " mov.b64 {%0, %1}, q0;\n"
+        "}\n"
+        : "=f"(q[2 * i]), "=f"(q[2 * i + 1])
+        : "f"(den), "f"(r), "f"(__uint_as_float(w[i] << 16)),
+          "f"(__uint_as_float(w[i] & 0xFFFF0000u)));
+  }
 }
 
 // As div_to_e2m1x8 with stochastic rounding: element e (0..7) of the eight
 // uses byte e of the 64 bits (u_lo, u_hi), least significant byte first.
 __device__ __forceinline__ uint32_t div_to_e2m1x8_sr(const uint32_t *w, float den, float r,
                                                      uint32_t u_lo, uint32_t u_hi) {
+  float q[8];
+  quotients8(w, den, r, q);
+  const uint32_t n_lo = ~u_lo, n_hi = ~u_hi;
   uint32_t out = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t u = (i < 2 ? u_lo : u_hi) >> (16 * (i & 1));
-    const float q0 = quotient(__uint_as_float(w[i] << 16), den, r);
-    const float q1 = quotient(__uint_as_float(w[i] & 0xFFFF0000u), den, r);
-    out |= cvt_e2m1x2(sr_e2m1_value(q0, u & 0xFFu), sr_e2m1_value(q1, (u >> 8) & 0xFFu))
-           << (8 * i);
+    const uint32_t n = (i < 2 ? n_lo : n_hi) >> (16 * (i & 1));
+    out |= cvt_e2m1x2(sr_e2m1_value(q[2 * i], n), sr_e2m1_value(q[2 * i + 1], n >> 8)) << (8 * i);
   }
   return out;
 }
