@@ -239,6 +239,32 @@ def nvfp4_quantize_sr(x_bits: np.ndarray, seed: int, rounds: int = 10, direction
     return codes, scales, np.float32(s_t.value)
 
 
+def nvfp4_quantize_2d(x_bits: np.ndarray, seed=None, rounds: int = 10):
+    """Bidimensional NVFP4 quantize of BF16 bits [rows, cols] (rows, cols % 16 == 0).
+
+    Returns (codes, scales, codes_t, scales_t, s_t): the rowwise NVFP4
+    quantize of x and that of x transposed (blocks of 16 down a column of x,
+    stored as [cols, rows/2] codes and [cols, rows/16] scales), under the one
+    tensor scale s_t = amax(x) / 2688 (x and x^T have the same amax).  The
+    columnwise result is the transposed output of NVIDIA/TransformerEngine
+    #3809 (NVFP4QuantizeBidimensionalG2RKernel, passed as (cols, rows)).
+    With a seed the codes are rounded stochastically: the rowwise blocks draw
+    with direction 0 and the columnwise blocks with direction 1 (the pages:
+    one draw per output block, keyed by its coordinates and direction).
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    assert x.shape[0] % 16 == 0 and x.shape[1] % 16 == 0
+    xt = np.ascontiguousarray(x.T)
+    if seed is None:
+        codes, scales, s_t = nvfp4_quantize(x)
+        codes_t, scales_t, s_tt = nvfp4_quantize(xt)
+    else:
+        codes, scales, s_t = nvfp4_quantize_sr(x, seed, rounds, direction=0)
+        codes_t, scales_t, s_tt = nvfp4_quantize_sr(xt, seed, rounds, direction=1)
+    assert s_t == s_tt
+    return codes, scales, codes_t, scales_t, s_t
+
+
 # ----------------------------------------------------------------- GEMM
 
 def block_gemm(fmt: int, a_codes, a_scales, b_codes, b_scales, m: int, n: int, k: int,

@@ -232,3 +232,66 @@ def test_nvfp4_zero_cases(oracle):
     u = _unpack(codes, 64)
     assert scales[1, 1] == 0 and not u[1, 16:32].any()
     assert scales[2, 2] == 0 and not u[2, 32:48].any()
+
+
+# ----------------------------------------------------------------- bidimensional NVFP4
+
+def _exact_regime_nvfp4(rows, cols, seed):
+    """BF16 x whose rowwise NVFP4 quantize is exact (s_t = 2^-3, every block
+    scale a power of two) with the expected codes from the nearest-grid
+    search; see test_nvfp4_exact_regime_reduces_to_nearest_grid."""
+    rng = np.random.default_rng(seed)
+    p = -3
+    q = rng.integers(-6, 3, size=(rows, cols // 16))
+    blk_amax = 6.0 * 2.0 ** p * np.ldexp(1.0, q)
+    x = rng.uniform(-1, 1, size=(rows, cols // 16, 16)) * blk_amax[..., None]
+    x[..., 0] = blk_amax
+    x = x.reshape(rows, cols)
+    x[0, :16] = 0
+    x[0, 0] = 2688.0 * 2.0 ** p
+    xb = synth.f32_to_bf16_bits(x.astype(np.float32))
+    blocks = fpref.bf16_bits_to_f64(xb).reshape(rows, cols // 16, 16)
+    den = np.abs(blocks).max(axis=-1) / 6.0        # = E4M3(sb) * s_t, a power of two
+    den[0, 0] = 2688.0 * 2.0 ** p / 6.0
+    codes = fpref.nearest_e2m1_codes_vec(blocks / den[..., None]).reshape(rows, cols)
+    return xb, codes
+
+
+def test_nvfp4_quantize_2d_columnwise_exact_regime(oracle):
+    """x is the transpose of an exact-regime matrix, so the columnwise output
+    of x (the rowwise quantize of x^T) has codes fixed by the nearest-grid
+    search, laid out [cols, rows/2]."""
+    xt, expected = _exact_regime_nvfp4(96, 160, 31)
+    x = np.ascontiguousarray(xt.T)                 # [160, 96]
+    codes, scales, codes_t, scales_t, s_t = oracle.nvfp4_quantize_2d(x)
+    assert s_t == np.float32(2.0 ** -3)
+    assert codes.shape == (160, 48) and codes_t.shape == (96, 80)
+    assert scales.shape == (160, 6) and scales_t.shape == (96, 10)
+    assert np.array_equal(_unpack(codes_t, 160), expected)
+
+
+def test_nvfp4_quantize_2d_orientation(oracle):
+    """A large element at (0, 0) fixes s_t; one small element at (r, c) lands at
+    row r, column c rowwise and at row c, column r columnwise."""
+    r, c = 45, 70
+    x = np.zeros((64, 96), dtype=np.uint16)
+    x[0, 0] = synth.f32_to_bf16_bits(np.array([336.0], np.float32))[0]  # s_t = 336 / 2688 = 1/8
+    x[r, c] = synth.f32_to_bf16_bits(np.array([-0.75], np.float32))[0]
+    codes, scales, codes_t, scales_t, s_t = oracle.nvfp4_quantize_2d(x)
+    assert s_t == np.float32(0.125)
+    u, ut = _unpack(codes, 96), _unpack(codes_t, 64)
+    # block amax 0.75: sb = E4M3(0.75 / 0.75) = 1.0 (byte 0x38), den = 1/8, -0.75 * 8 = -6 -> 15
+    assert u[r, c] == 15 and ut[c, r] == 15
+    assert scales[r, c // 16] == 0x38 and scales_t[c, r // 16] == 0x38
+    assert np.count_nonzero(u) == 2 and np.count_nonzero(ut) == 2
+
+
+def test_nvfp4_quantize_2d_symmetric_input(oracle):
+    x = synth.bf16_normal(128, 128, 2.0, seed=32)
+    x = np.triu(x) + np.triu(x, 1).T
+    codes, scales, codes_t, scales_t, _ = oracle.nvfp4_quantize_2d(x)
+    assert np.array_equal(codes, codes_t) and np.array_equal(scales, scales_t)
+    # stochastic rounding: the same scales, but the two directions draw differently
+    c2, s2, ct2, st2, _ = oracle.nvfp4_quantize_2d(x, seed=5)
+    assert np.array_equal(s2, scales) and np.array_equal(st2, scales)
+    assert not np.array_equal(c2, ct2)

@@ -218,3 +218,26 @@ def test_sr_is_unbiased_over_seeds():
     # and the spread is that of two-point rounding, not of round-to-nearest
     rne = _decode(oracle.nvfp4_quantize(x)[0])[0]
     assert np.mean(np.abs(mean - q)) < 0.5 * np.mean(np.abs(rne - q))
+
+
+def test_sr_columnwise_draws_use_direction_one():
+    """The columnwise output of the bidimensional quantize draws with direction
+    1: with x the transpose of the half-way input, element i of columnwise block
+    (r, j) rounds up iff byte i of the draw of counter (j, r, 1, 0) is < 128."""
+    rows, nblocks, seed = 16, 3, 0xABCDEF0123
+    f, xr = _halfway_input(rows, nblocks)
+    x = np.ascontiguousarray(xr.T)                # [16 (nblocks + 1), 16]
+    _, _, codes_t, scales_t, st = oracle.nvfp4_quantize_2d(x, seed=seed)
+    assert st == np.float32(2.0 ** -8)
+    _, c = _decode(codes_t)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for r in range(rows):
+        for j in range(1, nblocks + 1):
+            draw = oracle.philox4x32([j, r, 1, 0], key)
+            for i in range(16):
+                v = abs(float(f[r, 16 * j + i]))
+                if v == 6.0:
+                    continue
+                u = (int(draw[i // 4]) >> (8 * (i % 4))) & 0xFF
+                lo = max(k for k, g in enumerate(GRID) if g <= v)
+                assert c[r, 16 * j + i] & 7 == (lo + 1 if u < 128 else lo)
