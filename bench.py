@@ -12,7 +12,7 @@ GEMM.  `value` is 2*M*N*K per step over the device time of the step, in
 TFLOP/s; the GEMM kernel alone and the quantizer's GB/s are reported beside it
 with their roofline fractions.  The quantize-only workloads (quant2d_*: a
 bidimensional MXFP4 quantize; nvfp4_sr_*: an NVFP4 quantize with stochastic
-rounding) have no GEMM and report GB/s of algorithmic bytes instead.
+rounding; nvfp4_quant2d_sr_*: both) have no GEMM and report GB/s of algorithmic bytes instead.
 
 Timing: inputs are resident in HBM; the K steps are replayed from CUDA graphs
 (each holding one step per rotating input set) between two CUDA events on the
@@ -65,11 +65,14 @@ QUANT_KINDS = ("quant2d", "quant_sr")
 SR_SEED = 0x5EED5EED
 
 
-def quant_step_bytes(kind, m, k):
-    """Algorithmic bytes of a quantize-only step over a BF16 [m, k] tensor."""
-    if kind == "quant2d":   # read once; codes + UE8M0 scales of x and of x^T
-        return m * k * (2 + 2 * (0.5 + 1.0 / 32))
-    return m * k * (2 + 2 + 0.5 + 1.0 / 16)  # NVFP4: amax read + quantize read; codes + E4M3 scales
+def quant_step_bytes(w, m, k):
+    """Algorithmic bytes of a quantize-only step (workload w) over a BF16 [m, k] tensor."""
+    nv = w["fmt"] == "nvfp4"
+    amax = 2 if nv else 0                   # NVFP4: the amax pass reads x once more
+    blk = 16 if nv else 32
+    if w["kind"] == "quant2d":              # x read once; codes + scales of x and of x^T
+        return m * k * (amax + 2 + 2 * (0.5 + 1.0 / blk))
+    return m * k * (amax + 2 + 0.5 + 1.0 / blk)
 L2_BYTES = 129 * 1024 * 1024
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 : BF16 tensor ratio on GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -221,6 +224,10 @@ class DeviceWorkload:
                 s["codes_t"] = torch.empty(m * k // 2, dtype=u8, device=dev)
                 s["sf_t"] = torch.empty(mx.mx_scale_bytes(k, m, self.fmt, mx.MX_SCALE_TCGEN05),
                                         dtype=u8, device=dev)
+                if self.fmt == mx.MX_FMT_NVFP4:
+                    s["ts_a"] = torch.zeros(1, dtype=torch.float32, device=dev)
+                    s["qws"] = torch.empty(mx.mx_quantize_workspace_bytes(m, k, self.fmt),
+                                           dtype=u8, device=dev)
                 self.sets.append(s)
                 continue
             if self.kind == "quant_sr":
@@ -261,6 +268,14 @@ class DeviceWorkload:
         mx = self.mx
         m, n, k, fmt = self.m, self.n, self.k, self.fmt
         out = []
+        if self.kind == "quant2d" and fmt == mx.MX_FMT_NVFP4:
+            sr = 1 if self.w.get("sr") else 0
+
+            def qnv2d(s, st):
+                mx.nvfp4_quantize_bf16_2d(s["x_a"], m, k, k, mx.MX_SCALE_TCGEN05, s["codes_a"],
+                                          s["sf_a"], s["codes_t"], s["sf_t"], s["ts_a"], sr,
+                                          SR_SEED, 10, s["qws"], stream=st)
+            return [("quantize_2d", qnv2d)]
         if self.kind == "quant2d":
             def q2d(s, st):
                 mx.mx_quantize_bf16_2d(s["x_a"], m, k, k, fmt, mx.MX_SCALE_TCGEN05, s["codes_a"],
@@ -295,7 +310,7 @@ class DeviceWorkload:
         """Kernel launches of each call of the step (matches the library's launches)."""
         mx = self.mx
         if self.kind == "quant2d":
-            return {"quantize_2d": 1}
+            return {"quantize_2d": 1 if self.fmt == mx.MX_FMT_MXFP4 else 2}
         if self.kind == "quant_sr":
             return {"quantize_sr": 2}
         q = 1 if self.fmt == mx.MX_FMT_MXFP4 else 2
@@ -311,9 +326,9 @@ class DeviceWorkload:
         blk = 32 if self.fmt == self.mx.MX_FMT_MXFP4 else 16
         if self.kind == "quant2d":
             # BF16 read once, codes and scales written for x and for x^T
-            return {"quantize_2d": (quant_step_bytes(self.kind, m, k), 0.0)}
+            return {"quantize_2d": (quant_step_bytes(self.w, m, k), 0.0)}
         if self.kind == "quant_sr":
-            return {"quantize_sr": (quant_step_bytes(self.kind, m, k), 0.0)}
+            return {"quantize_sr": (quant_step_bytes(self.w, m, k), 0.0)}
         amax_pass = 0 if self.fmt == self.mx.MX_FMT_MXFP4 else 2
         qbytes = lambda r: r * k * (2 + amax_pass + 0.5 + 1.0 / blk)
         out_b = 2 if self.out == self.mx.MX_OUT_BF16 else 4
@@ -473,7 +488,10 @@ def oracle_step_sample(name, host, frac, prepared):
     t0 = time.perf_counter()
     if w["kind"] == "quant2d":
         mr = max(32, mr // 32 * 32)
-        oracle.mx_quantize_2d(host["a"][:mr])
+        if w["fmt"] == "nvfp4":
+            oracle.nvfp4_quantize_2d(host["a"][:mr], seed=SR_SEED if w.get("sr") else None)
+        else:
+            oracle.mx_quantize_2d(host["a"][:mr])
         return time.perf_counter() - t0, mr / m
     if w["kind"] == "quant_sr":
         oracle.nvfp4_quantize_sr(host["a"][:mr], SR_SEED, 10)
@@ -523,7 +541,7 @@ def cpu_baseline(name, host, target_s):
     t, f = oracle_step_sample(name, host, frac, prepared)
     kind = synth.WORKLOADS[name]["kind"]
     if kind in QUANT_KINDS:
-        gbs = quant_step_bytes(kind, m, k) * f / t / 1e9
+        gbs = quant_step_bytes(synth.WORKLOADS[name], m, k) * f / t / 1e9
         what = "both directions" if kind == "quant2d" else "stochastic rounding"
         return {"value": gbs, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
                 "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} rows, {what}), "
@@ -732,7 +750,7 @@ def main_reference(args):
     kind = synth.WORKLOADS[name]["kind"]
     quant_only = kind in QUANT_KINDS
     unit = "GB/s" if quant_only else "TFLOPS"
-    value = (quant_step_bytes(kind, m, k) * f / mean_t / 1e9 if quant_only
+    value = (quant_step_bytes(synth.WORKLOADS[name], m, k) * f / mean_t / 1e9 if quant_only
              else 2.0 * m * n * k * f / mean_t / 1e12)
     sample = (f"{f:.5f} of one step per step ({int(round(f * m))} of {m} output rows with the "
               f"matching share of the quantize work)")

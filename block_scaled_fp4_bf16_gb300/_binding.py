@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_quantize_bf16_sr.restype = i32
         L.nvfp4_quantize_bf16_sr.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, ctypes.c_uint64,
                                              i32, vp, sz, vp]
+        L.nvfp4_quantize_bf16_2d.restype = i32
+        L.nvfp4_quantize_bf16_2d.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, vp, i32,
+                                             ctypes.c_uint64, i32, vp, sz, vp]
         L.mx_quantize_bf16_2d.restype = i32
         L.mx_quantize_bf16_2d.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
         L.mx_scale_relayout.restype = i32
@@ -197,6 +200,17 @@ def mx_quantize_bf16_2d(x, rows, cols, ld_x, fmt, scale_layout, codes, scales, c
     return _check("mx_quantize_bf16_2d", lib().mx_quantize_bf16_2d(
         _ptr(x), rows, cols, ld_x, fmt, scale_layout, _ptr(codes), _ptr(scales), _ptr(codes_t),
         _ptr(scales_t), _stream(stream)))
+
+
+def nvfp4_quantize_bf16_2d(x, rows, cols, ld_x, scale_layout, codes, scales, codes_t, scales_t,
+                           tensor_scale, stochastic=0, seed=0, philox_rounds=10, workspace=None,
+                           workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("nvfp4_quantize_bf16_2d", lib().nvfp4_quantize_bf16_2d(
+        _ptr(x), rows, cols, ld_x, scale_layout, _ptr(codes), _ptr(scales), _ptr(codes_t),
+        _ptr(scales_t), _ptr(tensor_scale), int(stochastic), int(seed) & 0xFFFFFFFFFFFFFFFF,
+        philox_rounds, _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def mx_scale_relayout(plain, rows, cols, fmt, tiled, stream=None):

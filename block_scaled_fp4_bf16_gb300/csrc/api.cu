@@ -462,6 +462,60 @@ MX_API int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_
                                              static_cast<cudaStream_t>(stream)));
 }
 
+MX_API int nvfp4_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  int scale_layout, void *codes, void *scales, void *codes_t,
+                                  void *scales_t, float *tensor_scale, int stochastic,
+                                  uint64_t seed, int philox_rounds, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  const int fmt = MX_FMT_NVFP4;
+  // codes and scales may both be null (columnwise output only)
+  const bool rowwise = codes != nullptr || scales != nullptr;
+  if (!x || !codes_t || !scales_t || !tensor_scale || (rowwise && (!codes || !scales)))
+    return MX_ERR_INVALID_ARG;
+  if (scale_layout != MX_SCALE_PLAIN && scale_layout != MX_SCALE_TCGEN05) return MX_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || ld_x < cols) return MX_ERR_INVALID_ARG;
+  if (stochastic != 0 && stochastic != 1) return MX_ERR_INVALID_ARG;
+  if (stochastic && (philox_rounds < 1 || philox_rounds > MX_PHILOX_MAX_ROUNDS))
+    return MX_ERR_INVALID_ARG;
+  if (rows % 16 != 0 || cols % 16 != 0) return MX_ERR_UNSUPPORTED_SHAPE;
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED_SHAPE;
+  if ((rows + 127) / 128 * 128 * (cols / 16) >= (int64_t(1) << 31) ||
+      (cols + 127) / 128 * 128 * (rows / 16) >= (int64_t(1) << 31))
+    return MX_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || (ld_x % 8) != 0 || !aligned16(codes) || !aligned16(scales) ||
+      !aligned16(codes_t) || !aligned16(scales_t) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return MX_ERR_ALIGNMENT;  // (a null pointer is aligned)
+  if (!workspace || workspace_bytes < mx_quantize_workspace_bytes(rows, cols, fmt))
+    return MX_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+  // Both outputs are written concurrently from the same input: no output may
+  // overlap the input, the workspace or another output.
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
+  const Range in{xb, xb + static_cast<uintptr_t>(((rows - 1) * ld_x + cols) * 2)};
+  const uintptr_t wsb = reinterpret_cast<uintptr_t>(workspace);
+  const Range out[6] = {
+      {reinterpret_cast<uintptr_t>(codes), reinterpret_cast<uintptr_t>(codes) + static_cast<uintptr_t>(rows * cols / 2)},
+      {reinterpret_cast<uintptr_t>(scales), reinterpret_cast<uintptr_t>(scales) + mx_scale_bytes(rows, cols, fmt, scale_layout)},
+      {reinterpret_cast<uintptr_t>(codes_t), reinterpret_cast<uintptr_t>(codes_t) + static_cast<uintptr_t>(rows * cols / 2)},
+      {reinterpret_cast<uintptr_t>(scales_t), reinterpret_cast<uintptr_t>(scales_t) + mx_scale_bytes(cols, rows, fmt, scale_layout)},
+      {reinterpret_cast<uintptr_t>(tensor_scale), reinterpret_cast<uintptr_t>(tensor_scale) + sizeof(float)},
+      {wsb, wsb + mx_quantize_workspace_bytes(rows, cols, fmt)}};
+  for (int o = rowwise ? 0 : 2; o < 6; ++o) {
+    if (overlap(out[o], in)) return MX_ERR_INVALID_ARG;
+    for (int p = o + 1; p < 6; ++p)
+      if (overlap(out[o], out[p])) return MX_ERR_INVALID_ARG;
+  }
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  const mx::SrArgs sr{seed, philox_rounds, 0u};
+  return launch_rc(mx::launch_nvfp4_quantize_2d(
+      x, rows, cols, ld_x, scale_layout == MX_SCALE_TCGEN05, codes, scales, codes_t, scales_t,
+      tensor_scale, static_cast<uint32_t *>(workspace), stochastic ? &sr : nullptr,
+      static_cast<cudaStream_t>(stream)));
+}
+
 MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format,
                              void *tiled, void *stream) {
   if (!plain || !tiled || !valid_format(format)) return MX_ERR_INVALID_ARG;

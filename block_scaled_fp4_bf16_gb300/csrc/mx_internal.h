@@ -73,6 +73,14 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
 cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld, int tiled,
                                   void *codes, void *scales, void *codes_t, void *scales_t,
                                   cudaStream_t s);
+// Bidimensional NVFP4 quantize (rows, cols % 16): the amax pass into
+// `partials` (kAmaxPartials words), then rowwise codes/scales of x and of
+// x^T under one s_t; sr: stochastic rounding (direction 0 rowwise, 1
+// columnwise), null for round to nearest.
+cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                     int tiled, void *codes, void *scales, void *codes_t,
+                                     void *scales_t, float *tensor_scale, uint32_t *partials,
+                                     const SrArgs *sr, cudaStream_t s);
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
                                   cudaStream_t s);
 

@@ -400,6 +400,96 @@ __device__ __forceinline__ uint32_t div_to_e2m1x8_sr(const uint32_t *w, float de
   return out;
 }
 
+// Per-CTA constants of the NVFP4 rule.
+struct NvConst {
+  float s_t;      // amax_t / 2688
+  float six_s_t;  // 6 * s_t
+  float r6;       // RN(1 / (6 s_t)) when six_ok
+  bool six_ok;    // 6 s_t in [2^-100, 2^100]: amax_b / (6 s_t) by reciprocal + correction
+};
+
+// Reduces a tensor's kAmaxPartials partial maxima to s_t (thread 0 writes it
+// to *ts when write_ts) and fills den_tab / rcp_tab: den = E4M3(sb) * s_t and
+// RN(1 / den) for every scale byte sb (0 marks a den outside [2^-100, 2^100],
+// where the IEEE division is used instead).  Every thread of the CTA calls it
+// (it has barriers); the tables are visible to all on return.
+__device__ __forceinline__ NvConst nv_setup(const uint32_t *partials, float *ts, bool write_ts,
+                                            float *den_tab, float *rcp_tab) {
+  __shared__ uint32_t warp_max[kThreads / 32];
+  __shared__ float s_t_shared;
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < kAmaxPartials; i += kThreads) m = max(m, partials[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t v = 0;
+    for (int w = 0; w < kThreads / 32; ++w) v = max(v, warp_max[w]);
+    const float amax_t = __uint_as_float(v << 16);
+    const float s_t = __fdiv_rn(amax_t, 2688.0f);
+    s_t_shared = s_t;
+    if (write_ts) *ts = s_t;
+  }
+  __syncthreads();
+  NvConst c;
+  c.s_t = s_t_shared;
+  c.six_s_t = __fmul_rn(6.0f, c.s_t);
+  if (threadIdx.x < 128) {
+    const float den = __fmul_rn(e4m3_to_f32(threadIdx.x), c.s_t);
+    den_tab[threadIdx.x] = den;
+    rcp_tab[threadIdx.x] = (den >= 0x1p-100f && den <= 0x1p+100f) ? rcp_rn(den) : 0.0f;
+  }
+  // amax_b / (6 s_t) is taken the same way: RN(amax_b * r6) and one FMA
+  // correction give the correctly rounded quotient (Markstein) while 6 s_t
+  // stays in [2^-100, 2^100].  A quotient small enough for the correction to
+  // be inexact (fp32 subnormal) gives sb = 0 either way.
+  c.six_ok = c.six_s_t >= 0x1p-100f && c.six_s_t <= 0x1p+100f;
+  c.r6 = c.six_ok ? rcp_rn(c.six_s_t) : 0.0f;
+  __syncthreads();
+  return c;
+}
+
+// Scale byte and codes (element 2t in the low nibble of byte t) of one
+// 16-element block, given as eight BF16x2 words.  SR != 0 rounds the codes
+// stochastically with the Philox draw of counter (j, r, dir, 0).
+template <int SR>
+__device__ __forceinline__ uint32_t nv_block(const uint32_t *w, const NvConst &c,
+                                             const float *den_tab, const float *rcp_tab,
+                                             uint32_t j, uint32_t r, uint32_t dir, uint32_t k0,
+                                             uint32_t k1, int rounds, uint2 &out) {
+  const uint32_t amax = block_amax<8>(w);
+  uint32_t sb = 0;
+  if (c.s_t > 0.0f) {
+    const float a = __uint_as_float(amax << 16);
+    float q6;
+    if (c.six_ok) {
+      const float q0 = __fmul_rn(a, c.r6);
+      q6 = __fmaf_rn(__fmaf_rn(-q0, c.six_s_t, a), c.r6, q0);
+    } else {
+      q6 = __fdiv_rn(a, c.six_s_t);
+    }
+    sb = cvt_e4m3(q6);
+  }
+  out = make_uint2(0u, 0u);
+  if (sb != 0) {
+    const float den = den_tab[sb];
+    const float rc = rcp_tab[sb];
+    if constexpr (SR != 0) {
+      const uint4 d = philox4x32<SR>(make_uint4(j, r, dir, 0u), k0, k1, rounds);
+      out.x = div_to_e2m1x8_sr(&w[0], den, rc, d.x, d.y);
+      out.y = div_to_e2m1x8_sr(&w[4], den, rc, d.z, d.w);
+    } else if (rc != 0.0f) {
+      out.x = div_to_e2m1x8(&w[0], den, rc);
+      out.y = div_to_e2m1x8(&w[4], den, rc);
+    } else {
+      out.x = div_to_e2m1x8_ieee(&w[0], den);
+      out.y = div_to_e2m1x8_ieee(&w[4], den);
+    }
+  }
+  return sb;
+}
+
 // NVFP4 pass 2: every CTA reduces its tensor's partial maxima to s_t, then
 // thread b quantizes 16-element block b.  Each binary32 step of the
 // definition is one round-to-nearest operation (correctly rounded divisions
@@ -414,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_kernel(const __gri
   const uint32_t cta = gridDim.x - 1 - blockIdx.x;
   const QTensor &t = group_member(g, cta);
   // The thread's blocks are loaded first: their latency then overlaps the
-  // reduction of the partial maxima below, which they do not depend on.
+  // reduction of the partial maxima, which they do not depend on.
   const uint32_t kb = t.kbdiv.d;
   const uint32_t base = (cta - t.first_cta) * (kThreads * kNvBlocksPerThread) + threadIdx.x;
   uint8_t *__restrict__ scales = t.scales;
@@ -428,80 +518,17 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_kernel(const __gri
     if (b < t.total && rq[q] < t.rows)
       load32<WIDE>(t.x + static_cast<int64_t>(rq[q]) * t.ld + jq[q] * 16u, w[q]);
   }
-  __shared__ uint32_t warp_max[kThreads / 32];
-  __shared__ float s_t_shared;
-  // den = E4M3(sb) * s_t and RN(1 / den) for every scale byte sb (0 marks a
-  // den outside [2^-100, 2^100], where the IEEE division is used instead)
   __shared__ float den_tab[128], rcp_tab[128];
-  {
-    uint32_t m = 0;
-    for (int i = threadIdx.x; i < kAmaxPartials; i += kThreads) m = max(m, t.partials[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t v = 0;
-      for (int w = 0; w < kThreads / 32; ++w) v = max(v, warp_max[w]);
-      const float amax_t = __uint_as_float(v << 16);
-      const float s_t = __fdiv_rn(amax_t, 2688.0f);
-      s_t_shared = s_t;
-      if (cta == t.first_cta) *t.tensor_scale = s_t;
-    }
-    __syncthreads();
-  }
-  const float s_t = s_t_shared;
-  const float six_s_t = __fmul_rn(6.0f, s_t);
-  if (threadIdx.x < 128) {
-    const float den = __fmul_rn(e4m3_to_f32(threadIdx.x), s_t);
-    den_tab[threadIdx.x] = den;
-    rcp_tab[threadIdx.x] = (den >= 0x1p-100f && den <= 0x1p+100f) ? rcp_rn(den) : 0.0f;
-  }
-  // amax_b / (6 s_t) is taken the same way: RN(amax_b * r6) and one FMA
-  // correction give the correctly rounded quotient (Markstein) while 6 s_t
-  // stays in [2^-100, 2^100].  A quotient small enough for the correction to
-  // be inexact (fp32 subnormal) gives sb = 0 either way.
-  const bool six_ok = six_s_t >= 0x1p-100f && six_s_t <= 0x1p+100f;
-  const float r6 = six_ok ? rcp_rn(six_s_t) : 0.0f;
-  __syncthreads();
-
+  const NvConst c = nv_setup(t.partials, t.tensor_scale, cta == t.first_cta, den_tab, rcp_tab);
 #pragma unroll
   for (int q = 0; q < kNvBlocksPerThread; ++q) {
     if (base + q * kThreads >= t.total) continue;
     const uint32_t r = rq[q], j = jq[q];
     uint32_t sb = 0;
     if (r < t.rows) {
-      const uint32_t amax = block_amax<8>(w[q]);
-      if (s_t > 0.0f) {
-        const float a = __uint_as_float(amax << 16);
-        float q6;
-        if (six_ok) {
-          const float q0 = __fmul_rn(a, r6);
-          q6 = __fmaf_rn(__fmaf_rn(-q0, six_s_t, a), r6, q0);
-        } else {
-          q6 = __fdiv_rn(a, six_s_t);
-        }
-        sb = cvt_e4m3(q6);
-      }
-      uint2 out = make_uint2(0u, 0u);
-      if (sb != 0 && SR != 0) {
-        const float den = den_tab[sb];
-        const float rc = rcp_tab[sb];
-        const uint4 d = philox4x32<SR>(make_uint4(j, r, g.sr_direction, 0u), g.sr_key0, g.sr_key1,
-                                       g.sr_rounds);
-        out.x = div_to_e2m1x8_sr(&w[q][0], den, rc, d.x, d.y);
-        out.y = div_to_e2m1x8_sr(&w[q][4], den, rc, d.z, d.w);
-      } else if (sb != 0) {
-        const float den = den_tab[sb];
-        const float rc = rcp_tab[sb];
-        if (rc != 0.0f) {
-          out.x = div_to_e2m1x8(&w[q][0], den, rc);
-          out.y = div_to_e2m1x8(&w[q][4], den, rc);
-        } else {
-          out.x = div_to_e2m1x8_ieee(&w[q][0], den);
-          out.y = div_to_e2m1x8_ieee(&w[q][4], den);
-        }
-      }
+      uint2 out;
+      sb = nv_block<SR>(w[q], c, den_tab, rcp_tab, j, r, g.sr_direction, g.sr_key0, g.sr_key1,
+                        g.sr_rounds, out);
       *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
     }
     if (t.tiled) {
@@ -632,6 +659,122 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_2d_kernel(const __grid_c
   }
 }
 
+// Bidimensional NVFP4 quantize: as mx_quantize_2d_kernel with 16-element
+// blocks along both directions and the NVFP4 rule (each CTA first reduces
+// the tensor's partial maxima to s_t, as pass 2 does).  One CTA owns a 64-row
+// x 256-column tile:
+//   rowwise     each thread loads four 16-element row blocks (32-byte loads),
+//               quantizes them and parks them in shared memory;
+//   columnwise  after one barrier, each thread reads a column pair of a
+//               16-row block (one 32-bit word per row), regroups the halves
+//               into two columns and quantizes both into x^T [cols, rows / 2];
+//               this is done for two (pair, row block) units per thread.
+// The two 16-byte chunks of a parked block are swapped in every other group
+// of four blocks, so that the eight threads of a quarter warp store to eight
+// different bank groups.  Stochastic rounding draws with direction 0 for the
+// rowwise blocks and 1 for the columnwise ones.
+struct Nv2dArgs {
+  const uint16_t *x;
+  int64_t ld;
+  uint32_t rows, cols;
+  uint8_t *codes, *scales;      // x: [rows, cols / 2], scales of x (null: columnwise only)
+  uint8_t *codes_t, *scales_t;  // x^T: [cols, rows / 2], scales of x^T
+  const uint32_t *partials;     // the tensor's kAmaxPartials maxima (pass 1)
+  float *tensor_scale;          // s_t out
+  int tiled;
+  uint32_t kb, kbt;             // scale columns of x and of x^T (cols / 16, rows / 16)
+  uint32_t katoms, katoms_t;    // 4-scale atoms along a row of x and of x^T
+  uint32_t rows_pad, cols_pad;  // rows of x and of x^T with tiled padding
+  uint32_t key0, key1;          // Philox key (stochastic rounding)
+  int rounds;
+};
+
+template <bool WIDE, int SR>
+__global__ void __launch_bounds__(kThreads) nvfp4_quantize_2d_kernel(const __grid_constant__ Nv2dArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  __shared__ __align__(16) uint32_t tile[k2dRows][k2dCols / 2];
+  __shared__ float den_tab[128], rcp_tab[128];
+  const uint32_t r0 = blockIdx.y * k2dRows;
+  const uint32_t c0 = blockIdx.x * k2dCols;
+  constexpr int kPer = k2dRows * (k2dCols / 16) / kThreads;  // row blocks per thread (4)
+  uint32_t w[kPer][8];
+#pragma unroll
+  for (int h = 0; h < kPer; ++h) {
+    const uint32_t idx = threadIdx.x + h * kThreads;
+    const uint32_t r = r0 + (idx >> 4), j = c0 / 16 + (idx & 15);
+    if (r < a.rows && j < a.kb) {
+      load32<WIDE>(a.x + static_cast<int64_t>(r) * a.ld + j * 16u, w[h]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[h][i] = 0u;
+    }
+  }
+  const NvConst c = nv_setup(a.partials, a.tensor_scale, blockIdx.x == 0 && blockIdx.y == 0,
+                             den_tab, rcp_tab);
+#pragma unroll
+  for (int h = 0; h < kPer; ++h) {
+    const uint32_t idx = threadIdx.x + h * kThreads;
+    const uint32_t lr = idx >> 4, lb = idx & 15;  // tile row, 16-column block
+    const uint32_t r = r0 + lr, j = c0 / 16 + lb;
+    const bool inside = r < a.rows && j < a.kb;
+    uint4 *dst = reinterpret_cast<uint4 *>(&tile[lr][lb * 8]);
+    const uint32_t sw = (lb >> 2) & 1u;
+    dst[sw] = make_uint4(w[h][0], w[h][1], w[h][2], w[h][3]);
+    dst[sw ^ 1u] = make_uint4(w[h][4], w[h][5], w[h][6], w[h][7]);
+    if (a.codes == nullptr) continue;  // columnwise only (uniform across the grid)
+    uint32_t sb = 0;
+    if (inside) {
+      uint2 out;
+      sb = nv_block<SR>(w[h], c, den_tab, rcp_tab, j, r, 0u, a.key0, a.key1, a.rounds, out);
+      *reinterpret_cast<uint2 *>(a.codes + static_cast<int64_t>(r) * (a.cols >> 1) + j * 8u) = out;
+    }
+    if (a.tiled) {
+      if (r < a.rows_pad && j < a.katoms * 4u)
+        a.scales[tiled_offset(r, j, a.katoms)] = static_cast<uint8_t>(sb);
+    } else if (inside) {
+      a.scales[static_cast<int64_t>(r) * a.kb + j] = static_cast<uint8_t>(sb);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const uint32_t unit = threadIdx.x + u * kThreads;
+    const uint32_t cp = unit & 127u;          // column pair of the tile
+    const uint32_t rb = unit >> 7;            // 16-row block of the tile
+    const uint32_t i = r0 / 16 + rb;          // scale column of x^T
+    const uint32_t lb = cp >> 3;              // 16-column block holding the pair
+    const uint32_t chunk = ((cp >> 2) & 1u) ^ ((lb >> 2) & 1u);
+    const uint32_t wsw = lb * 8 + chunk * 4 + (cp & 3u);
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint32_t a0 = tile[rb * 16 + 2 * m][wsw];
+      const uint32_t a1 = tile[rb * 16 + 2 * m + 1][wsw];
+      lo[m] = __byte_perm(a0, a1, 0x5410);
+      hi[m] = __byte_perm(a0, a1, 0x7632);
+    }
+#pragma unroll
+    for (int qc = 0; qc < 2; ++qc) {
+      const uint32_t col = c0 + 2 * cp + qc;
+      const bool inside = col < a.cols && i < a.kbt;
+      uint32_t sb = 0;
+      if (inside) {
+        uint2 out;
+        sb = nv_block<SR>(qc ? hi : lo, c, den_tab, rcp_tab, i, col, 1u, a.key0, a.key1, a.rounds,
+                          out);
+        *reinterpret_cast<uint2 *>(a.codes_t + static_cast<int64_t>(col) * (a.rows >> 1) + i * 8u) = out;
+      }
+      if (a.tiled) {
+        if (col < a.cols_pad && i < a.katoms_t * 4u)
+          a.scales_t[tiled_offset(col, i, a.katoms_t)] = static_cast<uint8_t>(sb);
+      } else if (inside) {
+        a.scales_t[static_cast<int64_t>(col) * a.kbt + i] = static_cast<uint8_t>(sb);
+      }
+    }
+  }
+}
+
 // Plain [rows, kb] -> tiled order; one thread per output byte (padding 0).
 __global__ void __launch_bounds__(kThreads) scale_relayout_kernel(
     const uint8_t *__restrict__ plain, int64_t rows, int64_t kb, uint8_t *__restrict__ tiled,
@@ -741,6 +884,62 @@ cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int
   // 32 KB of shared memory per CTA: ask for the largest carve-out so that
   // registers, not shared memory, bound the CTAs per SM (idempotent).
   const cudaError_t e = launch_pdl(kern, dim3(gx, gy), dim3(kThreads), 0, s, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                     int tiled, void *codes, void *scales, void *codes_t,
+                                     void *scales_t, float *tensor_scale, uint32_t *partials,
+                                     const SrArgs *sr, cudaStream_t s) {
+  if (sr && (sr->rounds < 1 || sr->rounds > kPhiloxMaxRounds)) return cudaErrorInvalidValue;
+  const bool wide = wide_ok(x, ld);
+  // pass 1: the tensor's partial maxima
+  QGroup g{};
+  g.count = 1;
+  QTensor &t = g.t[0];
+  t.x = static_cast<const uint16_t *>(x);
+  t.partials = partials;
+  t.ld = ld;
+  t.rows = static_cast<uint32_t>(rows);
+  t.cols = static_cast<uint32_t>(cols);
+  t.real_total = t.rows * (t.cols / 16u);
+  t.kbdiv = make_fastdiv(t.cols / 16u);
+  cudaError_t e = launch_pdl(wide ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>,
+                             dim3(kAmaxPartials, 1), dim3(kThreads), 0, s, g);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  Nv2dArgs a{};
+  a.x = static_cast<const uint16_t *>(x);
+  a.ld = ld;
+  a.rows = static_cast<uint32_t>(rows);
+  a.cols = static_cast<uint32_t>(cols);
+  a.codes = static_cast<uint8_t *>(codes);
+  a.scales = static_cast<uint8_t *>(scales);
+  a.codes_t = static_cast<uint8_t *>(codes_t);
+  a.scales_t = static_cast<uint8_t *>(scales_t);
+  a.partials = partials;
+  a.tensor_scale = tensor_scale;
+  a.tiled = tiled;
+  a.kb = a.cols / 16;
+  a.kbt = a.rows / 16;
+  a.katoms = (a.kb + 3) / 4;
+  a.katoms_t = (a.kbt + 3) / 4;
+  a.rows_pad = tiled ? (a.rows + 127) / 128 * 128 : a.rows;
+  a.cols_pad = tiled ? (a.cols + 127) / 128 * 128 : a.cols;
+  if (sr) {
+    a.key0 = static_cast<uint32_t>(sr->seed);
+    a.key1 = static_cast<uint32_t>(sr->seed >> 32);
+    a.rounds = sr->rounds;
+  }
+  // the tiles cover the tiled padding of both outputs
+  const uint32_t gx = (a.cols_pad + k2dCols - 1) / k2dCols;
+  const uint32_t gy = (a.rows_pad + k2dRows - 1) / k2dRows;
+  auto kern = wide ? nvfp4_quantize_2d_kernel<true, 0> : nvfp4_quantize_2d_kernel<false, 0>;
+  if (sr && sr->rounds == 10)
+    kern = wide ? nvfp4_quantize_2d_kernel<true, 10> : nvfp4_quantize_2d_kernel<false, 10>;
+  else if (sr)
+    kern = wide ? nvfp4_quantize_2d_kernel<true, -1> : nvfp4_quantize_2d_kernel<false, -1>;
+  e = launch_pdl(kern, dim3(gx, gy), dim3(kThreads), 0, s, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -90,6 +90,10 @@ WORKLOADS = {
     # 16384 x 8192 gradient-like tensor: no GEMM (n = 0), HBM bound.
     "nvfp4_sr_16384x8192": dict(kind="quant_sr", fmt="nvfp4", m=16384, n=0, k=8192,
                                 sigma_a=1e-3, out="codes", split_k=1),
+    # Bidimensional NVFP4 quantize with stochastic rounding (rowwise and
+    # columnwise outputs) of the same tensor: no GEMM, HBM bound.
+    "nvfp4_quant2d_sr_16384x8192": dict(kind="quant2d", fmt="nvfp4", sr=True, m=16384, n=0,
+                                        k=8192, sigma_a=1e-3, out="codes", split_k=1),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 

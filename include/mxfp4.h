@@ -207,7 +207,9 @@ int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, int for
  *   codes_t, scales_t: out, exactly what mx_quantize_bf16 writes for x^T:
  *             codes_t [cols, rows / 2] bytes, scales_t
  *             mx_scale_bytes(cols, rows, format, scale_layout) bytes.
- * format: MX_FMT_MXFP4 only (MX_FMT_NVFP4 -> MX_ERR_UNSUPPORTED_FEATURE).
+ * format: MX_FMT_MXFP4 only (MX_FMT_NVFP4 -> MX_ERR_UNSUPPORTED_FEATURE; the
+ * NVFP4 form, which also needs a tensor scale and a workspace, is
+ * nvfp4_quantize_bf16_2d below).
  * No output may overlap the input or another output (MX_ERR_INVALID_ARG).
  * Launches one kernel; each element of x is read from memory once.
  *
@@ -223,6 +225,34 @@ int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, int for
 int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x, int format,
                         int scale_layout, void *codes, void *scales, void *codes_t,
                         void *scales_t, void *stream);
+
+/* Bidimensional NVFP4 quantize: the rowwise NVFP4 quantize of x and of x^T
+ * (blocks of 16 down a column of x) in one pass over x, under the one tensor
+ * scale s_t = amax(x) / 2688 (NVIDIA/TransformerEngine #3809: the
+ * rowwise + columnwise kernel, columnwise output transposed, passed as
+ * (cols, rows)).
+ *   x:        BF16 [rows, cols], row stride ld_x elements (ld_x >= cols,
+ *             ld_x % 8 == 0); rows % 16 == 0 and cols % 16 == 0.
+ *   codes, scales:     out, exactly what mx_quantize_bf16 (MX_FMT_NVFP4)
+ *             writes for x; both NULL for the columnwise output alone.
+ *   codes_t, scales_t: out, exactly what it writes for x^T: codes_t
+ *             [cols, rows / 2] bytes, scales_t mx_scale_bytes(cols, rows,
+ *             MX_FMT_NVFP4, scale_layout) bytes.
+ *   tensor_scale: out, s_t (device pointer, 4-byte aligned).
+ *   stochastic: 0 rounds the codes to nearest (seed, philox_rounds ignored);
+ *             1 rounds them as nvfp4_quantize_bf16_sr does, the rowwise
+ *             blocks with direction 0 and the columnwise blocks (row c of
+ *             x^T, j-th block along it) with direction 1 in the counter
+ *             (j, c, 1, 0); philox_rounds 1..MX_PHILOX_MAX_ROUNDS.
+ *   workspace: mx_quantize_workspace_bytes(rows, cols, MX_FMT_NVFP4) bytes.
+ * No output (nor the workspace) may overlap the input or another output
+ * (MX_ERR_INVALID_ARG).  Launches two kernels (amax, then the bidimensional
+ * quantize, which reads each element of x from memory once). */
+int nvfp4_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld_x,
+                           int scale_layout, void *codes, void *scales, void *codes_t,
+                           void *scales_t, float *tensor_scale, int stochastic, uint64_t seed,
+                           int philox_rounds, void *workspace, size_t workspace_bytes,
+                           void *stream);
 
 /* Plain scales [rows, cols / block] -> MX_SCALE_TCGEN05 order (see
  * mx_scale_bytes).  `tiled` receives mx_scale_bytes(rows, cols, format,

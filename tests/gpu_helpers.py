@@ -125,6 +125,35 @@ def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
             codes_t.cpu().numpy().reshape(cols, rows // 2), scales_t.cpu().numpy())
 
 
+def gpu_quantize_nv2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
+                      columnwise_only: bool = False, seed: int | None = None, rounds: int = 10):
+    """Bidimensional NVFP4 quantize on the GPU (stochastic rounding when a seed
+    is given); returns host (codes, scales, codes_t, scales_t, s_t), outputs
+    pre-filled with 0xAB (codes and scales None for the columnwise output alone)."""
+    rows, cols = x_bits.shape
+    ld = cols if ld is None else ld
+    padded = np.zeros((rows, ld), np.uint16)
+    padded[:, :cols] = x_bits
+    x = dev_bf16(padded)
+    fill = lambda n: torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")
+    fmt = mx.MX_FMT_NVFP4
+    codes, codes_t = fill(rows * cols // 2), fill(rows * cols // 2)
+    scales = fill(mx.mx_scale_bytes(rows, cols, fmt, layout))
+    scales_t = fill(mx.mx_scale_bytes(cols, rows, fmt, layout))
+    ts = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(mx.mx_quantize_workspace_bytes(rows, cols, fmt), dtype=torch.uint8,
+                     device="cuda")
+    if columnwise_only:
+        codes = scales = None
+    mx.nvfp4_quantize_bf16_2d(x, rows, cols, ld, layout, codes, scales, codes_t, scales_t, ts,
+                              0 if seed is None else 1, 0 if seed is None else seed, rounds, ws)
+    torch.cuda.synchronize()
+    return (None if codes is None else codes.cpu().numpy().reshape(rows, cols // 2),
+            None if scales is None else scales.cpu().numpy(),
+            codes_t.cpu().numpy().reshape(cols, rows // 2), scales_t.cpu().numpy(),
+            np.float32(ts.item()))
+
+
 def gpu_relayout(plain: np.ndarray, rows: int, cols: int, fmt: int) -> torch.Tensor:
     tiled = torch.full((mx.mx_scale_bytes(rows, cols, fmt, mx.MX_SCALE_TCGEN05),), 0xAB,
                        dtype=torch.uint8, device="cuda")

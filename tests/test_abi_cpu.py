@@ -133,6 +133,41 @@ def test_quantize_sr_argument_validation(lib):
     assert call(ws=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
 
 
+def test_nvfp4_quantize_2d_argument_validation(lib):
+    MB = 1 << 20
+    q = lib.nvfp4_quantize_bf16_2d
+    ok = dict(x=FAKE, rows=64, cols=96, ld=96, lay=1, c=FAKE + MB, s=FAKE + 2 * MB,
+              ct=FAKE + 3 * MB, st=FAKE + 4 * MB, ts=FAKE + 5 * MB, sr=1, rounds=10,
+              ws=FAKE + 6 * MB, wsb=1 << 16)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return q(a["x"], a["rows"], a["cols"], a["ld"], a["lay"], a["c"], a["s"], a["ct"], a["st"],
+                 a["ts"], a["sr"], 1234, a["rounds"], a["ws"], a["wsb"], None)
+    assert call(x=None) == mx.MX_ERR_INVALID_ARG
+    assert call(ct=None) == mx.MX_ERR_INVALID_ARG
+    assert call(ts=None) == mx.MX_ERR_INVALID_ARG
+    assert call(ld=64) == mx.MX_ERR_INVALID_ARG
+    assert call(lay=3) == mx.MX_ERR_INVALID_ARG
+    assert call(sr=2) == mx.MX_ERR_INVALID_ARG
+    assert call(rounds=0) == mx.MX_ERR_INVALID_ARG
+    assert call(rounds=17) == mx.MX_ERR_INVALID_ARG
+    assert call(rows=40) == mx.MX_ERR_UNSUPPORTED_SHAPE           # rows % 16
+    assert call(cols=88, ld=88) == mx.MX_ERR_UNSUPPORTED_SHAPE    # cols % 16
+    assert call(st=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
+    assert call(ts=FAKE + 5 * MB + 2) == mx.MX_ERR_ALIGNMENT
+    assert call(ld=100) == mx.MX_ERR_ALIGNMENT                    # ld % 8
+    assert call(ws=None) == mx.MX_ERR_WORKSPACE
+    assert call(wsb=8) == mx.MX_ERR_WORKSPACE
+    assert call(ct=FAKE + MB + 64) == mx.MX_ERR_INVALID_ARG       # codes_t overlaps codes
+    assert call(c=FAKE + 1024) == mx.MX_ERR_INVALID_ARG           # codes overlap the input
+    assert call(ws=FAKE + 4 * MB) == mx.MX_ERR_INVALID_ARG        # workspace overlaps scales_t
+    assert call(c=None) == mx.MX_ERR_INVALID_ARG                  # rowwise codes without scales
+    # rounding to nearest ignores the round count
+    assert call(sr=0, rounds=0, x=None) == mx.MX_ERR_INVALID_ARG
+
+
 def _group(lib, tensors, fmt=0, layout=0, ws=None, wsb=0):
     arr = (mx.mx_quantize_tensor * max(1, len(tensors)))()
     for i, t in enumerate(tensors):

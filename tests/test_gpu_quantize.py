@@ -6,8 +6,8 @@ import pytest
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import (gpu_quantize, gpu_quantize_2d, gpu_quantize_group, gpu_quantize_sr,
-                               gpu_relayout)
+from tests.gpu_helpers import (gpu_quantize, gpu_quantize_2d, gpu_quantize_group, gpu_quantize_nv2d,
+                               gpu_quantize_sr, gpu_relayout)
 
 pytestmark = pytest.mark.gpu
 
@@ -378,3 +378,76 @@ def test_nvfp4_sr_is_deterministic_and_unbiased_on_the_gpu():
         acc += np.where(c & 8, -1.0, 1.0) * grid[c & 7]
     step = np.where(np.abs(q) < 2, 0.5, np.where(np.abs(q) < 4, 1.0, 2.0))
     assert np.all(np.abs(acc / n - q) <= step * (5 * 0.5 / np.sqrt(n) + 1 / 256))
+
+
+# ---------------------------------------------------------------- bidimensional NVFP4
+
+def _check_nv2d(x, layout, ld=None, seed=None, rounds=10):
+    codes, scales, codes_t, scales_t, s_t = gpu_quantize_nv2d(x, layout, ld=ld, seed=seed,
+                                                             rounds=rounds)
+    rc, rs, rct, rst, rt = oracle.nvfp4_quantize_2d(x, seed=seed, rounds=rounds)
+    assert np.float32(s_t).view(np.uint32) == np.float32(rt).view(np.uint32)
+    assert np.array_equal(codes, rc), "rowwise codes: " + _explain(x, codes, rc, scales, rs, 16)
+    assert np.array_equal(codes_t, rct), "columnwise codes: " + _explain(
+        np.ascontiguousarray(x.T), codes_t, rct, scales_t, rst, 16)
+    if layout == PLAIN:
+        assert np.array_equal(scales, rs.ravel()) and np.array_equal(scales_t, rst.ravel())
+    else:
+        assert np.array_equal(scales, oracle.scale_tile(rs))
+        assert np.array_equal(scales_t, oracle.scale_tile(rst))
+
+
+@pytest.mark.parametrize("rows,cols", [(16, 16), (32, 48), (64, 96), (96, 256), (160, 288),
+                                       (544, 1040), (256, 4096), (4096, 272)])
+@pytest.mark.parametrize("layout", [PLAIN, TILED])
+@pytest.mark.parametrize("seed", [None, 0x5EED])
+def test_nvfp4_quantize_2d_matches_oracle(rows, cols, layout, seed):
+    x = synth.bf16_normal(rows, cols, 1.0, seed=rows * 5 + cols)
+    x[0, :16] = 0                                     # zero row block
+    x[:16, min(5, cols - 1)] = 0x8000                 # column block of -0
+    _check_nv2d(x, layout, seed=seed)
+
+
+def test_nvfp4_quantize_2d_leading_dim_special_values_and_rounds():
+    x = synth.bf16_normal(96, 160, 3.0, seed=51)
+    x[2, :] = synth.f32_to_bf16_bits(np.full(160, 1e-40, np.float32))   # subnormals
+    x[:, 3] = 0x7F7F                                                   # largest finite
+    x[40:64, 70] = 0x0001
+    _check_nv2d(x, TILED, ld=168)                    # 16-byte (not 32-byte) aligned rows
+    _check_nv2d(x, PLAIN, ld=256, seed=7)
+    _check_nv2d(x, TILED, seed=0xFFFFFFFF00000001, rounds=7)
+    _check_nv2d(np.zeros((32, 64), np.uint16), PLAIN, seed=3)          # s_t = 0
+
+
+def test_nvfp4_quantize_2d_rowwise_equals_one_dimensional_calls():
+    """The rowwise output equals mx_quantize_bf16 / nvfp4_quantize_bf16_sr on x,
+    the columnwise output equals them on x^T with direction 1 (oracle) and the
+    same s_t."""
+    x = synth.bf16_normal(128, 192, 0.5, seed=52)
+    c, s, ct, st, ts = gpu_quantize_nv2d(x, TILED)
+    c1, s1, t1 = gpu_quantize(x, NV, TILED)
+    ct1, st1, tt1 = gpu_quantize(np.ascontiguousarray(x.T), NV, TILED)
+    assert np.array_equal(c, c1) and np.array_equal(s, s1) and ts == t1
+    assert np.array_equal(ct, ct1) and np.array_equal(st, st1) and tt1 == ts
+    c, s, ct, st, ts = gpu_quantize_nv2d(x, PLAIN, seed=99)
+    c1, s1, t1 = gpu_quantize_sr(x, 99, 10, PLAIN)
+    assert np.array_equal(c, c1) and np.array_equal(s, s1) and ts == t1
+
+
+def test_nvfp4_quantize_2d_full_size():
+    """The 16384 x 8192 tensor of the stochastic-rounding workload, both roundings."""
+    x = synth.workload_inputs("nvfp4_sr_16384x8192")["a"]
+    _check_nv2d(x, TILED, seed=0x5EED5EED)
+    _check_nv2d(x, TILED)
+
+
+def test_nvfp4_quantize_2d_columnwise_only():
+    x = synth.bf16_normal(192, 320, 1.0, seed=53)
+    for seed in (None, 17):
+        _, _, rct, rst, rt = oracle.nvfp4_quantize_2d(x, seed=seed)
+        for layout in (PLAIN, TILED):
+            codes, scales, codes_t, scales_t, ts = gpu_quantize_nv2d(x, layout, columnwise_only=True,
+                                                                    seed=seed)
+            assert codes is None and scales is None and ts == rt
+            assert np.array_equal(codes_t, rct)
+            assert np.array_equal(scales_t, rst.ravel() if layout == PLAIN else oracle.scale_tile(rst))
