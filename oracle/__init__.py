@@ -99,6 +99,11 @@ def _load():
                                                  ctypes.c_int, ctypes.c_uint32, c_u8p, c_u8p,
                                                  ctypes.POINTER(ctypes.c_float)]
         lib.oracle_nvfp4_quantize_sr.restype = None
+        lib.oracle_gelu.argtypes = [ctypes.c_double]
+        lib.oracle_gelu.restype = ctypes.c_double
+        lib.oracle_gemm_epilogue.argtypes = [c_f64p, c_i64, c_i64, ctypes.POINTER(ctypes.c_float),
+                                             ctypes.c_int, ctypes.c_double, c_f64p, c_f64p]
+        lib.oracle_gemm_epilogue.restype = None
         lib.oracle_block_gemm.argtypes = [ctypes.c_int, c_u8p, c_u8p, c_u8p, c_u8p,
                                           c_i64, c_i64, c_i64, ctypes.c_float, ctypes.c_float,
                                           c_i64p, c_i64, c_i64p, c_i64, c_f64p, c_f64p]
@@ -310,6 +315,29 @@ def nvfp4_gemm(a_codes, a_scales, b_codes, b_scales, m, n, k, a_tensor_scale,
 
 
 # ----------------------------------------------------------------- scale order
+
+def gelu(y: float) -> float:
+    """GELU(y) = y * Phi(y) (erf form), binary64."""
+    return float(_load().oracle_gelu(float(y)))
+
+
+def gemm_epilogue(d, bias=None, gelu_on: bool = False, beta: float = 0.0, c=None) -> np.ndarray:
+    """act(d + beta * c + bias[None, :]) in binary64 (act = GELU or identity).
+
+    d: the GEMM result alpha * A * B^T, [m, n] (binary64); bias: FP32 [n] or
+    None; c: the prior contents of D as values, [m, n], or None (no beta term).
+    """
+    d = np.ascontiguousarray(d, dtype=np.float64)
+    m, n = d.shape
+    out = np.empty_like(d)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    cc = None if c is None else np.ascontiguousarray(c, dtype=np.float64)
+    _load().oracle_gemm_epilogue(_ptr(d, ctypes.c_double), m, n,
+                                 None if b is None else _ptr(b, ctypes.c_float), int(bool(gelu_on)),
+                                 float(beta), None if cc is None else _ptr(cc, ctypes.c_double),
+                                 _ptr(out, ctypes.c_double))
+    return out
+
 
 def scale_tile(plain: np.ndarray) -> np.ndarray:
     """Plain scales [rows, kb] -> the 128x4 tiled order (flat uint8 array)."""

@@ -412,6 +412,41 @@ void oracle_nvfp4_quantize_sr(const uint16_t *x, int64_t rows, int64_t cols, int
 }
 
 /* ------------------------------------------------------------------ */
+/* GEMM epilogue: bias, GELU, beta                                      */
+/* ------------------------------------------------------------------ */
+
+/* GELU(y) = y * Phi(y), the Gaussian error linear unit in its defining form
+ * (Phi the standard normal CDF), evaluated as Phi(y) = erfc(-y / sqrt(2)) / 2,
+ * which equals (1 + erf(y / sqrt(2))) / 2 without its cancellation for
+ * negative y. */
+double oracle_gelu(double y)
+{
+    return 0.5 * y * erfc(-y / sqrt(2.0));
+}
+
+/* out[i, j] = act(d[i, j] + beta * c[i, j] + bias[j]) in binary64, where
+ * act is GELU when gelu != 0 and the identity otherwise; bias (length n)
+ * and c ([m, n]) may be NULL (no term).  "Integrate MXFP4 hipblaslt GEMM
+ * support" (ROCm/TransformerEngine #697) names bias, GELU and beta != 0 as
+ * what the block-scaled GEMM leaves out, and the AITER a4w4 bias as FP32;
+ * the order (scale, then the C and bias terms, then the activation) is the
+ * usual GEMM epilogue D = act(alpha A B^T + beta C + bias). */
+void oracle_gemm_epilogue(const double *d, int64_t m, int64_t n, const float *bias, int gelu,
+                          double beta, const double *c, double *out)
+{
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double y = d[i * n + j];
+            if (c)
+                y += beta * c[i * n + j];
+            if (bias)
+                y += (double)bias[j];
+            out[i * n + j] = gelu ? oracle_gelu(y) : y;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* GEMM                                                                */
 /* ------------------------------------------------------------------ */
 
