@@ -14,4 +14,5 @@ from ._binding import (  # noqa: F401
     mx_scale_bytes, mx_scale_relayout, mx_selftest_wait_timeout, mxfp4_gemm, nvfp4_gemm,
     mxfp4_gemm_static_workspace, MX_STATIC_WORKSPACE_BYTES, MX_QUANTIZE_GROUP_MAX,
     mx_quantize_tensor, mx_quantize_bf16_group, mx_quantize_group_workspace_bytes,
-    mx_quantize_bf16_2d, nvfp4_quantize_bf16_sr, MX_PHILOX_MAX_ROUNDS, nvfp4_quantize_bf16_2d)
+    mx_quantize_bf16_2d, nvfp4_quantize_bf16_sr, MX_PHILOX_MAX_ROUNDS, nvfp4_quantize_bf16_2d,
+    mx_gemm_epilogue, mxfp4_gemm_ex, nvfp4_gemm_ex)

@@ -48,6 +48,11 @@ class mx_quantize_tensor(ctypes.Structure):
                 ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
 
 
+class mx_gemm_epilogue(ctypes.Structure):
+    """include/mxfp4.h: optional GEMM epilogue (bias FP32 [n], beta * D_in, GELU)."""
+    _fields_ = [("bias", ctypes.c_void_p), ("beta", ctypes.c_float), ("gelu", ctypes.c_int)]
+
+
 class MXError(RuntimeError):
     def __init__(self, fn: str, code: int):
         self.code = code
@@ -89,6 +94,12 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_uint64, i32, vp, sz, vp]
         L.mx_quantize_bf16_2d.restype = i32
         L.mx_quantize_bf16_2d.argtypes = [vp, i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
+        ep = ctypes.POINTER(mx_gemm_epilogue)
+        L.mxfp4_gemm_ex.restype = i32
+        L.mxfp4_gemm_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, ep, vp, sz, vp]
+        L.nvfp4_gemm_ex.restype = i32
+        L.nvfp4_gemm_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, ep, vp,
+                                    sz, vp]
         L.mx_scale_relayout.restype = i32
         L.mx_scale_relayout.argtypes = [vp, i64, i64, i32, vp, vp]
         L.mx_gemm_workspace_bytes.restype = sz
@@ -237,6 +248,36 @@ def nvfp4_gemm(a_codes, a_scales, b_codes, b_scales, a_tensor_scale, b_tensor_sc
         _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(a_tensor_scale),
         _ptr(b_tensor_scale), _ptr(d), m, n, k, layout, out_dtype, split_k, _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+def _epilogue(bias, beta, gelu):
+    if bias is None and not beta and not gelu:
+        return None
+    return ctypes.byref(mx_gemm_epilogue(_ptr(bias), float(beta), int(bool(gelu))))
+
+
+def mxfp4_gemm_ex(a_codes, a_scales, b_codes, b_scales, d, m, n, k, layout=MX_LAYOUT_TN,
+                  out_dtype=MX_OUT_BF16, split_k=0, bias=None, beta=0.0, gelu=False,
+                  workspace=None, workspace_bytes=None, stream=None):
+    """mxfp4_gemm with the epilogue D = act(A B^T + beta * D_in + bias)."""
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("mxfp4_gemm_ex", lib().mxfp4_gemm_ex(
+        _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(d), m, n, k, layout,
+        out_dtype, split_k, _epilogue(bias, beta, gelu), _ptr(workspace), workspace_bytes,
+        _stream(stream)))
+
+
+def nvfp4_gemm_ex(a_codes, a_scales, b_codes, b_scales, a_tensor_scale, b_tensor_scale, d, m, n,
+                  k, layout=MX_LAYOUT_TN, out_dtype=MX_OUT_FP32, split_k=0, bias=None, beta=0.0,
+                  gelu=False, workspace=None, workspace_bytes=None, stream=None):
+    """nvfp4_gemm with the epilogue D = act(alpha A B^T + beta * D_in + bias)."""
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace) if not isinstance(workspace, int) else 0
+    return _check("nvfp4_gemm_ex", lib().nvfp4_gemm_ex(
+        _ptr(a_codes), _ptr(a_scales), _ptr(b_codes), _ptr(b_scales), _ptr(a_tensor_scale),
+        _ptr(b_tensor_scale), _ptr(d), m, n, k, layout, out_dtype, split_k,
+        _epilogue(bias, beta, gelu), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def mxfp4_gemm_static_workspace(a_codes, a_scales, b_codes, b_scales, d, m, n, k,

@@ -159,11 +159,22 @@ int num_sms_or_default() {
   return 152;
 }
 
+// Byte range [lo, hi) of a buffer, for the checks that inputs and outputs
+// written concurrently do not overlap.
+struct Range {
+  uintptr_t lo, hi;
+};
+
+bool overlap(const Range &p, const Range &q) { return p.lo < q.hi && q.lo < p.hi; }
+
 int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *b_codes,
                 const void *b_scales, const float *a_ts, const float *b_ts, void *d, int64_t m,
-                int64_t n, int64_t k, int layout, int out_dtype, int split_k, void *workspace,
-                size_t workspace_bytes, void *stream) {
+                int64_t n, int64_t k, int layout, int out_dtype, int split_k,
+                const mx_gemm_epilogue *epi, void *workspace, size_t workspace_bytes,
+                void *stream) {
   if (!a_codes || !a_scales || !b_codes || !b_scales || !d) return MX_ERR_INVALID_ARG;
+  if (epi && epi->gelu != 0 && epi->gelu != 1) return MX_ERR_INVALID_ARG;
+  if (epi && epi->bias && !aligned16(epi->bias)) return MX_ERR_ALIGNMENT;
   if (fmt == MX_FMT_NVFP4 && (!a_ts || !b_ts)) return MX_ERR_INVALID_ARG;
   if (split_k < 0) return MX_ERR_INVALID_ARG;
   if (layout != MX_LAYOUT_TN) return MX_ERR_UNSUPPORTED_FEATURE;
@@ -178,6 +189,15 @@ int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *
   if (fmt == MX_FMT_NVFP4 &&
       ((reinterpret_cast<uintptr_t>(a_ts) & 3u) || (reinterpret_cast<uintptr_t>(b_ts) & 3u)))
     return MX_ERR_ALIGNMENT;
+  const size_t d_bytes = static_cast<size_t>(m) * static_cast<size_t>(n) *
+                         (out_dtype == MX_OUT_FP32 ? 4u : 2u);
+  const Range d_range{reinterpret_cast<uintptr_t>(d), reinterpret_cast<uintptr_t>(d) + d_bytes};
+  if (epi && epi->bias) {
+    // the bias is read while D is written
+    const uintptr_t b = reinterpret_cast<uintptr_t>(epi->bias);
+    if (overlap(Range{b, b + static_cast<uintptr_t>(n) * sizeof(float)}, d_range))
+      return MX_ERR_INVALID_ARG;
+  }
   DeviceInfo *dev = nullptr;
   const int rc = device_info(&dev);
   if (rc != MX_OK) return rc;
@@ -188,6 +208,8 @@ int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *
                         static_cast<size_t>(n) * sizeof(float);
     if (!workspace || workspace_bytes < need) return MX_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+    const uintptr_t w = reinterpret_cast<uintptr_t>(workspace);
+    if (overlap(Range{w, w + need}, d_range)) return MX_ERR_INVALID_ARG;
   }
   CUtensorMap tma, tmb, tmd, tmsa, tmsb;
   // the single-CTA kernel (M <= 128) loads the M rows of A, the pair kernel 128 per CTA
@@ -231,6 +253,12 @@ int gemm_common(int fmt, const void *a_codes, const void *a_scales, const void *
   g.workspace = static_cast<float *>(workspace);
   g.status = dev->status;
   g.num_sms = dev->num_sms;
+  if (epi) {
+    g.epi.bias = epi->bias;
+    g.epi.gelu = epi->gelu;
+    g.epi.beta = epi->beta;
+    g.epi.c = epi->beta != 0.0f ? d : nullptr;  // beta == 0: D stays write-only
+  }
   return launch_rc(mx::launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
@@ -310,12 +338,6 @@ int quantize_tensor_args(const void *x, int64_t rows, int64_t cols, int64_t ld_x
   return MX_OK;
 }
 
-// Byte range [lo, hi) of a buffer, for the overlap check of grouped calls.
-struct Range {
-  uintptr_t lo, hi;
-};
-
-bool overlap(const Range &p, const Range &q) { return p.lo < q.hi && q.lo < p.hi; }
 
 }  // namespace
 
@@ -543,7 +565,7 @@ MX_API int mxfp4_gemm(const void *a_codes, const void *a_scales, const void *b_c
                       int out_dtype, int split_k, void *workspace, size_t workspace_bytes,
                       void *stream) {
   return gemm_common(MX_FMT_MXFP4, a_codes, a_scales, b_codes, b_scales, nullptr, nullptr, d, m, n,
-                     k, layout, out_dtype, split_k, workspace, workspace_bytes, stream);
+                     k, layout, out_dtype, split_k, nullptr, workspace, workspace_bytes, stream);
 }
 
 MX_API int nvfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
@@ -552,7 +574,27 @@ MX_API int nvfp4_gemm(const void *a_codes, const void *a_scales, const void *b_c
                       int layout, int out_dtype, int split_k, void *workspace,
                       size_t workspace_bytes, void *stream) {
   return gemm_common(MX_FMT_NVFP4, a_codes, a_scales, b_codes, b_scales, a_tensor_scale,
-                     b_tensor_scale, d, m, n, k, layout, out_dtype, split_k, workspace,
+                     b_tensor_scale, d, m, n, k, layout, out_dtype, split_k, nullptr, workspace,
+                     workspace_bytes, stream);
+}
+
+MX_API int mxfp4_gemm_ex(const void *a_codes, const void *a_scales, const void *b_codes,
+                         const void *b_scales, void *d, int64_t m, int64_t n, int64_t k,
+                         int layout, int out_dtype, int split_k,
+                         const mx_gemm_epilogue *epilogue, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  return gemm_common(MX_FMT_MXFP4, a_codes, a_scales, b_codes, b_scales, nullptr, nullptr, d, m, n,
+                     k, layout, out_dtype, split_k, epilogue, workspace, workspace_bytes, stream);
+}
+
+MX_API int nvfp4_gemm_ex(const void *a_codes, const void *a_scales, const void *b_codes,
+                         const void *b_scales, const float *a_tensor_scale,
+                         const float *b_tensor_scale, void *d, int64_t m, int64_t n, int64_t k,
+                         int layout, int out_dtype, int split_k,
+                         const mx_gemm_epilogue *epilogue, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  return gemm_common(MX_FMT_NVFP4, a_codes, a_scales, b_codes, b_scales, a_tensor_scale,
+                     b_tensor_scale, d, m, n, k, layout, out_dtype, split_k, epilogue, workspace,
                      workspace_bytes, stream);
 }
 

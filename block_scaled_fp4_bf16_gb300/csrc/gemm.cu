@@ -96,6 +96,8 @@ struct Params {
   FastDiv div_tiles;           // by m_tiles * n_tiles
   FastDiv div_group;           // by 8 * n_tiles
   FastDiv div_last;            // by m_tiles % 8
+  EpiParams epi;               // bias / beta / GELU terms (used when epi_on)
+  int epi_on;                  // 1: apply them (never with partials)
 };
 
 // Unit -> (m tile, n tile, split); tiles are walked in groups of 8 M tiles
@@ -357,6 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kChunk; ++j) f[j] = __fmul_rn(f[j], alpha);
         }
+        if (p.epi_on) {
+          constexpr int kG = OUT_F32 ? 4 : 8;
+#pragma unroll
+          for (int g = 0; g < kChunk / kG; ++g)
+            epilogue_terms<kG, OUT_F32>(&f[g * kG], p.epi,
+                                        static_cast<int64_t>(row0 + lane) * p.n + col0 + g * kG,
+                                        col0 + g * kG);
+        }
         uint8_t *stage_buf;
         if (last) {
           stage_buf = smem + ((warp - 2) * kChunks + c) * kStagingBytes;
@@ -425,35 +435,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Split-K reduction: out[m, n] = alpha * sum_{s = 0..S-1} ws[s, m, n], summed
-// in split order (deterministic), then rounded once to BF16 or FP32.
+// in split order (deterministic), then the epilogue terms (bias, beta * C,
+// GELU) when epi_on, then rounded once to BF16 or FP32.  Eight consecutive
+// outputs per thread and step (M, N % 32 == 0).
+template <int OUT_F32>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws,
-                                                            int splits, int64_t mn, void *out,
-                                                            int out_fp32, const float *a_ts,
-                                                            const float *b_ts) {
+                                                            int splits, int64_t mn, int n,
+                                                            void *out, const float *a_ts,
+                                                            const float *b_ts, EpiParams epi,
+                                                            int epi_on) {
   griddep_launch_dependents();
   griddep_wait();
   float alpha = 1.0f;
   if (a_ts != nullptr) alpha = __fmul_rn(*a_ts, *b_ts);
-  const int64_t n4 = mn >> 2;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+  const int64_t n8 = mn >> 3;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 acc = reinterpret_cast<const float4 *>(ws)[i];
+    const float4 *p0 = reinterpret_cast<const float4 *>(ws) + 2 * i;
+    float4 lo = p0[0], hi = p0[1];
     for (int s = 1; s < splits; ++s) {
-      const float4 v = reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(s) * mn)[i];
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      const float4 *ps = reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(s) * mn) + 2 * i;
+      const float4 a = ps[0], b = ps[1];
+      lo.x += a.x;
+      lo.y += a.y;
+      lo.z += a.z;
+      lo.w += a.w;
+      hi.x += b.x;
+      hi.y += b.y;
+      hi.z += b.z;
+      hi.w += b.w;
     }
-    acc.x = __fmul_rn(acc.x, alpha);
-    acc.y = __fmul_rn(acc.y, alpha);
-    acc.z = __fmul_rn(acc.z, alpha);
-    acc.w = __fmul_rn(acc.w, alpha);
-    if (out_fp32) {
-      reinterpret_cast<float4 *>(out)[i] = acc;
+    float f[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], alpha);
+    if (epi_on) epilogue_terms<8, OUT_F32>(f, epi, 8 * i, static_cast<int>((8 * i) % n));
+    if constexpr (OUT_F32) {
+      float4 *o = reinterpret_cast<float4 *>(out) + 2 * i;
+      o[0] = make_float4(f[0], f[1], f[2], f[3]);
+      o[1] = make_float4(f[4], f[5], f[6], f[7]);
     } else {
-      reinterpret_cast<uint2 *>(out)[i] =
-          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      reinterpret_cast<uint4 *>(out)[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
     }
   }
 }
@@ -507,6 +529,8 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.div_group = make_fastdiv(static_cast<uint32_t>(8 * p.n_tiles));
   p.div_last = make_fastdiv(static_cast<uint32_t>(p.m_tiles % 8));
   p.a_rows = static_cast<int>(g.m);  // the A map's box is M rows (M <= 128 here)
+  p.epi = g.epi;
+  p.epi_on = (g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu)) ? 1 : 0;
   const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
   e = launch_pdl(gemm_kernel<FMT, BN, OUT_F32>, dim3(grid), dim3(kThreads), C::kSmemBytes, s,
                  *g.tmap_a, *g.tmap_b, *g.tmap_d, p);
@@ -561,13 +585,15 @@ int gemm_out_box_cols(int out_fp32, int split_k) { return (out_fp32 || split_k >
 
 cudaError_t launch_splitk_reduce(const GemmArgs &g, cudaStream_t s) {
   const int64_t mn = g.m * g.n;
-  int64_t rgrid = (mn / 4 + 255) / 256;
+  int64_t rgrid = (mn / 8 + 255) / 256;
   if (rgrid > 4 * g.num_sms) rgrid = 4 * g.num_sms;
+  const int epi_on = (g.epi.bias || g.epi.c || g.epi.gelu) ? 1 : 0;
+  const float *ats = g.fmt == 1 ? g.a_ts : static_cast<const float *>(nullptr);
+  const float *bts = g.fmt == 1 ? g.b_ts : static_cast<const float *>(nullptr);
   const cudaError_t e = launch_pdl(
-      splitk_reduce_kernel, dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s,
-      static_cast<const float *>(g.workspace), g.split_k, mn, g.d, g.out_fp32,
-      g.fmt == 1 ? g.a_ts : static_cast<const float *>(nullptr),
-      g.fmt == 1 ? g.b_ts : static_cast<const float *>(nullptr));
+      g.out_fp32 ? splitk_reduce_kernel<1> : splitk_reduce_kernel<0>,
+      dim3(static_cast<unsigned>(rgrid)), dim3(256), 0, s, static_cast<const float *>(g.workspace),
+      g.split_k, mn, static_cast<int>(g.n), g.d, ats, bts, g.epi, epi_on);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

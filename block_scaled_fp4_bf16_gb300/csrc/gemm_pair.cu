@@ -81,6 +81,8 @@ struct PairParams {
   FastDiv div_tiles;           // by pm_tiles * n_tiles
   FastDiv div_group;           // by 16 * n_tiles (the units of a group of 16 M tiles)
   FastDiv div_last;            // by pm_tiles % 16 (the size of a last, partial group)
+  EpiParams epi;               // bias / beta / GELU terms (used when epi_on)
+  int epi_on;                  // 1: apply them (never with partials)
 };
 
 // Unit -> (256-row tile of M, 256-column tile of N, split), in groups of 16
@@ -355,6 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[j] = __uint_as_float(r[c * 16 + 4 * i + j]);
               if (FMT == 1 && !p.partial) f[j] = __fmul_rn(f[j], alpha);
             }
+            if (p.epi_on)
+              epilogue_terms<4, 1>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 4 * i,
+                                   col0 + 4 * i);
             v[i] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                               __float_as_uint(f[3]));
           }
@@ -367,6 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[j] = __uint_as_float(r[c * 32 + 8 * i + j]);
               if (FMT == 1 && !p.partial) f[j] = __fmul_rn(f[j], alpha);
             }
+            if (p.epi_on)
+              epilogue_terms<8, 0>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 8 * i,
+                                   col0 + 8 * i);
             v[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
           }
@@ -448,6 +456,8 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.div_tiles = make_fastdiv(static_cast<uint32_t>(p.pm_tiles * p.n_tiles));
   p.div_group = make_fastdiv(static_cast<uint32_t>(16 * p.n_tiles));
   p.div_last = make_fastdiv(static_cast<uint32_t>(p.pm_tiles % 16));
+  p.epi = g.epi;
+  p.epi_on = (g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu)) ? 1 : 0;
   const int clusters = p.num_units < max_clusters[dev] ? p.num_units : max_clusters[dev];
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.numAttrs = 2;  // cluster shape + programmatic stream serialization

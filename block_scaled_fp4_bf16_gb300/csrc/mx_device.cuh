@@ -432,6 +432,56 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   return out;
 }
 
+// GEMM epilogue of N consecutive outputs of one row (N = 4 or 8; idx = the
+// flat index row * n + col of the first, col its column): f = act(f +
+// beta * C + bias), each term only when present (C in the output dtype:
+// FP32 when OUT_F32, else BF16), act = GELU(y) = y * Phi(y) when e.gelu.
+// Every step is one binary32 operation; Phi is CUDA's normcdff.
+template <int N, int OUT_F32>
+__device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int64_t idx, int col) {
+  static_assert(N == 4 || N == 8, "groups of 4 or 8 outputs");
+  if (e.c != nullptr) {
+    float cv[N];
+    if constexpr (OUT_F32) {
+      const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(e.c) + idx);
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) {
+        const float4 v = src[i];
+        cv[4 * i] = v.x;
+        cv[4 * i + 1] = v.y;
+        cv[4 * i + 2] = v.z;
+        cv[4 * i + 3] = v.w;
+      }
+    } else {
+      static_assert(OUT_F32 || N == 8, "BF16 outputs in groups of 8");
+      const uint4 v = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(e.c) + idx);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        cv[2 * j] = __uint_as_float(w[j] << 16);
+        cv[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) f[j] = __fmaf_rn(e.beta, cv[j], f[j]);
+  }
+  if (e.bias != nullptr) {
+    const float4 *b = reinterpret_cast<const float4 *>(e.bias + col);
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float4 v = __ldg(b + i);
+      f[4 * i] = __fadd_rn(f[4 * i], v.x);
+      f[4 * i + 1] = __fadd_rn(f[4 * i + 1], v.y);
+      f[4 * i + 2] = __fadd_rn(f[4 * i + 2], v.z);
+      f[4 * i + 3] = __fadd_rn(f[4 * i + 3], v.w);
+    }
+  }
+  if (e.gelu) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) f[j] = __fmul_rn(f[j], normcdff(f[j]));
+  }
+}
+
 // binary32 -> E4M3 byte (round to nearest even, saturating at 448).
 __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   uint16_t out;

@@ -84,6 +84,16 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
                                   cudaStream_t s);
 
+// Optional GEMM epilogue: D = act(alpha * acc + beta * C + bias), act = GELU
+// (y * Phi(y)) or the identity.  c: the prior contents of D (same dtype and
+// layout), null when beta == 0; bias: FP32 [N] (16-byte aligned) or null.
+struct EpiParams {
+  const float *bias;
+  const void *c;
+  float beta;
+  int gelu;
+};
+
 struct GemmArgs {
   int fmt;  // 0 MXFP4, 1 NVFP4
   const CUtensorMap *tmap_a;  // codes A [M, K/2] bytes, box 128 rows
@@ -97,6 +107,7 @@ struct GemmArgs {
   int out_fp32;
   int64_t m, n, k;
   int split_k;   // >= 1, already resolved
+  EpiParams epi; // all null / 0: plain epilogue
   int bn;        // single-CTA kernel: 128 or 256
   int pair;      // 1: CTA-pair kernel with 256 x 256 tiles
   float *workspace;

@@ -292,6 +292,39 @@ int nvfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
                void *d, int64_t m, int64_t n, int64_t k, int layout, int out_dtype, int split_k,
                void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- GEMM epilogue: bias, GELU, beta ------------------------------------
+ * "Integrate MXFP4 hipblaslt GEMM support" (ROCm/TransformerEngine #697)
+ * names what that block-scaled GEMM leaves out: bias, GELU and beta != 0
+ * (and gives the AITER a4w4 bias as FP32).  The _ex entry points below add
+ * them to mxfp4_gemm / nvfp4_gemm as one optional epilogue:
+ *   D[i, j] = act(alpha * sum_k A[i, k] B[j, k] + beta * D_in[i, j] + bias[j])
+ * with act = GELU(y) = y * Phi(y) (Phi the standard normal CDF, the erf form
+ * of GELU) when gelu == 1, the identity when gelu == 0; alpha = 1 for MXFP4
+ * and s_tA * s_tB for NVFP4.  Each term is one binary32 operation on the
+ * FP32 accumulator, in the order written (beta * D_in by one FMA); the
+ * result is then rounded once to the output type.  D_in is the content of D
+ * before the call, in the output type; with beta == 0 it is not read (D is
+ * write-only, as without an epilogue). */
+typedef struct mx_gemm_epilogue {
+  const float *bias; /* device FP32 [n], 16-byte aligned, or NULL; must not overlap D */
+  float beta;        /* scale of D_in; 0: D is not read                             */
+  int gelu;          /* 0 or 1                                                      */
+} mx_gemm_epilogue;
+
+/* mxfp4_gemm / nvfp4_gemm with an epilogue (NULL: exactly those calls).
+ * Additional errors: gelu not 0/1 or a bias overlapping D
+ * (MX_ERR_INVALID_ARG), a bias not 16-byte aligned (MX_ERR_ALIGNMENT).  With
+ * split-K the terms are applied by the reduction kernel. */
+int mxfp4_gemm_ex(const void *a_codes, const void *a_scales, const void *b_codes,
+                  const void *b_scales, void *d, int64_t m, int64_t n, int64_t k, int layout,
+                  int out_dtype, int split_k, const mx_gemm_epilogue *epilogue, void *workspace,
+                  size_t workspace_bytes, void *stream);
+int nvfp4_gemm_ex(const void *a_codes, const void *a_scales, const void *b_codes,
+                  const void *b_scales, const float *a_tensor_scale, const float *b_tensor_scale,
+                  void *d, int64_t m, int64_t n, int64_t k, int layout, int out_dtype, int split_k,
+                  const mx_gemm_epilogue *epilogue, void *workspace, size_t workspace_bytes,
+                  void *stream);
+
 /* Size of the fixed device scratch array of mxfp4_gemm_static_workspace. */
 #define MX_STATIC_WORKSPACE_BYTES (16u << 20) /* 16 MiB */
 

@@ -98,6 +98,23 @@ def test_gemm_argument_validation(lib):
                           None, 0, None) == mx.MX_ERR_INVALID_ARG
 
 
+def test_gemm_epilogue_argument_validation(lib):
+    MB = 1 << 20
+
+    def call(gelu=0, bias=None, beta=0.0, d=FAKE + 4 * MB, m=128, n=128):
+        ep = mx.mx_gemm_epilogue(bias, beta, gelu)
+        return lib.mxfp4_gemm_ex(FAKE, FAKE + MB, FAKE + 2 * MB, FAKE + 3 * MB, d, m, n, 256, 0, 0, 1,
+                                 ctypes.byref(ep), None, 0, None)
+    assert call(gelu=2) == mx.MX_ERR_INVALID_ARG
+    assert call(gelu=-1) == mx.MX_ERR_INVALID_ARG
+    assert call(bias=FAKE + 8 * MB + 4) == mx.MX_ERR_ALIGNMENT       # bias not 16-byte aligned
+    assert call(bias=FAKE + 4 * MB + 256) == mx.MX_ERR_INVALID_ARG   # bias inside D
+    # the NVFP4 form still needs its tensor scales
+    ep = mx.mx_gemm_epilogue(None, 0.0, 1)
+    assert lib.nvfp4_gemm_ex(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 128, 128, 256, 0, 1, 1,
+                             ctypes.byref(ep), None, 0, None) == mx.MX_ERR_INVALID_ARG
+
+
 def test_quantize_argument_validation(lib):
     q = lib.mx_quantize_bf16
     assert q(None, 4, 32, 32, 0, 0, FAKE, FAKE, None, None, 0, None) == mx.MX_ERR_INVALID_ARG
