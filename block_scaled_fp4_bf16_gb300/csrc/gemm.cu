@@ -96,8 +96,7 @@ struct Params {
   FastDiv div_tiles;           // by m_tiles * n_tiles
   FastDiv div_group;           // by 8 * n_tiles
   FastDiv div_last;            // by m_tiles % 8
-  EpiParams epi;               // bias / beta / GELU terms (used when epi_on)
-  int epi_on;                  // 1: apply them (never with partials)
+  EpiParams epi;               // bias / beta / GELU terms (kernels instantiated with EPI)
 };
 
 // Unit -> (m tile, n tile, split); tiles are walked in groups of 8 M tiles
@@ -126,8 +125,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // OUT_F32: 1 -> FP32 boxes of 32 rows x 16 columns, 0 -> BF16 boxes of 32 x 32;
-// either way 64 bytes per row, stored with the 64-byte swizzle.
-template <int FMT, int BN, int OUT_F32>
+// either way 64 bytes per row, stored with the 64-byte swizzle.  EPI: 1
+// applies the epilogue terms of p.epi (never with split-K partials).
+template <int FMT, int BN, int OUT_F32, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b,
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kChunk; ++j) f[j] = __fmul_rn(f[j], alpha);
         }
-        if (p.epi_on) {
+        if constexpr (EPI != 0) {
           constexpr int kG = OUT_F32 ? 4 : 8;
 #pragma unroll
           for (int g = 0; g < kChunk / kG; ++g)
@@ -494,7 +494,7 @@ __global__ void wait_selftest_kernel(uint32_t *status, uint64_t timeout_ns) {
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0u, &abort_flag, status, timeout_ns);
 }
 
-template <int FMT, int BN, int OUT_F32>
+template <int FMT, int BN, int OUT_F32, int EPI>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   using C = Cfg<FMT, BN>;
   static bool attr_set[64] = {};
@@ -502,7 +502,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, OUT_F32>,
+    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, OUT_F32, EPI>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -530,9 +530,8 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.div_last = make_fastdiv(static_cast<uint32_t>(p.m_tiles % 8));
   p.a_rows = static_cast<int>(g.m);  // the A map's box is M rows (M <= 128 here)
   p.epi = g.epi;
-  p.epi_on = (g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu)) ? 1 : 0;
   const int grid = p.num_units < g.num_sms ? p.num_units : g.num_sms;
-  e = launch_pdl(gemm_kernel<FMT, BN, OUT_F32>, dim3(grid), dim3(kThreads), C::kSmemBytes, s,
+  e = launch_pdl(gemm_kernel<FMT, BN, OUT_F32, EPI>, dim3(grid), dim3(kThreads), C::kSmemBytes, s,
                  *g.tmap_a, *g.tmap_b, *g.tmap_d, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || g.split_k <= 1) return e;
@@ -542,8 +541,11 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 template <int FMT, int BN>
 cudaError_t launch_bn(const GemmArgs &g, cudaStream_t s) {
   // split-K partials are FP32 whatever the final output type
-  return (g.out_fp32 || g.split_k > 1) ? launch_typed<FMT, BN, 1>(g, s)
-                                       : launch_typed<FMT, BN, 0>(g, s);
+  // with split-K the reduction applies the epilogue terms
+  if (g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu))
+    return g.out_fp32 ? launch_typed<FMT, BN, 1, 1>(g, s) : launch_typed<FMT, BN, 0, 1>(g, s);
+  return (g.out_fp32 || g.split_k > 1) ? launch_typed<FMT, BN, 1, 0>(g, s)
+                                       : launch_typed<FMT, BN, 0, 0>(g, s);
 }
 
 }  // namespace

@@ -81,8 +81,7 @@ struct PairParams {
   FastDiv div_tiles;           // by pm_tiles * n_tiles
   FastDiv div_group;           // by 16 * n_tiles (the units of a group of 16 M tiles)
   FastDiv div_last;            // by pm_tiles % 16 (the size of a last, partial group)
-  EpiParams epi;               // bias / beta / GELU terms (used when epi_on)
-  int epi_on;                  // 1: apply them (never with partials)
+  EpiParams epi;               // bias / beta / GELU terms (kernels instantiated with EPI)
 };
 
 // Unit -> (256-row tile of M, 256-column tile of N, split), in groups of 16
@@ -113,7 +112,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-template <int FMT, int OUT_F32>
+// EPI: 1 applies the epilogue terms of p.epi (never with split-K partials);
+// 0 compiles the plain epilogue.
+template <int FMT, int OUT_F32, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[j] = __uint_as_float(r[c * 16 + 4 * i + j]);
               if (FMT == 1 && !p.partial) f[j] = __fmul_rn(f[j], alpha);
             }
-            if (p.epi_on)
+            if constexpr (EPI != 0)
               epilogue_terms<4, 1>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 4 * i,
                                    col0 + 4 * i);
             v[i] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[j] = __uint_as_float(r[c * 32 + 8 * i + j]);
               if (FMT == 1 && !p.partial) f[j] = __fmul_rn(f[j], alpha);
             }
-            if (p.epi_on)
+            if constexpr (EPI != 0)
               epilogue_terms<8, 0>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 8 * i,
                                    col0 + 8 * i);
             v[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
@@ -407,10 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int FMT, int OUT_F32>
+template <int FMT, int OUT_F32, int EPI>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   using C = PairCfg<FMT>;
-  auto kernel = gemm_pair_kernel<FMT, OUT_F32>;
+  auto kernel = gemm_pair_kernel<FMT, OUT_F32, EPI>;
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -457,7 +458,6 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.div_group = make_fastdiv(static_cast<uint32_t>(16 * p.n_tiles));
   p.div_last = make_fastdiv(static_cast<uint32_t>(p.pm_tiles % 16));
   p.epi = g.epi;
-  p.epi_on = (g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu)) ? 1 : 0;
   const int clusters = p.num_units < max_clusters[dev] ? p.num_units : max_clusters[dev];
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.numAttrs = 2;  // cluster shape + programmatic stream serialization
@@ -471,11 +471,20 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 
 cudaError_t launch_gemm_pair(const GemmArgs &g, cudaStream_t s) {
   const bool f32 = g.out_fp32 || g.split_k > 1;
+  // with split-K the reduction applies the epilogue terms
+  const bool epi = g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu);
   cudaError_t e;
-  if (g.fmt == 0)
-    e = f32 ? launch_typed<0, 1>(g, s) : launch_typed<0, 0>(g, s);
-  else
-    e = f32 ? launch_typed<1, 1>(g, s) : launch_typed<1, 0>(g, s);
+  if (g.fmt == 0) {
+    if (epi)
+      e = f32 ? launch_typed<0, 1, 1>(g, s) : launch_typed<0, 0, 1>(g, s);
+    else
+      e = f32 ? launch_typed<0, 1, 0>(g, s) : launch_typed<0, 0, 0>(g, s);
+  } else {
+    if (epi)
+      e = f32 ? launch_typed<1, 1, 1>(g, s) : launch_typed<1, 0, 1>(g, s);
+    else
+      e = f32 ? launch_typed<1, 1, 0>(g, s) : launch_typed<1, 0, 0>(g, s);
+  }
   if (e != cudaSuccess || g.split_k <= 1) return e;
   return launch_splitk_reduce(g, s);
 }
