@@ -251,6 +251,8 @@ class DeviceWorkload:
                     s["ts_b"] = torch.zeros(1, dtype=torch.float32, device=dev)
                     qws = mx.mx_quantize_group_workspace_bytes(2, self.fmt)
                     s["qws"] = torch.empty(qws, dtype=u8, device=dev)
+                if "bias" in host_inputs:
+                    s["bias"] = torch.from_numpy(host_inputs["bias"]).to(dev)
             else:
                 s["codes_a"] = torch.from_numpy(host_inputs["a_codes"]).to(dev)
                 s["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).to(dev)
@@ -295,8 +297,14 @@ class DeviceWorkload:
                     fmt, mx.MX_SCALE_TCGEN05, s.get("qws"), stream=st)
             out.append(("quantize", q))
 
+        gelu = bool(self.w.get("gelu"))
+
         def gemm(s, st):
-            if fmt == mx.MX_FMT_MXFP4:
+            if fmt == mx.MX_FMT_MXFP4 and (gelu or "bias" in s):
+                mx.mxfp4_gemm_ex(s["codes_a"], s["sf_a"], s["codes_b"], s["sf_b"], s["d"], m, n, k,
+                                 mx.MX_LAYOUT_TN, self.out, self.split_k, s.get("bias"), 0.0, gelu,
+                                 s["ws"], stream=st)
+            elif fmt == mx.MX_FMT_MXFP4:
                 mx.mxfp4_gemm(s["codes_a"], s["sf_a"], s["codes_b"], s["sf_b"], s["d"], m, n, k,
                               mx.MX_LAYOUT_TN, self.out, self.split_k, s["ws"], stream=st)
             else:
@@ -333,6 +341,8 @@ class DeviceWorkload:
         qbytes = lambda r: r * k * (2 + amax_pass + 0.5 + 1.0 / blk)
         out_b = 2 if self.out == self.mx.MX_OUT_BF16 else 4
         gemm_bytes = (m + n) * k * (0.5 + 1.0 / blk) + m * n * out_b
+        if self.w.get("bias"):
+            gemm_bytes += n * 4
         res = {"gemm": (gemm_bytes, 2.0 * m * n * k)}
         if self.kind == "bf16":
             res["quantize"] = (qbytes(m) + qbytes(n), 0.0)
@@ -442,6 +452,8 @@ def time_e2e(wl, host_inputs, steps):
     if wl.kind == "bf16":
         pinned["x_b"] = torch.from_numpy(host_inputs["b"].view(np.int16)).view(
             torch.bfloat16).pin_memory()
+        if "bias" in host_inputs:
+            pinned["bias"] = torch.from_numpy(host_inputs["bias"]).pin_memory()
     elif wl.kind == "codes":
         pinned["codes_a"] = torch.from_numpy(host_inputs["a_codes"]).pin_memory()
         pinned["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).pin_memory()
@@ -501,7 +513,9 @@ def oracle_step_sample(name, host, frac, prepared):
             oracle.mx_quantize(host["a"][:mr])
             oracle.mx_quantize(host["b"][:nr])
             qa, sa, qb, sb = prepared
-            oracle.mx_gemm(qa, sa, qb, sb, m, n, k, rows=np.arange(mr))
+            d = oracle.mx_gemm(qa, sa, qb, sb, m, n, k, rows=np.arange(mr))[0]
+            if w.get("bias") or w.get("gelu"):
+                oracle.gemm_epilogue(d, bias=host.get("bias"), gelu_on=bool(w.get("gelu")))
         else:
             oracle.nvfp4_quantize(host["a"][:mr])
             oracle.nvfp4_quantize(host["b"][:nr])

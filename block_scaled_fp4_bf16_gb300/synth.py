@@ -73,6 +73,10 @@ WORKLOADS = {
     # BF16 activations and weights quantized to MXFP4, BF16 out.
     "quant_gemm_2048x4096x4096": dict(kind="bf16", fmt="mxfp4", m=2048, n=4096, k=4096,
                                       sigma_a=1.0, sigma_b=0.02, out="bf16", split_k=1),
+    # The same step with the GEMM epilogue D = GELU(A W^T + bias), FP32 bias [N].
+    "quant_gemm_bias_gelu_2048x4096x4096": dict(kind="bf16", fmt="mxfp4", m=2048, n=4096, k=4096,
+                                                sigma_a=1.0, sigma_b=0.02, out="bf16", split_k=1,
+                                                bias=True, sigma_bias=1.0, gelu=True),
     # LLM MLP up-projection, compute bound.
     "mlp_up_16384x28672x8192": dict(kind="bf16", fmt="mxfp4", m=16384, n=28672, k=8192,
                                     sigma_a=1.0, sigma_b=0.015, out="bf16", split_k=1),
@@ -106,7 +110,8 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
                     k: int | None = None) -> dict:
     """Host inputs of a workload (optionally at other sizes with the same recipe).
 
-    kind == "bf16": {"a": BF16 bits [m, k], "b": BF16 bits [n, k]}
+    kind == "bf16": {"a": BF16 bits [m, k], "b": BF16 bits [n, k]} (+ "bias": FP32 [n]
+                    for a workload with a bias)
     kind == "codes": {"a_codes", "a_scales", "b_codes", "b_scales"} (plain scales)
     kind == "quant2d" or "quant_sr": {"a": BF16 bits [m, k]}
     """
@@ -116,8 +121,12 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
     k = w["k"] if k is None else k
     seed = workload_seed(name) * 16
     if w["kind"] == "bf16":
-        return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1),
-                "b": bf16_normal(n, k, w["sigma_b"], seed + 2)}
+        out = {"a": bf16_normal(m, k, w["sigma_a"], seed + 1),
+               "b": bf16_normal(n, k, w["sigma_b"], seed + 2)}
+        if w.get("bias"):
+            rng = np.random.Generator(np.random.Philox(seed + 3))
+            out["bias"] = (rng.standard_normal(n, dtype=np.float32) * np.float32(w["sigma_bias"]))
+        return out
     if w["kind"] in ("quant2d", "quant_sr"):
         return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1)}
     kb = k // 32
