@@ -334,6 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kChunks; ++c) {
         float f[kChunk];
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * kChunk;
+        // this chunk's bias, one column per lane, loaded before the tensor
+        // memory load so that the two latencies overlap
+        float bias_l = 0.0f;
+        if constexpr (EPI != 0) {
+          const int bc = nt * BN + c * kChunk + lane;
+          if (p.epi.bias != nullptr && lane < kChunk && bc < p.n) bias_l = __ldg(p.epi.bias + bc);
+        }
         if constexpr (kChunk == 32) {
           uint32_t r[32];
           tc_ld_32x32b_x32(taddr, r);
@@ -362,10 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (EPI != 0) {
           constexpr int kG = OUT_F32 ? 4 : 8;
 #pragma unroll
-          for (int g = 0; g < kChunk / kG; ++g)
+          for (int g = 0; g < kChunk / kG; ++g) {
+            float bv[kG];
+#pragma unroll
+            for (int j = 0; j < kG; ++j) bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l, g * kG + j);
             epilogue_terms<kG, OUT_F32>(&f[g * kG], p.epi,
-                                        static_cast<int64_t>(row0 + lane) * p.n + col0 + g * kG,
-                                        col0 + g * kG);
+                                        static_cast<int64_t>(row0 + lane) * p.n + col0 + g * kG, bv);
+          }
         }
         uint8_t *stage_buf;
         if (last) {
@@ -468,7 +478,16 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
     float f[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], alpha);
-    if (epi_on) epilogue_terms<8, OUT_F32>(f, epi, 8 * i, static_cast<int>((8 * i) % n));
+    if (epi_on) {
+      float bv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      if (epi.bias != nullptr) {
+        const float4 *b = reinterpret_cast<const float4 *>(epi.bias + (8 * i) % n);
+        const float4 b0 = __ldg(b), b1 = __ldg(b + 1);
+        bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+        bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+      }
+      epilogue_terms<8, OUT_F32>(f, epi, 8 * i, bv);
+    }
     if constexpr (OUT_F32) {
       float4 *o = reinterpret_cast<float4 *>(out) + 2 * i;
       o[0] = make_float4(f[0], f[1], f[2], f[3]);

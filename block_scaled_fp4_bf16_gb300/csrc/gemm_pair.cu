@@ -303,6 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = cluster; u < p.num_units; u += nclusters, ++tile) {
       int pm, nt, sp;
       decode_unit(p, u, pm, nt, sp);
+      // the bias of this warp's 128 columns, four per lane (loaded before the
+      // wait, so that its latency is hidden; N % 32 == 0: a lane's four
+      // columns are all in range or all out)
+      float bias_l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (EPI != 0) {
+        const int bc = nt * 256 + h * 128 + 4 * lane;
+        if (p.epi.bias != nullptr && bc < p.n) {
+          const float4 v = __ldg(reinterpret_cast<const float4 *>(p.epi.bias + bc));
+          bias_l[0] = v.x;
+          bias_l[1] = v.y;
+          bias_l[2] = v.z;
+          bias_l[3] = v.w;
+        }
+      }
       const bool ready = mbar_wait(smem_u32(tfull), tile & 1u, abort, p.status);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
@@ -358,9 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[j] = __uint_as_float(r[c * 16 + 4 * i + j]);
               if (FMT == 1 && !p.partial) f[j] = __fmul_rn(f[j], alpha);
             }
-            if constexpr (EPI != 0)
+            if constexpr (EPI != 0) {
+              float bv[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int cc = c * 16 + 4 * i + j;  // column within the warp's 128
+                bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc & 3], cc >> 2);
+              }
               epilogue_terms<4, 1>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 4 * i,
-                                   col0 + 4 * i);
+                                   bv);
+            }
             v[i] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                               __float_as_uint(f[3]));
           }
@@ -373,9 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[j] = __uint_as_float(r[c * 32 + 8 * i + j]);
               if (FMT == 1 && !p.partial) f[j] = __fmul_rn(f[j], alpha);
             }
-            if constexpr (EPI != 0)
+            if constexpr (EPI != 0) {
+              float bv[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int cc = c * 32 + 8 * i + j;  // column within the warp's 128
+                bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc & 3], cc >> 2);
+              }
               epilogue_terms<8, 0>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 8 * i,
-                                   col0 + 8 * i);
+                                   bv);
+            }
             v[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
           }

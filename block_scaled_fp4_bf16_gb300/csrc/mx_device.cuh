@@ -432,13 +432,48 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   return out;
 }
 
+// GELU(y) = y Phi(y), Phi the standard normal CDF.  For a = |y|,
+// Phi(-a) = erfc(z) / 2 with z = a / sqrt 2, and erfc comes from the Chebyshev
+// fit of Numerical Recipes (Press, Teukolsky, Vetterling, Flannery, 2nd ed.,
+// section 6.2, erfcc; fractional error below 1.2e-7 for every z >= 0):
+//   erfc(z) ~ t exp(-z^2 + P(t)),  t = 1 / (1 + z / 2),  P of degree 9.
+// The exponent -z^2 = -a^2 / 2 is taken as -(h + l) / 2 with h = RN(a^2) and
+// l = a^2 - h exact (one FMA), so that only the final FMA of the argument
+// rounds; then GELU(y) = y Phi(-a) for y <= 0 and y - y Phi(-a) for y > 0.
+// Relative error below 2^-24 (y^2 / 2 + 40): the fit, CUDA's expf (2 ulp)
+// and __fdividef (2 ulp), the Horner rounding and the argument's rounding,
+// which grows with its magnitude y^2 / 2.  One MUFU reciprocal and one
+// exponential per value.
+__device__ __forceinline__ float gelu_f32(float y) {
+  const float a = fabsf(y);
+  const float z = __fmul_rn(a, 0.70710678118654752f);
+  const float t = __fdividef(1.0f, __fmaf_rn(0.5f, z, 1.0f));
+  float p = 0.17087277f;
+  p = __fmaf_rn(p, t, -0.82215223f);
+  p = __fmaf_rn(p, t, 1.48851587f);
+  p = __fmaf_rn(p, t, -1.13520398f);
+  p = __fmaf_rn(p, t, 0.27886807f);
+  p = __fmaf_rn(p, t, -0.18628806f);
+  p = __fmaf_rn(p, t, 0.09678418f);
+  p = __fmaf_rn(p, t, 0.37409196f);
+  p = __fmaf_rn(p, t, 1.00002368f);
+  p = __fmaf_rn(p, t, -1.26551223f);
+  const float h = __fmul_rn(a, a);
+  const float l = __fmaf_rn(a, a, -h);
+  const float arg = __fmaf_rn(-0.5f, h, __fmaf_rn(-0.5f, l, p));
+  const float phi = __fmul_rn(__fmul_rn(0.5f, t), expf(arg));  // Phi(-|y|)
+  const float yp = __fmul_rn(y, phi);
+  return y > 0.0f ? __fsub_rn(y, yp) : yp;
+}
+
 // GEMM epilogue of N consecutive outputs of one row (N = 4 or 8; idx = the
-// flat index row * n + col of the first, col its column): f = act(f +
-// beta * C + bias), each term only when present (C in the output dtype:
-// FP32 when OUT_F32, else BF16), act = GELU(y) = y * Phi(y) when e.gelu.
-// Every step is one binary32 operation; Phi is CUDA's normcdff.
+// flat index row * n + col of the first): f = act(f + beta * C + bias), each
+// term only when present (C in the output dtype: FP32 when OUT_F32, else
+// BF16; bv: the N bias values, null when e.bias is null), act = GELU when
+// e.gelu.  Every step but GELU (gelu_f32) is one binary32 operation.
 template <int N, int OUT_F32>
-__device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int64_t idx, int col) {
+__device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int64_t idx,
+                                               const float *bv) {
   static_assert(N == 4 || N == 8, "groups of 4 or 8 outputs");
   if (e.c != nullptr) {
     float cv[N];
@@ -466,19 +501,12 @@ __device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int
     for (int j = 0; j < N; ++j) f[j] = __fmaf_rn(e.beta, cv[j], f[j]);
   }
   if (e.bias != nullptr) {
-    const float4 *b = reinterpret_cast<const float4 *>(e.bias + col);
 #pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-      const float4 v = __ldg(b + i);
-      f[4 * i] = __fadd_rn(f[4 * i], v.x);
-      f[4 * i + 1] = __fadd_rn(f[4 * i + 1], v.y);
-      f[4 * i + 2] = __fadd_rn(f[4 * i + 2], v.z);
-      f[4 * i + 3] = __fadd_rn(f[4 * i + 3], v.w);
-    }
+    for (int j = 0; j < N; ++j) f[j] = __fadd_rn(f[j], bv[j]);
   }
   if (e.gelu) {
 #pragma unroll
-    for (int j = 0; j < N; ++j) f[j] = __fmul_rn(f[j], normcdff(f[j]));
+    for (int j = 0; j < N; ++j) f[j] = gelu_f32(f[j]);
   }
 }
 
