@@ -61,7 +61,8 @@ struct QTensor {
   uint32_t rows, cols;
   uint32_t total;               // scale blocks incl. row padding
   uint32_t real_total;          // rows * kb
-  uint32_t first_cta;
+  uint32_t first_cta;          // first CTA (MXFP4) or chunk (NVFP4 pass 2) of this tensor
+  uint32_t nchunks;            // NVFP4 pass 2: chunks of kThreads * kNvBlocksPerThread blocks
   uint32_t katoms;
   FastDiv kbdiv;                // kb = cols / block
   int tiled;
@@ -490,53 +491,91 @@ __device__ __forceinline__ uint32_t nv_block(const uint32_t *w, const NvConst &c
   return sb;
 }
 
-// NVFP4 pass 2: every CTA reduces its tensor's partial maxima to s_t, then
-// thread b quantizes 16-element block b.  Each binary32 step of the
-// definition is one round-to-nearest operation (correctly rounded divisions
-// where it divides).  The CTAs take the blocks in the reverse of the order in
-// which pass 1 swept them, so the first blocks quantized are the ones pass 1
-// read last, which are still in L2.  SR != 0 rounds the codes stochastically
-// (SR = 10: Philox4x32-10 unrolled; SR < 0: g.sr_rounds rounds).
+// NVFP4 pass 2, persistent: a tensor's blocks are cut into chunks of
+// kThreads * kNvBlocksPerThread (chunks first_cta .. of the group's chunk
+// list), and each CTA first reduces the partial maxima of every tensor of the
+// group to its s_t and tables (once), then loops over chunks blockIdx.x,
+// blockIdx.x + gridDim.x, ...: thread t quantizes blocks t and t + kThreads
+// of the chunk, and the next chunk's blocks are loaded before the current
+// ones are quantized, so that their latency overlaps the arithmetic.  Each
+// binary32 step of the definition is one round-to-nearest operation
+// (correctly rounded divisions where it divides).  Chunks are taken in the
+// reverse of the order in which pass 1 swept the blocks, so the first ones
+// quantized are those pass 1 read last, which are still in L2.  SR != 0
+// rounds the codes stochastically (SR = 10: Philox4x32-10 unrolled; SR < 0:
+// g.sr_rounds rounds).
+// resident CTAs per SM: 4 for round to nearest; 3 with stochastic rounding,
+// whose Philox and rounding arithmetic need more than 64 registers a thread
+constexpr int nv_ctas_per_sm(int sr) { return sr != 0 ? 3 : 4; }
+
+struct NvChunk {
+  uint32_t w[kNvBlocksPerThread][8];
+  uint32_t r[kNvBlocksPerThread], j[kNvBlocksPerThread];
+  int ti;       // tensor of the group
+  uint32_t b0;  // first block of this thread in the chunk
+};
+
+template <bool WIDE>
+__device__ __forceinline__ void nv_load_chunk(const QGroup &g, uint32_t chunk, NvChunk &k) {
+  int ti = 0;
+#pragma unroll
+  for (int i = 1; i < kQuantizeGroupMax; ++i)
+    if (i < g.count && chunk >= g.t[i].first_cta) ti = i;
+  const QTensor &t = g.t[ti];
+  k.ti = ti;
+  k.b0 = (chunk - t.first_cta) * (kThreads * kNvBlocksPerThread) + threadIdx.x;
+#pragma unroll
+  for (int q = 0; q < kNvBlocksPerThread; ++q) {
+    const uint32_t b = k.b0 + q * kThreads;
+    k.r[q] = fast_div(b, t.kbdiv);
+    k.j[q] = b - k.r[q] * t.kbdiv.d;
+    if (b < t.total && k.r[q] < t.rows)
+      load32<WIDE>(t.x + static_cast<int64_t>(k.r[q]) * t.ld + k.j[q] * 16u, k.w[q]);
+  }
+}
+
 template <bool WIDE, int SR>
-__global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_kernel(const __grid_constant__ QGroup g) {
+__global__ void __launch_bounds__(kThreads, nv_ctas_per_sm(SR)) nvfp4_quantize_kernel(const __grid_constant__ QGroup g) {
   griddep_launch_dependents();
   griddep_wait();
-  const uint32_t cta = gridDim.x - 1 - blockIdx.x;
-  const QTensor &t = group_member(g, cta);
-  // The thread's blocks are loaded first: their latency then overlaps the
-  // reduction of the partial maxima, which they do not depend on.
-  const uint32_t kb = t.kbdiv.d;
-  const uint32_t base = (cta - t.first_cta) * (kThreads * kNvBlocksPerThread) + threadIdx.x;
-  uint8_t *__restrict__ scales = t.scales;
-  uint32_t w[kNvBlocksPerThread][8];
-  uint32_t rq[kNvBlocksPerThread], jq[kNvBlocksPerThread];
-#pragma unroll
-  for (int q = 0; q < kNvBlocksPerThread; ++q) {
-    const uint32_t b = base + q * kThreads;
-    rq[q] = fast_div(b, t.kbdiv);
-    jq[q] = b - rq[q] * kb;
-    if (b < t.total && rq[q] < t.rows)
-      load32<WIDE>(t.x + static_cast<int64_t>(rq[q]) * t.ld + jq[q] * 16u, w[q]);
+  const uint32_t nchunks = g.t[g.count - 1].first_cta + g.t[g.count - 1].nchunks;
+  uint32_t ch = blockIdx.x;
+  NvChunk next;
+  if (ch < nchunks) nv_load_chunk<WIDE>(g, nchunks - 1 - ch, next);
+  // the per-tensor constants, once per CTA (the first loads are in flight)
+  __shared__ float den_tab[kQuantizeGroupMax][128], rcp_tab[kQuantizeGroupMax][128];
+  __shared__ NvConst consts[kQuantizeGroupMax];
+  for (int i = 0; i < g.count; ++i) {
+    const NvConst c = nv_setup(g.t[i].partials, g.t[i].tensor_scale, blockIdx.x == 0, den_tab[i],
+                               rcp_tab[i]);
+    if (threadIdx.x == 0) consts[i] = c;
   }
-  __shared__ float den_tab[128], rcp_tab[128];
-  const NvConst c = nv_setup(t.partials, t.tensor_scale, cta == t.first_cta, den_tab, rcp_tab);
+  __syncthreads();
+  for (; ch < nchunks; ch += gridDim.x) {
+    const NvChunk cur = next;
+    if (ch + gridDim.x < nchunks) nv_load_chunk<WIDE>(g, nchunks - 1 - (ch + gridDim.x), next);
+    const QTensor &t = g.t[cur.ti];
+    const NvConst c = consts[cur.ti];
+    const uint32_t kb = t.kbdiv.d;
+    uint8_t *__restrict__ scales = t.scales;
 #pragma unroll
-  for (int q = 0; q < kNvBlocksPerThread; ++q) {
-    if (base + q * kThreads >= t.total) continue;
-    const uint32_t r = rq[q], j = jq[q];
-    uint32_t sb = 0;
-    if (r < t.rows) {
-      uint2 out;
-      sb = nv_block<SR>(w[q], c, den_tab, rcp_tab, j, r, g.sr_direction, g.sr_key0, g.sr_key1,
-                        g.sr_rounds, out);
-      *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
-    }
-    if (t.tiled) {
-      scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sb);
-      if (j == kb - 1)
-        for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
-    } else {
-      scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
+    for (int q = 0; q < kNvBlocksPerThread; ++q) {
+      if (cur.b0 + q * kThreads >= t.total) continue;
+      const uint32_t r = cur.r[q], j = cur.j[q];
+      uint32_t sb = 0;
+      if (r < t.rows) {
+        uint2 out;
+        sb = nv_block<SR>(cur.w[q], c, den_tab[cur.ti], rcp_tab[cur.ti], j, r, g.sr_direction,
+                          g.sr_key0, g.sr_key1, g.sr_rounds, out);
+        *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
+      }
+      if (t.tiled) {
+        scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sb);
+        if (j == kb - 1)
+          for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
+      } else {
+        scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
+      }
     }
   }
 }
@@ -814,7 +853,8 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
     g.sr_rounds = sr->rounds;
   }
   bool wide = true;
-  uint32_t ctas = 0;
+  uint32_t ctas = 0;  // MXFP4: CTAs; NVFP4: chunks of pass 2
+  int num_sms = 152;
   for (int i = 0; i < count; ++i) {
     const QuantizeArgs &a = tensors[i];
     QTensor &t = g.t[i];
@@ -836,7 +876,9 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
     t.kbdiv = make_fastdiv(kb);
     t.tiled = a.tiled;
     const uint32_t per_cta = kThreads * (fmt == 0 ? 1u : static_cast<uint32_t>(kNvBlocksPerThread));
-    ctas += (t.total + per_cta - 1) / per_cta;
+    t.nchunks = (t.total + per_cta - 1) / per_cta;
+    ctas += t.nchunks;
+    if (a.num_sms > 0) num_sms = a.num_sms;
     wide = wide && wide_ok(a.x, a.ld);
   }
   cudaError_t e;
@@ -853,7 +895,10 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
       kern = wide ? nvfp4_quantize_kernel<true, 10> : nvfp4_quantize_kernel<false, 10>;
     else if (sr)
       kern = wide ? nvfp4_quantize_kernel<true, -1> : nvfp4_quantize_kernel<false, -1>;
-    e = launch_pdl(kern, dim3(ctas), dim3(kThreads), 0, s, g);
+    // persistent: as many CTAs as are resident, each looping over chunks
+    const uint32_t resident = static_cast<uint32_t>(num_sms * nv_ctas_per_sm(sr ? 1 : 0));
+    const uint32_t grid = ctas < resident ? ctas : resident;
+    e = launch_pdl(kern, dim3(grid), dim3(kThreads), 0, s, g);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
