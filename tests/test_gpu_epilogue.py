@@ -188,3 +188,21 @@ def test_plain_entry_points_unchanged_by_a_null_epilogue():
         torch.cuda.synchronize()
         out.append(d.view(torch.int16).cpu().numpy())
     assert np.array_equal(out[0], out[1])
+
+
+def test_bias_gelu_workload_full_size_sampled():
+    """The bias + GELU workload as bench.py runs it (quantize A and W, GEMM with
+    the FP32 bias and GELU), checked on sampled output rows."""
+    from tests.gpu_helpers import sample_indices
+    name = "quant_gemm_bias_gelu_2048x4096x4096"
+    w = synth.workload_inputs(name)
+    m, n, k = 2048, 4096, 4096
+    ca, sa_t, _ = gpu_quantize(w["a"], MX, TILED)
+    cb, sb_t, _ = gpu_quantize(w["b"], MX, TILED)
+    ra, rsa = oracle.mx_quantize(w["a"])
+    rb, rsb = oracle.mx_quantize(w["b"])
+    assert np.array_equal(ca, ra) and np.array_equal(cb, rb)
+    got = _run(MX, (ca, sa_t, cb, sb_t), m, n, k, False, 1, w["bias"], 0.0, True, None)
+    rows = sample_indices(m, 48, 256, seed=11)
+    ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k, rows=rows)
+    _check(got[rows], ref, s_abs, w["bias"], 0.0, None, True, False, "bias+gelu workload")

@@ -451,3 +451,10 @@ def test_nvfp4_quantize_2d_columnwise_only():
             assert codes is None and scales is None and ts == rt
             assert np.array_equal(codes_t, rct)
             assert np.array_equal(scales_t, rst.ravel() if layout == PLAIN else oracle.scale_tile(rst))
+
+
+def test_nvfp4_sr_full_size_bench_tensor():
+    """The 16384 x 8192 tensor of the stochastic-rounding workload, in the tile
+    scale order and with the seed bench.py uses."""
+    x = synth.workload_inputs("nvfp4_sr_16384x8192")["a"]
+    _check_nv_sr(x, 0x5EED5EED, 10, TILED)
