@@ -104,6 +104,25 @@ def dist_env():
     return world, rank, local
 
 
+def reduce_max(x, world, device):
+    """The maximum of a per-rank float over all ranks of the default process
+    group (x itself on one rank); device: where the collective's tensor lives
+    ("cuda" under NCCL, "cpu" under gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(work_per_step, ms_per_step_max, world):
+    """Whole-job throughput of N replicas: every rank does work_per_step per
+    step, and the job's step takes the slowest rank's time."""
+    return world * work_per_step / (ms_per_step_max * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -653,19 +672,12 @@ def main_ours(args):
     time.sleep(0.3)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    ms_per_step = ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = reduce_max(ms / args.steps, world, "cuda")
 
     per_call = time_calls(wl, args.steps)
     e2e_steps = args.e2e_steps or min(args.steps, 200)
     e2e_ms, h2d, d2h = time_e2e(wl, host, e2e_steps)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, world, "cuda")
 
     peaks, peak_src = load_peaks()
     fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
@@ -675,7 +687,7 @@ def main_ours(args):
     # a quantize-only step has no GEMM: its value is algorithmic GB/s
     step_work = sum(b for b, _ in wl.algorithmic().values()) / 1e9 if quant_only else flops / 1e12
     unit = "GB/s" if quant_only else "TFLOPS"
-    value = world * step_work / (ms_per_step * 1e-3)
+    value = job_throughput(step_work, ms_per_step, world)
     alg = wl.algorithmic()
     kpc = wl.kernels_per_call()
     kernels = {}
@@ -716,7 +728,7 @@ def main_ours(args):
         "roofline": roofline,
         "kernels": kernels,
         "sum_of_calls_ms": sum(per_call.values()),
-        "e2e": {"value": world * step_work / (e2e_ms * 1e-3), "unit": unit,
+        "e2e": {"value": job_throughput(step_work, e2e_ms, world), "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps * sum(kpc.values()),
         "clocks": clocks,
