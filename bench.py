@@ -25,7 +25,8 @@ during the timed region.
 
 `e2e` is the same metric through the public C ABI with the inputs in pinned
 host memory: every step copies A and W host->device, quantizes, multiplies
-and copies D back.  `cpu_baseline` is the CPU oracle (tests' reference
+and copies D back, with the steps pipelined over three streams (copy in,
+compute, copy out) so that one step's copies overlap its neighbours' compute.  `cpu_baseline` is the CPU oracle (tests' reference
 implementation, untuned) on a bounded sample of the same step.
 
 --impl reference times that oracle instead (rank 0 only), each step a
@@ -461,9 +462,14 @@ def time_calls(wl, steps, per_graph=40):
 
 
 def time_e2e(wl, host_inputs, steps):
-    """Same metric through the C ABI from pinned host buffers (H2D + step + D2H)."""
+    """Same metric through the C ABI from pinned host buffers: every step copies
+    its inputs host -> device, runs the step's calls and copies its result back
+    to the host.  The steps are pipelined over three streams (copy in, compute,
+    copy out), as a serving loop would run them: step i's inputs are copied
+    while step i-1 computes and step i-2's result is read back.  A rotating set's
+    device buffers are refilled only after the step that last used them has been
+    read back, and each set has its own pinned result buffers."""
     torch = wl.torch
-    s0 = wl.sets[0]
     pinned = {}
     if wl.kind in ("bf16",) + QUANT_KINDS:
         pinned["x_a"] = torch.from_numpy(host_inputs["a"].view(np.int16)).view(
@@ -478,32 +484,46 @@ def time_e2e(wl, host_inputs, steps):
         pinned["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).pin_memory()
     # the step's result read back: D, or the code outputs of a quantize step
     result_keys = {"quant2d": ["codes_a", "codes_t"], "quant_sr": ["codes_a"]}.get(wl.kind, ["d"])
-    results = {key: torch.empty(s0[key].shape, dtype=s0[key].dtype).pin_memory()
-               for key in result_keys}
+    nset = len(wl.sets)
+    results = [{key: torch.empty(st[key].shape, dtype=st[key].dtype).pin_memory()
+                for key in result_keys} for st in wl.sets]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = sum(t.numel() * t.element_size() for t in results.values())
-    stream = torch.cuda.Stream()
+    d2h = sum(t.numel() * t.element_size() for t in results[0].values())
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_out = {}
 
     def one(i):
-        s = wl.sets[i % len(wl.sets)]
-        for key, t in pinned.items():
-            s[key].view(-1).copy_(t.view(-1), non_blocking=True)
+        k = i % nset
+        st = wl.sets[k]
+        if i - nset in ev_out:
+            s_in.wait_event(ev_out.pop(i - nset))  # set k's last step has been read back
+        with torch.cuda.stream(s_in):
+            for key, t in pinned.items():
+                st[key].view(-1).copy_(t.view(-1), non_blocking=True)
+        ev_in = torch.cuda.Event()
+        ev_in.record(s_in)
+        s_cmp.wait_event(ev_in)
         for _, fn in wl.calls():
-            fn(s, stream.cuda_stream)
-        for key, t in results.items():
-            t.copy_(s[key], non_blocking=True)
+            fn(st, s_cmp.cuda_stream)
+        ev_cmp = torch.cuda.Event()
+        ev_cmp.record(s_cmp)
+        s_out.wait_event(ev_cmp)
+        with torch.cuda.stream(s_out):
+            for key, t in results[k].items():
+                t.copy_(st[key], non_blocking=True)
+        ev_out[i] = torch.cuda.Event()
+        ev_out[i].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            one(i)
+    for i in range(3):
+        one(i)
     torch.cuda.synchronize()
+    ev_out.clear()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for i in range(steps):
-            one(i)
-        end.record(stream)
+    start.record(s_in)
+    for i in range(steps):
+        one(i)
+    end.record(s_out)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps, h2d, d2h
 
