@@ -21,7 +21,9 @@
 //   warps 2..9  both CTAs: two warps per tensor-memory lane quarter, 128
 //               columns each, pull the accumulator into registers at once,
 //               hand it back to the MMA warp (arrivals counted in the leader),
-//               then convert and store 32-row boxes with TMA.
+//               then convert and store 32-row boxes with TMA.  The instances
+//               with GELU or beta * C in the epilogue run 16 such warps
+//               (warps 2..17, four per lane quarter, 64 columns each).
 // Every wait is bounded; the CTAs meet at a cluster barrier before freeing
 // tensor memory and leaving, so no remote arrival targets a finished CTA.
 #include <cuda_bf16.h>
@@ -34,15 +36,20 @@
 namespace mx {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
 constexpr int kStagingBytes = 2048;  // per epilogue warp: 32 rows x 64 bytes
 constexpr int kStageKBytes = 128;    // 256 FP4 codes of K per stage
 
-template <int FMT>
+// EW: epilogue warps per CTA.  8 (128 accumulator columns each) for the plain
+// epilogue; 16 (64 columns each) for the instances with epilogue terms, whose
+// per-output work (bias, beta * C, GELU) needs more warps to hide its latency
+// behind the next tile's MMAs.
+template <int FMT, int EW>
 struct PairCfg {
+  static constexpr int kEpiWarps = EW;
+  static constexpr int kThreads = 64 + 32 * EW;   // producer, MMA issuer, epilogue
+  static constexpr int kWarpCols = 1024 / EW;     // accumulator columns per epilogue warp
   static constexpr int kAtomsK = FMT == 0 ? 2 : 4;  // 4-scale atoms per stage along K
-  static constexpr int kStages = FMT == 0 ? 6 : 5;
+  static constexpr int kStages = (FMT == 0 && EW == 8) ? 6 : 5;
   static constexpr int kABytes = 128 * kStageKBytes;
   static constexpr int kBBytes = 128 * kStageKBytes;  // this CTA's half of B
   static constexpr int kSfaBytes = kAtomsK * 512;
@@ -53,7 +60,8 @@ struct PairCfg {
   static constexpr int kTmemCols = 512;
   static_assert(kSfCol + kStages * kSfSetCols <= kTmemCols, "tensor memory budget");
   // the last tile's output boxes are staged in the idle stage ring
-  static_assert(kEpiWarps * 8 * 2048 <= kStages * kStageBytes, "ring holds the last tile's boxes");
+  static_assert(kEpiWarps * (kWarpCols / 16) * kStagingBytes <= kStages * kStageBytes,
+                "ring holds the last tile's boxes");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static constexpr int kStagingOff = kStages * kStageBytes;
   static constexpr int kBarBytes = 8 * (2 * kStages + 3) + 16;
@@ -112,18 +120,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// EPI: 1 applies the epilogue terms of p.epi (never with split-K partials);
-// 0 compiles the plain epilogue.
+// EPI: 0 compiles the plain epilogue; 1 applies the epilogue terms of p.epi
+// (never with split-K partials) with 8 epilogue warps (a bias only); 2 the
+// same with 16 epilogue warps (GELU or beta * C, whose per-output work needs
+// them).
 template <int FMT, int OUT_F32, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(PairCfg<FMT, EPI == 2 ? 16 : 8>::kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_sfa,
                      const __grid_constant__ CUtensorMap tmap_sfb,
                      const __grid_constant__ CUtensorMap tmap_d, const PairParams p) {
-  using C = PairCfg<FMT>;
+  using C = PairCfg<FMT, EPI == 2 ? 16 : 8>;
   constexpr int kBoxCols = OUT_F32 ? 16 : 32;
-  constexpr int kBoxes = 128 / kBoxCols;  // per epilogue warp and tile
+  constexpr int kBoxes = C::kWarpCols / kBoxCols;  // per epilogue warp and tile
   extern __shared__ __align__(1024) uint8_t smem[];
   // The 128-byte swizzle needs 1024-byte aligned stages; were the dynamic
   // shared memory ever placed otherwise, report it and leave (every thread
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(tfull), 1);
     mbar_init(smem_u32(tempty), 2);
-    mbar_init(smem_u32(eload), kEpiWarps);
+    mbar_init(smem_u32(eload), C::kEpiWarps);
     *abort = 0u;
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     griddep_wait();
     const int q = warp & 3;          // tensor-memory lane quarter of this warp
-    const int h = (warp - 2) >> 2;   // which 128 of the 256 columns
+    const int h = (warp - 2) >> 2;   // which kWarpCols-column group of the 256 columns
     uint8_t *stage_base = smem + C::kStagingOff + (warp - 2) * C::kStagingBufs * kStagingBytes;
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
     float alpha = 1.0f;
@@ -303,29 +313,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = cluster; u < p.num_units; u += nclusters, ++tile) {
       int pm, nt, sp;
       decode_unit(p, u, pm, nt, sp);
-      // the bias of this warp's 128 columns, four per lane (loaded before the
-      // wait, so that its latency is hidden; N % 32 == 0: a lane's four
+      // the bias of this warp's columns, kWarpCols / 32 per lane (loaded
+      // before the wait, so that its latency is hidden; N % 32 == 0: a lane's
       // columns are all in range or all out)
-      float bias_l[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      constexpr int kBiasPerLane = C::kWarpCols / 32;
+      float bias_l[kBiasPerLane];
+#pragma unroll
+      for (int j = 0; j < kBiasPerLane; ++j) bias_l[j] = 0.0f;
       if constexpr (EPI != 0) {
-        const int bc = nt * 256 + h * 128 + 4 * lane;
+        const int bc = nt * 256 + h * C::kWarpCols + kBiasPerLane * lane;
         if (p.epi.bias != nullptr && bc < p.n) {
-          const float4 v = __ldg(reinterpret_cast<const float4 *>(p.epi.bias + bc));
-          bias_l[0] = v.x;
-          bias_l[1] = v.y;
-          bias_l[2] = v.z;
-          bias_l[3] = v.w;
+#pragma unroll
+          for (int j = 0; j < kBiasPerLane; ++j) bias_l[j] = __ldg(p.epi.bias + bc + j);
         }
       }
       const bool ready = mbar_wait(smem_u32(tfull), tile & 1u, abort, p.status);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;
       tc_fence_after();
-      uint32_t r[128];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-      tc_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-      tc_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-      tc_ld_32x32b_x32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-      tc_ld_32x32b_x32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+      uint32_t r[C::kWarpCols];
+      const uint32_t taddr =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * C::kWarpCols);
+#pragma unroll
+      for (int i = 0; i < C::kWarpCols / 32; ++i)
+        tc_ld_32x32b_x32(taddr + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * i]));
       tc_wait_ld();
       // The accumulator is in registers.  The CTA's epilogue warps meet
       // (bounded) before any of them starts converting, so that no warp's
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int y = p.partial ? sp * p.m + row0 : row0;
 #pragma unroll
       for (int c = 0; c < kBoxes; ++c) {
-        const int col0 = nt * 256 + h * 128 + c * kBoxCols;
+        const int col0 = nt * 256 + h * C::kWarpCols + c * kBoxCols;
         if (!rows_ok || col0 >= p.n) continue;  // warp-uniform
         uint8_t *stage_buf;
         if (last) {
@@ -376,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float bv[4];
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const int cc = c * 16 + 4 * i + j;  // column within the warp's 128
-                bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc & 3], cc >> 2);
+                const int cc = c * 16 + 4 * i + j;  // column within the warp's columns
+                bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc % kBiasPerLane], cc / kBiasPerLane);
               }
               epilogue_terms<4, 1>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 4 * i,
                                    bv);
@@ -398,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               float bv[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const int cc = c * 32 + 8 * i + j;  // column within the warp's 128
-                bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc & 3], cc >> 2);
+                const int cc = c * 32 + 8 * i + j;  // column within the warp's columns
+                bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc % kBiasPerLane], cc / kBiasPerLane);
               }
               epilogue_terms<8, 0>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 8 * i,
                                    bv);
@@ -438,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int FMT, int OUT_F32, int EPI>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
-  using C = PairCfg<FMT>;
+  using C = PairCfg<FMT, EPI == 2 ? 16 : 8>;
   auto kernel = gemm_pair_kernel<FMT, OUT_F32, EPI>;
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
@@ -453,7 +463,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -499,16 +509,21 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 
 cudaError_t launch_gemm_pair(const GemmArgs &g, cudaStream_t s) {
   const bool f32 = g.out_fp32 || g.split_k > 1;
-  // with split-K the reduction applies the epilogue terms
-  const bool epi = g.split_k == 1 && (g.epi.bias || g.epi.c || g.epi.gelu);
+  // with split-K the reduction applies the epilogue terms; GELU and beta * C
+  // take the 16-warp epilogue, a bias alone the 8-warp one
+  const int epi = g.split_k != 1 ? 0 : (g.epi.gelu || g.epi.c) ? 2 : g.epi.bias ? 1 : 0;
   cudaError_t e;
   if (g.fmt == 0) {
-    if (epi)
+    if (epi == 2)
+      e = f32 ? launch_typed<0, 1, 2>(g, s) : launch_typed<0, 0, 2>(g, s);
+    else if (epi == 1)
       e = f32 ? launch_typed<0, 1, 1>(g, s) : launch_typed<0, 0, 1>(g, s);
     else
       e = f32 ? launch_typed<0, 1, 0>(g, s) : launch_typed<0, 0, 0>(g, s);
   } else {
-    if (epi)
+    if (epi == 2)
+      e = f32 ? launch_typed<1, 1, 2>(g, s) : launch_typed<1, 0, 2>(g, s);
+    else if (epi == 1)
       e = f32 ? launch_typed<1, 1, 1>(g, s) : launch_typed<1, 0, 1>(g, s);
     else
       e = f32 ? launch_typed<1, 1, 0>(g, s) : launch_typed<1, 0, 0>(g, s);
