@@ -16,7 +16,9 @@ E2M1/E4M3/BF16 codec checks against brute-force nearest-value searches and
 library routines, the exhaustive BF16 quantize sweep, GEMM brute force against
 a dequantize-then-fp64 matmul, the closed-form invariants, and for the
 stochastic-rounding path the published Philox4x32 known answers, exact
-rational rounding and the half-way inputs that expose the draw layout.
+rational rounding and the half-way inputs that expose the draw layout, and for
+the GEMM epilogue the normal CDF at known points, scipy's normal CDF and the
+reflection identity of GELU.
 """
 from __future__ import annotations
 
