@@ -344,7 +344,9 @@ __device__ __forceinline__ uint4 philox4x32(uint4 c, uint32_t k0, uint32_t k1, i
 // F(b) = ceil(p 2^22); the 1 is taken off again at the end (exactly).
 __device__ __forceinline__ float sr_e2m1_value(float q, uint32_t nu) {
   const float a = fabsf(q);
-  const float off = a < 1.0f ? 1.0f : 0.0f;
+  // off = 1 below 1, else 0, as one saturating FMA (FMA pipe, not ALU):
+  // 2^30 (1 - a) is >= 64 for every binary32 a < 1, 0 at 1, negative above
+  const float off = __saturatef(__fmaf_rn(-a, 0x1p30f, 0x1p30f));
   const float b = __fadd_ru(a, off);
   const uint32_t add = ((nu & 0xFFu) << 14) | 0x3FFFu;
   const float t = __uint_as_float((__float_as_uint(b) + add) & 0xFFC00000u);
