@@ -731,7 +731,7 @@ struct Nv2dArgs {
 };
 
 template <bool WIDE, int SR>
-__global__ void __launch_bounds__(kThreads) nvfp4_quantize_2d_kernel(const __grid_constant__ Nv2dArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __grid_constant__ Nv2dArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ __align__(16) uint32_t tile[k2dRows][k2dCols / 2];
