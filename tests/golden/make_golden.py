@@ -45,6 +45,30 @@ def main():
     with open(os.path.join(HERE, "oracle_regression.json"), "w") as f:
         json.dump(out, f, indent=1)
 
+    # stochastic rounding, the bidimensional NVFP4 quantize and the GEMM epilogue
+    y = synth.bf16_normal(32, 64, 0.5, seed=0x6022)
+    sr10, _, _ = oracle.nvfp4_quantize_sr(y, 0x0123456789ABCDEF, 10)
+    sr7, _, _ = oracle.nvfp4_quantize_sr(y, 0x0123456789ABCDEF, 7)
+    _, _, ct, st, _ = oracle.nvfp4_quantize_2d(y, seed=0x0123456789ABCDEF)
+    draws = [oracle.philox4x32([j, r, d, 0], [0x89ABCDEF, 0x01234567], 10).tolist()
+             for j, r, d in ((0, 0, 0), (3, 17, 0), (1, 2, 1))]
+    bias = np.linspace(-1.0, 1.0, 3).astype(np.float32)
+    c = np.arange(9, dtype=np.float64).reshape(3, 3) - 4.0
+    epi = oracle.gemm_epilogue(d, bias=bias, gelu_on=True, beta=0.5, c=c)
+    out2 = {
+        "about": "oracle regression fixture written by make_golden.py (CPU oracle only)",
+        "sr_input_seed": 0x6022, "sr_seed": 0x0123456789ABCDEF,
+        "sr10_codes_hex": [bytes(r).hex() for r in sr10],
+        "sr7_codes_hex": [bytes(r).hex() for r in sr7],
+        "nv2d_sr_codes_t_hex": [bytes(r).hex() for r in ct],
+        "nv2d_sr_scales_t": st.tolist(),
+        "philox_draws": draws,
+        "epilogue_bias": bias.tolist(), "epilogue_c": c.tolist(), "epilogue_beta": 0.5,
+        "epilogue_gelu_d": epi.tolist(),
+    }
+    with open(os.path.join(HERE, "oracle_regression_sr_epilogue.json"), "w") as f:
+        json.dump(out2, f, indent=1)
+
 
 if __name__ == "__main__":
     main()

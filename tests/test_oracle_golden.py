@@ -28,3 +28,28 @@ def test_oracle_regression_fixture(oracle):
     d, s_abs = oracle.mx_gemm(a, sa, b, sb, 32, 32, 256, rows=g["gemm_rows"], cols=g["gemm_cols"])
     assert d.tolist() == g["gemm_d"]
     assert s_abs.tolist() == g["gemm_s_abs"]
+
+
+def test_oracle_regression_fixture_sr_and_epilogue(oracle):
+    g = json.load(open(os.path.join(HERE, "oracle_regression_sr_epilogue.json")))
+    y = synth.bf16_normal(32, 64, 0.5, seed=g["sr_input_seed"])
+    seed = g["sr_seed"]
+    c10, _, _ = oracle.nvfp4_quantize_sr(y, seed, 10)
+    c7, _, _ = oracle.nvfp4_quantize_sr(y, seed, 7)
+    assert [bytes(r).hex() for r in c10] == g["sr10_codes_hex"]
+    assert [bytes(r).hex() for r in c7] == g["sr7_codes_hex"]
+    _, _, ct, st, _ = oracle.nvfp4_quantize_2d(y, seed=seed)
+    assert [bytes(r).hex() for r in ct] == g["nv2d_sr_codes_t_hex"]
+    assert st.tolist() == g["nv2d_sr_scales_t"]
+    draws = [oracle.philox4x32([j, r, d, 0], [0x89ABCDEF, 0x01234567], 10).tolist()
+             for j, r, d in ((0, 0, 0), (3, 17, 0), (1, 2, 1))]
+    assert draws == g["philox_draws"]
+    gg = json.load(open(os.path.join(HERE, "oracle_regression.json")))
+    a = synth.fp4_codes(32, 256, seed=gg["gemm_seeds"][0])
+    b = synth.fp4_codes(32, 256, seed=gg["gemm_seeds"][1])
+    sa = synth.scale_bytes(32, 8, 120, 134, seed=gg["gemm_seeds"][2])
+    sb = synth.scale_bytes(32, 8, 120, 134, seed=gg["gemm_seeds"][3])
+    d, _ = oracle.mx_gemm(a, sa, b, sb, 32, 32, 256, rows=gg["gemm_rows"], cols=gg["gemm_cols"])
+    epi = oracle.gemm_epilogue(d, bias=np.float32(g["epilogue_bias"]), gelu_on=True,
+                               beta=g["epilogue_beta"], c=np.array(g["epilogue_c"]))
+    assert epi.tolist() == g["epilogue_gelu_d"]
