@@ -497,9 +497,10 @@ __device__ __forceinline__ uint32_t nv_block(const uint32_t *w, const NvConst &c
 // kThreads * kNvBlocksPerThread (chunks first_cta .. of the group's chunk
 // list), and each CTA first reduces the partial maxima of every tensor of the
 // group to its s_t and tables (once), then loops over chunks blockIdx.x,
-// blockIdx.x + gridDim.x, ...: thread t quantizes blocks t and t + kThreads
-// of the chunk, and the next chunk's blocks are loaded before the current
-// ones are quantized, so that their latency overlaps the arithmetic.  Each
+// blockIdx.x + gridDim.x, ...: thread t quantizes blocks 2t and 2t + 1 of
+// the chunk (one division for the pair; with an even block count per row the
+// pair's codes and scales are written with one store each), and the next
+// chunk's blocks are loaded before the current ones are quantized, so that their latency overlaps the arithmetic.  Each
 // binary32 step of the definition is one round-to-nearest operation
 // (correctly rounded divisions where it divides).  Chunks are taken in the
 // reverse of the order in which pass 1 swept the blocks, so the first ones
@@ -510,11 +511,14 @@ __device__ __forceinline__ uint32_t nv_block(const uint32_t *w, const NvConst &c
 // whose Philox and rounding arithmetic need more than 64 registers a thread
 constexpr int nv_ctas_per_sm(int sr) { return sr != 0 ? 3 : 4; }
 
+// A thread's two consecutive blocks b0, b0 + 1 of a chunk (the second is the
+// next block of the row, or the first block of the next row).
+static_assert(kNvBlocksPerThread == 2, "a thread quantizes a pair of consecutive blocks");
 struct NvChunk {
   uint32_t w[kNvBlocksPerThread][8];
   uint32_t r[kNvBlocksPerThread], j[kNvBlocksPerThread];
   int ti;       // tensor of the group
-  uint32_t b0;  // first block of this thread in the chunk
+  uint32_t b0;  // first block of this thread
 };
 
 template <bool WIDE>
@@ -525,15 +529,16 @@ __device__ __forceinline__ void nv_load_chunk(const QGroup &g, uint32_t chunk, N
     if (i < g.count && chunk >= g.t[i].first_cta) ti = i;
   const QTensor &t = g.t[ti];
   k.ti = ti;
-  k.b0 = (chunk - t.first_cta) * (kThreads * kNvBlocksPerThread) + threadIdx.x;
+  k.b0 = (chunk - t.first_cta) * (kThreads * kNvBlocksPerThread) + 2 * threadIdx.x;
+  k.r[0] = fast_div(k.b0, t.kbdiv);
+  k.j[0] = k.b0 - k.r[0] * t.kbdiv.d;
+  const bool same_row = k.j[0] + 1 < t.kbdiv.d;
+  k.r[1] = same_row ? k.r[0] : k.r[0] + 1;
+  k.j[1] = same_row ? k.j[0] + 1 : 0u;
 #pragma unroll
-  for (int q = 0; q < kNvBlocksPerThread; ++q) {
-    const uint32_t b = k.b0 + q * kThreads;
-    k.r[q] = fast_div(b, t.kbdiv);
-    k.j[q] = b - k.r[q] * t.kbdiv.d;
-    if (b < t.total && k.r[q] < t.rows)
+  for (int q = 0; q < kNvBlocksPerThread; ++q)
+    if (k.b0 + q < t.total && k.r[q] < t.rows)
       load32<WIDE>(t.x + static_cast<int64_t>(k.r[q]) * t.ld + k.j[q] * 16u, k.w[q]);
-  }
 }
 
 template <bool WIDE, int SR>
@@ -560,9 +565,34 @@ __global__ void __launch_bounds__(kThreads, nv_ctas_per_sm(SR)) nvfp4_quantize_k
     const NvConst c = consts[cur.ti];
     const uint32_t kb = t.kbdiv.d;
     uint8_t *__restrict__ scales = t.scales;
+    if ((kb & 1u) == 0) {
+      // kb even (cols % 32 == 0): the pair lies in one row, its 16 code bytes
+      // are 16-byte aligned and its two scale bytes adjacent
+      if (cur.b0 >= t.total) continue;  // total = rows_pad * kb is even
+      const uint32_t r = cur.r[0], j = cur.j[0];
+      uint32_t sb0 = 0, sb1 = 0;
+      if (r < t.rows) {
+        uint2 o0, o1;
+        sb0 = nv_block<SR>(cur.w[0], c, den_tab[cur.ti], rcp_tab[cur.ti], j, r, g.sr_direction,
+                           g.sr_key0, g.sr_key1, g.sr_rounds, o0);
+        sb1 = nv_block<SR>(cur.w[1], c, den_tab[cur.ti], rcp_tab[cur.ti], j + 1, r,
+                           g.sr_direction, g.sr_key0, g.sr_key1, g.sr_rounds, o1);
+        *reinterpret_cast<uint4 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) =
+            make_uint4(o0.x, o0.y, o1.x, o1.y);
+      }
+      const uint16_t s2 = static_cast<uint16_t>(sb0 | (sb1 << 8));
+      if (t.tiled) {
+        *reinterpret_cast<uint16_t *>(scales + tiled_offset(r, j, t.katoms)) = s2;
+        if (j + 2 == kb)
+          for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
+      } else {
+        *reinterpret_cast<uint16_t *>(scales + static_cast<int64_t>(r) * kb + j) = s2;
+      }
+      continue;
+    }
 #pragma unroll
     for (int q = 0; q < kNvBlocksPerThread; ++q) {
-      if (cur.b0 + q * kThreads >= t.total) continue;
+      if (cur.b0 + q >= t.total) continue;
       const uint32_t r = cur.r[q], j = cur.j[q];
       uint32_t sb = 0;
       if (r < t.rows) {
