@@ -23,7 +23,11 @@
  *   - NVIDIA/TransformerEngine #3809 (NVFP4 quantize kernels): BF16 -> NVFP4
  *     with E4M3 per-16 scales and an FP32 per-tensor amax; one kernel per
  *     call where possible; round-to-nearest output byte-identical across
- *     implementations.
+ *     implementations; a bidimensional (rowwise + columnwise) kernel; and
+ *     stochastic rounding with one Philox4x32 draw per output block.
+ * mxfp4_gemm / nvfp4_gemm keep the first page's limits (beta == 0, no bias,
+ * no GELU).  mxfp4_gemm_ex / nvfp4_gemm_ex add those terms as an optional
+ * epilogue, with the FP32 bias the a4w4 review asks for.
  *
  * Conventions of every entry point:
  *   - Return 0 (MX_OK) or a negative MX_ERR_* code.  On an argument error
