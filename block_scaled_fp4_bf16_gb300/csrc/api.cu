@@ -534,7 +534,7 @@ MX_API int nvfp4_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int
   const mx::SrArgs sr{seed, philox_rounds, 0u};
   return launch_rc(mx::launch_nvfp4_quantize_2d(
       x, rows, cols, ld_x, scale_layout == MX_SCALE_TCGEN05, codes, scales, codes_t, scales_t,
-      tensor_scale, static_cast<uint32_t *>(workspace), stochastic ? &sr : nullptr,
+      tensor_scale, static_cast<uint32_t *>(workspace), stochastic ? &sr : nullptr, dev->num_sms,
       static_cast<cudaStream_t>(stream)));
 }
 

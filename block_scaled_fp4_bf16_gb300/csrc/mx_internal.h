@@ -80,7 +80,7 @@ cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int
 cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld,
                                      int tiled, void *codes, void *scales, void *codes_t,
                                      void *scales_t, float *tensor_scale, uint32_t *partials,
-                                     const SrArgs *sr, cudaStream_t s);
+                                     const SrArgs *sr, int num_sms, cudaStream_t s);
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
                                   cudaStream_t s);
 

@@ -256,36 +256,36 @@ __device__ __forceinline__ float rcp_rn(float v) {
 // q0 = RN(x * r), the exact residual t = x - q0 * den (one FMA) and
 // q = RN(q0 + t * r) is the correctly rounded quotient x / den (Markstein's
 // correction); den is kept away from overflow and underflow by the caller.
-// The sign of x is then copied onto q, which only matters for x = -0.
+// The steps are taken with -r, which gives -q exactly (rounding to nearest
+// is symmetric), and also the right signed zero: x = +0 gives -0 and x = -0
+// gives +0, where the steps with +r would give +0 for both.  The conversion
+// to E2M1 is symmetric too, so flipping every code's sign bit yields the
+// codes of q.
 __device__ __forceinline__ uint32_t div_to_e2m1x8(const uint32_t *w, float den, float r) {
   uint32_t out;
   asm("{\n"
-      " .reg .b64 rr, nd, x0, x1, x2, x3, q0, q1, q2, q3, t0, t1, t2, t3;\n"
-      " .reg .f32 a0, b0, a1, b1, a2, b2, a3, b3, nden;\n"
+      " .reg .b64 nr, dd, x0, x1, x2, x3, q0, q1, q2, q3, t0, t1, t2, t3;\n"
+      " .reg .f32 a0, b0, a1, b1, a2, b2, a3, b3, rneg;\n"
       " .reg .b8 c0, c1, c2, c3;\n"
-      " neg.f32 nden, %1;\n"
-      " mov.b64 rr, {%2, %2};\n mov.b64 nd, {nden, nden};\n"
+      " .reg .b32 packed;\n"
+      " neg.f32 rneg, %2;\n"
+      " mov.b64 nr, {rneg, rneg};\n mov.b64 dd, {%1, %1};\n"
       " mov.b64 x0, {%3, %4};\n mov.b64 x1, {%5, %6};\n"
       " mov.b64 x2, {%7, %8};\n mov.b64 x3, {%9, %10};\n"
-      " mul.rn.f32x2 q0, x0, rr;\n mul.rn.f32x2 q1, x1, rr;\n"
-      " mul.rn.f32x2 q2, x2, rr;\n mul.rn.f32x2 q3, x3, rr;\n"
-      " fma.rn.f32x2 t0, q0, nd, x0;\n fma.rn.f32x2 t1, q1, nd, x1;\n"
-      " fma.rn.f32x2 t2, q2, nd, x2;\n fma.rn.f32x2 t3, q3, nd, x3;\n"
-      " fma.rn.f32x2 q0, t0, rr, q0;\n fma.rn.f32x2 q1, t1, rr, q1;\n"
-      " fma.rn.f32x2 q2, t2, rr, q2;\n fma.rn.f32x2 q3, t3, rr, q3;\n"
-      // the quotient takes the sign of x (den > 0); the residual step alone
-      // would turn x = -0 into +0
-      " and.b64 t0, x0, 0x8000000080000000;\n or.b64 q0, q0, t0;\n"
-      " and.b64 t1, x1, 0x8000000080000000;\n or.b64 q1, q1, t1;\n"
-      " and.b64 t2, x2, 0x8000000080000000;\n or.b64 q2, q2, t2;\n"
-      " and.b64 t3, x3, 0x8000000080000000;\n or.b64 q3, q3, t3;\n"
+      " mul.rn.f32x2 q0, x0, nr;\n mul.rn.f32x2 q1, x1, nr;\n"
+      " mul.rn.f32x2 q2, x2, nr;\n mul.rn.f32x2 q3, x3, nr;\n"
+      " fma.rn.f32x2 t0, q0, dd, x0;\n fma.rn.f32x2 t1, q1, dd, x1;\n"
+      " fma.rn.f32x2 t2, q2, dd, x2;\n fma.rn.f32x2 t3, q3, dd, x3;\n"
+      " fma.rn.f32x2 q0, t0, nr, q0;\n fma.rn.f32x2 q1, t1, nr, q1;\n"
+      " fma.rn.f32x2 q2, t2, nr, q2;\n fma.rn.f32x2 q3, t3, nr, q3;\n"
       " mov.b64 {a0, b0}, q0;\n mov.b64 {a1, b1}, q1;\n"
       " mov.b64 {a2, b2}, q2;\n mov.b64 {a3, b3}, q3;\n"
       " cvt.rn.satfinite.e2m1x2.f32 c0, b0, a0;\n"
       " cvt.rn.satfinite.e2m1x2.f32 c1, b1, a1;\n"
       " cvt.rn.satfinite.e2m1x2.f32 c2, b2, a2;\n"
       " cvt.rn.satfinite.e2m1x2.f32 c3, b3, a3;\n"
-      " mov.b32 %0, {c0, c1, c2, c3};\n"
+      " mov.b32 packed, {c0, c1, c2, c3};\n"
+      " xor.b32 %0, packed, 0x88888888;\n"
       "}\n"
       : "=r"(out)
       : "f"(den), "f"(r), "f"(__uint_as_float(w[0] << 16)),
@@ -355,33 +355,32 @@ __device__ __forceinline__ float sr_e2m1_value(float q, uint32_t nu) {
 }
 
 // Eight BF16 (four words, element 2i in the low half of word i) divided by
-// den: the correctly rounded quotients with the sign of x (the sequence of
-// div_to_e2m1x8 in packed FP32x2 operations; r == 0 selects the IEEE
-// division).
-__device__ __forceinline__ void quotients8(const uint32_t *w, float den, float r, float *q) {
+// den, negated: -q for the correctly rounded quotients q, with the signed
+// zeros of div_to_e2m1x8 (the sequence there in packed FP32x2 operations;
+// r == 0 selects the IEEE division of -x).
+__device__ __forceinline__ void neg_quotients8(const uint32_t *w, float den, float r, float *nq) {
   if (r == 0.0f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      q[2 * i] = __fdiv_rn(__uint_as_float(w[i] << 16), den);
-      q[2 * i + 1] = __fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), den);
+      nq[2 * i] = __fdiv_rn(-__uint_as_float(w[i] << 16), den);
+      nq[2 * i + 1] = __fdiv_rn(-__uint_as_float(w[i] & 0xFFFF0000u), den);
     }
     return;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     asm("{\n"
-        " .reg .b64 rr, nd, x, q0, t;\n"
-        " .reg .f32 nden;\n"
-        " neg.f32 nden, %2;\n"
-        " mov.b64 rr, {%3, %3};\n mov.b64 nd, {nden, nden};\n"
+        " .reg .b64 nr, dd, x, q0, t;\n"
+        " .reg .f32 rneg;\n"
+        " neg.f32 rneg, %3;\n"
+        " mov.b64 nr, {rneg, rneg};\n mov.b64 dd, {%2, %2};\n"
         " mov.b64 x, {%4, %5};\n"
-        " mul.rn.f32x2 q0, x, rr;\n"
-        " fma.rn.f32x2 t, q0, nd, x;\n"
-        " fma.rn.f32x2 q0, t, rr, q0;\n"
-        " and.b64 t, x, 0x8000000080000000;\n or.b64 q0, q0, t;\n"
+        " mul.rn.f32x2 q0, x, nr;\n"
+        " fma.rn.f32x2 t, q0, dd, x;\n"
+        " fma.rn.f32x2 q0, t, nr, q0;\n"
         " mov.b64 {%0, %1}, q0;\n"
         "}\n"
-        : "=f"(q[2 * i]), "=f"(q[2 * i + 1])
+        : "=f"(nq[2 * i]), "=f"(nq[2 * i + 1])
         : "f"(den), "f"(r), "f"(__uint_as_float(w[i] << 16)),
           "f"(__uint_as_float(w[i] & 0xFFFF0000u)));
   }
@@ -389,18 +388,21 @@ __device__ __forceinline__ void quotients8(const uint32_t *w, float den, float r
 
 // As div_to_e2m1x8 with stochastic rounding: element e (0..7) of the eight
 // uses byte e of the 64 bits (u_lo, u_hi), least significant byte first.
+// The rounding of -q is that of q with the sign flipped (it depends on |q|
+// alone), so it runs on the negated quotients and the sign bits are flipped
+// back in the packed codes.
 __device__ __forceinline__ uint32_t div_to_e2m1x8_sr(const uint32_t *w, float den, float r,
                                                      uint32_t u_lo, uint32_t u_hi) {
-  float q[8];
-  quotients8(w, den, r, q);
+  float nq[8];
+  neg_quotients8(w, den, r, nq);
   const uint32_t n_lo = ~u_lo, n_hi = ~u_hi;
   uint32_t out = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t n = (i < 2 ? n_lo : n_hi) >> (16 * (i & 1));
-    out |= cvt_e2m1x2(sr_e2m1_value(q[2 * i], n), sr_e2m1_value(q[2 * i + 1], n >> 8)) << (8 * i);
+    out |= cvt_e2m1x2(sr_e2m1_value(nq[2 * i], n), sr_e2m1_value(nq[2 * i + 1], n >> 8)) << (8 * i);
   }
-  return out;
+  return out ^ 0x88888888u;
 }
 
 // Per-CTA constants of the NVFP4 rule.
@@ -732,8 +734,8 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_2d_kernel(const __grid_c
 
 // Bidimensional NVFP4 quantize: as mx_quantize_2d_kernel with 16-element
 // blocks along both directions and the NVFP4 rule (each CTA first reduces
-// the tensor's partial maxima to s_t, as pass 2 does).  One CTA owns a 64-row
-// x 256-column tile:
+// the tensor's partial maxima to s_t, as pass 2 does).  A CTA handles one
+// 64-row x 256-column tile at a time:
 //   rowwise     each thread loads four 16-element row blocks (32-byte loads),
 //               quantizes them and parks them in shared memory;
 //   columnwise  after one barrier, each thread reads a column pair of a
@@ -758,20 +760,15 @@ struct Nv2dArgs {
   uint32_t rows_pad, cols_pad;  // rows of x and of x^T with tiled padding
   uint32_t key0, key1;          // Philox key (stochastic rounding)
   int rounds;
+  uint32_t tiles_x, tiles;      // tiles along a row, and in all
 };
 
-template <bool WIDE, int SR>
-__global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __grid_constant__ Nv2dArgs a) {
-  griddep_launch_dependents();
-  griddep_wait();
-  __shared__ __align__(16) uint32_t tile[k2dRows][k2dCols / 2];
-  __shared__ float den_tab[128], rcp_tab[128];
-  const uint32_t r0 = blockIdx.y * k2dRows;
-  const uint32_t c0 = blockIdx.x * k2dCols;
-  constexpr int kPer = k2dRows * (k2dCols / 16) / kThreads;  // row blocks per thread (4)
-  uint32_t w[kPer][8];
+// Loads the row blocks of tile `tile` (zeros outside x).
+template <bool WIDE, int PER>
+__device__ __forceinline__ void nv2d_load_tile(const Nv2dArgs &a, uint32_t tile, uint32_t (&w)[PER][8]) {
+  const uint32_t r0 = tile / a.tiles_x * k2dRows, c0 = tile % a.tiles_x * k2dCols;
 #pragma unroll
-  for (int h = 0; h < kPer; ++h) {
+  for (int h = 0; h < PER; ++h) {
     const uint32_t idx = threadIdx.x + h * kThreads;
     const uint32_t r = r0 + (idx >> 4), j = c0 / 16 + (idx & 15);
     if (r < a.rows && j < a.kb) {
@@ -781,68 +778,90 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __
       for (int i = 0; i < 8; ++i) w[h][i] = 0u;
     }
   }
-  const NvConst c = nv_setup(a.partials, a.tensor_scale, blockIdx.x == 0 && blockIdx.y == 0,
-                             den_tab, rcp_tab);
+}
+
+// Persistent: CTA b takes tiles b, b + grid, ... counted from the last one
+// (the rows that pass 1 read last, the likeliest to be in L2), so that the
+// reduction of the partial maxima and the tables are made once per CTA.
+template <bool WIDE, int SR>
+__global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __grid_constant__ Nv2dArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  __shared__ __align__(16) uint32_t tile[k2dRows][k2dCols / 2];
+  __shared__ float den_tab[128], rcp_tab[128];
+  constexpr int kPer = k2dRows * (k2dCols / 16) / kThreads;  // row blocks per thread (4)
+  uint32_t w[kPer][8];
+  uint32_t t = blockIdx.x;  // the grid has at most a.tiles CTAs
+  nv2d_load_tile<WIDE>(a, a.tiles - 1 - t, w);
+  const NvConst c = nv_setup(a.partials, a.tensor_scale, blockIdx.x == 0, den_tab, rcp_tab);
+  for (;;) {
+    const uint32_t tid = a.tiles - 1 - t;
+    const uint32_t r0 = tid / a.tiles_x * k2dRows, c0 = tid % a.tiles_x * k2dCols;
 #pragma unroll
-  for (int h = 0; h < kPer; ++h) {
-    const uint32_t idx = threadIdx.x + h * kThreads;
-    const uint32_t lr = idx >> 4, lb = idx & 15;  // tile row, 16-column block
-    const uint32_t r = r0 + lr, j = c0 / 16 + lb;
-    const bool inside = r < a.rows && j < a.kb;
-    uint4 *dst = reinterpret_cast<uint4 *>(&tile[lr][lb * 8]);
-    const uint32_t sw = (lb >> 2) & 1u;
-    dst[sw] = make_uint4(w[h][0], w[h][1], w[h][2], w[h][3]);
-    dst[sw ^ 1u] = make_uint4(w[h][4], w[h][5], w[h][6], w[h][7]);
-    if (a.codes == nullptr) continue;  // columnwise only (uniform across the grid)
-    uint32_t sb = 0;
-    if (inside) {
-      uint2 out;
-      sb = nv_block<SR>(w[h], c, den_tab, rcp_tab, j, r, 0u, a.key0, a.key1, a.rounds, out);
-      *reinterpret_cast<uint2 *>(a.codes + static_cast<int64_t>(r) * (a.cols >> 1) + j * 8u) = out;
-    }
-    if (a.tiled) {
-      if (r < a.rows_pad && j < a.katoms * 4u)
-        a.scales[tiled_offset(r, j, a.katoms)] = static_cast<uint8_t>(sb);
-    } else if (inside) {
-      a.scales[static_cast<int64_t>(r) * a.kb + j] = static_cast<uint8_t>(sb);
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const uint32_t unit = threadIdx.x + u * kThreads;
-    const uint32_t cp = unit & 127u;          // column pair of the tile
-    const uint32_t rb = unit >> 7;            // 16-row block of the tile
-    const uint32_t i = r0 / 16 + rb;          // scale column of x^T
-    const uint32_t lb = cp >> 3;              // 16-column block holding the pair
-    const uint32_t chunk = ((cp >> 2) & 1u) ^ ((lb >> 2) & 1u);
-    const uint32_t wsw = lb * 8 + chunk * 4 + (cp & 3u);
-    uint32_t lo[8], hi[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const uint32_t a0 = tile[rb * 16 + 2 * m][wsw];
-      const uint32_t a1 = tile[rb * 16 + 2 * m + 1][wsw];
-      lo[m] = __byte_perm(a0, a1, 0x5410);
-      hi[m] = __byte_perm(a0, a1, 0x7632);
-    }
-#pragma unroll
-    for (int qc = 0; qc < 2; ++qc) {
-      const uint32_t col = c0 + 2 * cp + qc;
-      const bool inside = col < a.cols && i < a.kbt;
+    for (int h = 0; h < kPer; ++h) {
+      const uint32_t idx = threadIdx.x + h * kThreads;
+      const uint32_t lr = idx >> 4, lb = idx & 15;  // tile row, 16-column block
+      const uint32_t r = r0 + lr, j = c0 / 16 + lb;
+      const bool inside = r < a.rows && j < a.kb;
+      uint4 *dst = reinterpret_cast<uint4 *>(&tile[lr][lb * 8]);
+      const uint32_t sw = (lb >> 2) & 1u;
+      dst[sw] = make_uint4(w[h][0], w[h][1], w[h][2], w[h][3]);
+      dst[sw ^ 1u] = make_uint4(w[h][4], w[h][5], w[h][6], w[h][7]);
+      if (a.codes == nullptr) continue;  // columnwise only (uniform across the grid)
       uint32_t sb = 0;
       if (inside) {
         uint2 out;
-        sb = nv_block<SR>(qc ? hi : lo, c, den_tab, rcp_tab, i, col, 1u, a.key0, a.key1, a.rounds,
-                          out);
-        *reinterpret_cast<uint2 *>(a.codes_t + static_cast<int64_t>(col) * (a.rows >> 1) + i * 8u) = out;
+        sb = nv_block<SR>(w[h], c, den_tab, rcp_tab, j, r, 0u, a.key0, a.key1, a.rounds, out);
+        *reinterpret_cast<uint2 *>(a.codes + static_cast<int64_t>(r) * (a.cols >> 1) + j * 8u) = out;
       }
       if (a.tiled) {
-        if (col < a.cols_pad && i < a.katoms_t * 4u)
-          a.scales_t[tiled_offset(col, i, a.katoms_t)] = static_cast<uint8_t>(sb);
+        if (r < a.rows_pad && j < a.katoms * 4u)
+          a.scales[tiled_offset(r, j, a.katoms)] = static_cast<uint8_t>(sb);
       } else if (inside) {
-        a.scales_t[static_cast<int64_t>(col) * a.kbt + i] = static_cast<uint8_t>(sb);
+        a.scales[static_cast<int64_t>(r) * a.kb + j] = static_cast<uint8_t>(sb);
       }
     }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t unit = threadIdx.x + u * kThreads;
+      const uint32_t cp = unit & 127u;          // column pair of the tile
+      const uint32_t rb = unit >> 7;            // 16-row block of the tile
+      const uint32_t i = r0 / 16 + rb;          // scale column of x^T
+      const uint32_t lb = cp >> 3;              // 16-column block holding the pair
+      const uint32_t chunk = ((cp >> 2) & 1u) ^ ((lb >> 2) & 1u);
+      const uint32_t wsw = lb * 8 + chunk * 4 + (cp & 3u);
+      uint32_t lo[8], hi[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint32_t a0 = tile[rb * 16 + 2 * m][wsw];
+        const uint32_t a1 = tile[rb * 16 + 2 * m + 1][wsw];
+        lo[m] = __byte_perm(a0, a1, 0x5410);
+        hi[m] = __byte_perm(a0, a1, 0x7632);
+      }
+#pragma unroll
+      for (int qc = 0; qc < 2; ++qc) {
+        const uint32_t col = c0 + 2 * cp + qc;
+        const bool inside = col < a.cols && i < a.kbt;
+        uint32_t sb = 0;
+        if (inside) {
+          uint2 out;
+          sb = nv_block<SR>(qc ? hi : lo, c, den_tab, rcp_tab, i, col, 1u, a.key0, a.key1, a.rounds,
+                            out);
+          *reinterpret_cast<uint2 *>(a.codes_t + static_cast<int64_t>(col) * (a.rows >> 1) + i * 8u) = out;
+        }
+        if (a.tiled) {
+          if (col < a.cols_pad && i < a.katoms_t * 4u)
+            a.scales_t[tiled_offset(col, i, a.katoms_t)] = static_cast<uint8_t>(sb);
+        } else if (inside) {
+          a.scales_t[static_cast<int64_t>(col) * a.kbt + i] = static_cast<uint8_t>(sb);
+        }
+      }
+    }
+    t += gridDim.x;
+    if (t >= a.tiles) break;
+    __syncthreads();  // every thread has read the tile before it is overwritten
+    nv2d_load_tile<WIDE>(a, a.tiles - 1 - t, w);
   }
 }
 
@@ -967,7 +986,7 @@ cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int
 cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld,
                                      int tiled, void *codes, void *scales, void *codes_t,
                                      void *scales_t, float *tensor_scale, uint32_t *partials,
-                                     const SrArgs *sr, cudaStream_t s) {
+                                     const SrArgs *sr, int num_sms, cudaStream_t s) {
   if (sr && (sr->rounds < 1 || sr->rounds > kPhiloxMaxRounds)) return cudaErrorInvalidValue;
   const bool wide = wide_ok(x, ld);
   // pass 1: the tensor's partial maxima
@@ -1009,14 +1028,19 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
     a.rounds = sr->rounds;
   }
   // the tiles cover the tiled padding of both outputs
-  const uint32_t gx = (a.cols_pad + k2dCols - 1) / k2dCols;
-  const uint32_t gy = (a.rows_pad + k2dRows - 1) / k2dRows;
+  a.tiles_x = (a.cols_pad + k2dCols - 1) / k2dCols;
+  a.tiles = a.tiles_x * ((a.rows_pad + k2dRows - 1) / k2dRows);
+  // stochastic rounding: persistent (its tables are made once per CTA);
+  // round to nearest: one tile per CTA (the next CTA's loads overlap the
+  // tail of the last one's better than a loop's do)
+  const uint32_t resident = static_cast<uint32_t>(num_sms > 0 ? num_sms : 152) * 4u;
+  const uint32_t grid = sr && a.tiles > resident ? resident : a.tiles;
   auto kern = wide ? nvfp4_quantize_2d_kernel<true, 0> : nvfp4_quantize_2d_kernel<false, 0>;
   if (sr && sr->rounds == 10)
     kern = wide ? nvfp4_quantize_2d_kernel<true, 10> : nvfp4_quantize_2d_kernel<false, 10>;
   else if (sr)
     kern = wide ? nvfp4_quantize_2d_kernel<true, -1> : nvfp4_quantize_2d_kernel<false, -1>;
-  e = launch_pdl(kern, dim3(gx, gy), dim3(kThreads), 0, s, a);
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), 0, s, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
