@@ -12,7 +12,8 @@ GEMM.  `value` is 2*M*N*K per step over the device time of the step, in
 TFLOP/s; the GEMM kernel alone and the quantizer's GB/s are reported beside it
 with their roofline fractions.  The quantize-only workloads (quant2d_*: a
 bidimensional MXFP4 quantize; nvfp4_sr_*: an NVFP4 quantize with stochastic
-rounding; nvfp4_quant2d_sr_*: both) have no GEMM and report GB/s of algorithmic bytes instead.
+rounding; nvfp4_quant2d_sr_*: both; nvfp4_quant2d_*: bidimensional NVFP4 with
+rounding to nearest) have no GEMM and report GB/s of algorithmic bytes instead.
 
 Timing: inputs are resident in HBM; the K steps are replayed from CUDA graphs
 (each holding one step per rotating input set) between two CUDA events on the

@@ -63,7 +63,8 @@ def scale_bytes(rows: int, kb: int, lo: int, hi: int, seed: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# The five workloads of the block-scaled GEMM (sizes and distributions).
+# The workloads of the block-scaled GEMM and its quantizers (sizes and
+# distributions).
 # --------------------------------------------------------------------------
 
 WORKLOADS = {
@@ -98,6 +99,9 @@ WORKLOADS = {
     # columnwise outputs) of the same tensor: no GEMM, HBM bound.
     "nvfp4_quant2d_sr_16384x8192": dict(kind="quant2d", fmt="nvfp4", sr=True, m=16384, n=0,
                                         k=8192, sigma_a=1e-3, out="codes", split_k=1),
+    # The same bidimensional NVFP4 quantize with rounding to nearest.
+    "nvfp4_quant2d_16384x8192": dict(kind="quant2d", fmt="nvfp4", sr=False, m=16384, n=0,
+                                     k=8192, sigma_a=1e-3, out="codes", split_k=1),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
