@@ -628,8 +628,9 @@ def kernel_source_hash(call):
 
 
 def recorded_traffic(name, call):
-    """DRAM bytes per launch from the committed ncu summary, if its kernels
-    have not changed since the counters were taken."""
+    """DRAM bytes per call (one launch, or the two of an NVFP4 quantize) from
+    the committed ncu summary, if its kernels have not changed since the
+    counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path) or call not in CALL_SOURCES:
         return None
