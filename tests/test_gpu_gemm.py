@@ -112,6 +112,32 @@ def test_mxfp4_explicit_split_k(split_k, m, n, k):
     _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=True, split_k=split_k)
 
 
+@pytest.mark.parametrize("m,n,k,split_k", [(32, 256, 4096, 16), (64, 20480, 512, 2)])
+def test_split_k_many_splits_and_many_tiles(m, n, k, split_k):
+    """Split-K of the single-CTA kernel with 16 splits of one stage each, and
+    with more tiles (160) than CTAs, so that a CTA takes several (tile,
+    split) units in turn."""
+    a, sa, b, sb = _codes_case(m, n, k, seed=79 + split_k)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=False, split_k=split_k)
+    _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32=True, split_k=split_k)
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_split_k_tiles_do_not_depend_on_n(out_fp32):
+    """The first two 128-column tiles of a 160-tile split-K GEMM (CTAs take
+    several units in turn) equal, bit for bit, the same GEMM with N = 256
+    (one unit per CTA): same splits, same order of the additions."""
+    m, n, k = 32, 20480, 1024
+    a, sa, b, sb = _codes_case(m, n, k, seed=81)
+    big = gpu_gemm(MX, a, oracle.scale_tile(sa), b, oracle.scale_tile(sb), m, n, k, out_fp32,
+                   split_k=2)
+    small = gpu_gemm(MX, a, oracle.scale_tile(sa), b[:256], oracle.scale_tile(sb[:256]), m, 256, k,
+                     out_fp32, split_k=2)
+    assert np.array_equal(big[:, :256], small)
+    ref, s_abs = oracle.mx_gemm(a, sa, b[:256], sb[:256], m, 256, k)
+    (check_fp32 if out_fp32 else check_bf16)(small, ref, s_abs, "split 2, N = 256")
+
+
 def test_single_cta_wide_tile_path():
     """M <= 128 with N wide enough for the single-CTA 256-column tile."""
     m, n, k = 96, 78848, 256

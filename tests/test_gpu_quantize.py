@@ -441,6 +441,17 @@ def test_nvfp4_quantize_2d_full_size():
     _check_nv2d(x, TILED)
 
 
+def test_nvfp4_quantize_2d_more_tiles_than_resident_ctas():
+    """With stochastic rounding the kernel is persistent (4 CTAs per SM, each
+    taking every grid-th 64 x 256 tile): 701 tiles of a narrow tensor, the last
+    one ragged (16 of its 64 rows), so that some CTAs take two tiles."""
+    x = synth.bf16_normal(64 * 700 + 16, 32, 1.0, seed=54)
+    x[-16:, :16] = 0                                  # a zero block in the ragged tile
+    for layout in (PLAIN, TILED):
+        _check_nv2d(x, layout, seed=0x5EED)
+    _check_nv2d(x, TILED)
+
+
 def test_nvfp4_quantize_2d_columnwise_only():
     x = synth.bf16_normal(192, 320, 1.0, seed=53)
     for seed in (None, 17):
