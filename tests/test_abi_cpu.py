@@ -265,3 +265,14 @@ def test_no_gpu_reports_unavailable(lib):
     # a well-formed call fails at the device check, not silently
     rc = _gemm(lib)
     assert rc in (mx.MX_ERR_CUDA, mx.MX_ERR_UNSUPPORTED_ARCH)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises: there is no fallback path."""
+    from block_scaled_fp4_bf16_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "libmxfp4.so"))
+    with pytest.raises(RuntimeError, match="is missing"):
+        _binding.mx_scale_bytes(128, 256, mx.MX_FMT_MXFP4, mx.MX_SCALE_TCGEN05)
+    with pytest.raises(RuntimeError, match="is missing"):
+        _binding.mx_available()
