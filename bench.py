@@ -42,6 +42,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -532,11 +533,19 @@ def time_e2e(wl, host_inputs, steps):
 # --------------------------------------------------------------------- CPU oracle
 
 def oracle_step_sample(name, host, frac, prepared):
-    """Run the CPU oracle on the fraction `frac` of one step; returns seconds."""
+    """Run the CPU oracle on the fraction `frac` of one step; returns (seconds,
+    the fraction actually run).  Quantize-only steps take the first rows of
+    the tensor.  GEMM steps take a sqrt(frac) M x sqrt(frac) N block of D
+    (every output of it over the whole K) and quantize the matching share
+    (frac) of the rows of A and of B, so that each part of the step is cut
+    by the same factor."""
     import oracle
     w, m, n, k = workload_shape(name)
     mr = max(1, int(round(m * frac)))
     nr = max(1, int(round(n * frac)))
+    g = math.sqrt(frac)
+    dm = max(1, min(m, int(round(m * g))))     # output rows of the block
+    dn = max(1, min(n, int(round(n * g))))     # output columns of the block
     t0 = time.perf_counter()
     if w["kind"] == "quant2d":
         mr = max(32, mr // 32 * 32)
@@ -548,23 +557,26 @@ def oracle_step_sample(name, host, frac, prepared):
     if w["kind"] == "quant_sr":
         oracle.nvfp4_quantize_sr(host["a"][:mr], SR_SEED, 10)
         return time.perf_counter() - t0, mr / m
+    rows, cols = np.arange(dm), np.arange(dn)
     if w["kind"] == "bf16":
         if w["fmt"] == "mxfp4":
             oracle.mx_quantize(host["a"][:mr])
             oracle.mx_quantize(host["b"][:nr])
             qa, sa, qb, sb = prepared
-            d = oracle.mx_gemm(qa, sa, qb, sb, m, n, k, rows=np.arange(mr))[0]
+            d = oracle.mx_gemm(qa, sa, qb, sb, m, n, k, rows=rows, cols=cols)[0]
             if w.get("bias") or w.get("gelu"):
-                oracle.gemm_epilogue(d, bias=host.get("bias"), gelu_on=bool(w.get("gelu")))
+                bias = host.get("bias")
+                oracle.gemm_epilogue(d, bias=None if bias is None else bias[:dn],
+                                     gelu_on=bool(w.get("gelu")))
         else:
             oracle.nvfp4_quantize(host["a"][:mr])
             oracle.nvfp4_quantize(host["b"][:nr])
             qa, sa, ta, qb, sb, tb = prepared
-            oracle.nvfp4_gemm(qa, sa, qb, sb, m, n, k, ta, tb, rows=np.arange(mr))
+            oracle.nvfp4_gemm(qa, sa, qb, sb, m, n, k, ta, tb, rows=rows, cols=cols)
     else:
         oracle.mx_gemm(host["a_codes"], host["a_scales"], host["b_codes"], host["b_scales"],
-                       m, n, k, rows=np.arange(mr))
-    return time.perf_counter() - t0, mr / m
+                       m, n, k, rows=rows, cols=cols)
+    return time.perf_counter() - t0, dm * dn / (m * n)
 
 
 def oracle_prepare(name, host):
@@ -602,8 +614,14 @@ def cpu_baseline(name, host, target_s):
                           f"{t:.1f} s on the host CPU"}
     value = 2.0 * m * n * k * f / t / 1e12
     return {"value": value, "unit": "TFLOPS", "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} output rows with "
-                      f"the matching share of the quantize work), {t:.1f} s on the host CPU"}
+            "sample": f"{f:.5f} of one step ({gemm_block(f, m, n)} with the matching share of "
+                      f"the quantize work), {t:.1f} s on the host CPU"}
+
+
+def gemm_block(f, m, n):
+    """The output block a GEMM sample of fraction f covers, in words."""
+    g = math.sqrt(f)
+    return f"a {int(round(m * g))} x {int(round(n * g))} block of the {m} x {n} output"
 
 
 # --------------------------------------------------------------------- traffic record
@@ -787,7 +805,9 @@ def main_reference(args):
     prepared = oracle_prepare(name, host)
     pilot, f0 = oracle_step_sample(name, host, 1.0 / 256, prepared)
     budget = 150.0 / (args.steps + args.warmup)      # seconds per step
-    frac = min(1.0, max(1.0 / m, f0 * budget / max(pilot, 1e-6)))
+    kind = synth.WORKLOADS[name]["kind"]
+    smallest = 1.0 / m if kind in QUANT_KINDS else 1.0 / (m * n)   # one row / one output
+    frac = min(1.0, max(smallest, f0 * budget / max(pilot, 1e-6)))
     for _ in range(args.warmup):
         oracle_step_sample(name, host, frac, prepared)
     times, f = [], frac
@@ -795,13 +815,13 @@ def main_reference(args):
         t, f = oracle_step_sample(name, host, frac, prepared)
         times.append(t)
     mean_t = statistics.fmean(times)
-    kind = synth.WORKLOADS[name]["kind"]
     quant_only = kind in QUANT_KINDS
     unit = "GB/s" if quant_only else "TFLOPS"
     value = (quant_step_bytes(synth.WORKLOADS[name], m, k) * f / mean_t / 1e9 if quant_only
              else 2.0 * m * n * k * f / mean_t / 1e12)
-    sample = (f"{f:.5f} of one step per step ({int(round(f * m))} of {m} output rows with the "
-              f"matching share of the quantize work)")
+    sample = (f"{f:.6f} of one step per step ({int(round(f * m))} of {m} rows)" if quant_only
+              else f"{f:.6f} of one step per step ({gemm_block(f, m, n)} with the matching "
+                   f"share of the quantize work)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
