@@ -121,17 +121,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // EPI: 0 compiles the plain epilogue; 1 applies the epilogue terms of p.epi
-// (never with split-K partials) with 8 epilogue warps (a bias only); 2 the
-// same with 16 epilogue warps (GELU or beta * C, whose per-output work needs
-// them).
+// (never with split-K partials) with 8 epilogue warps (a bias only); 2 and 3
+// the same with 16 epilogue warps, whose per-output work needs them: 2 for
+// beta * C (and a bias) and compiled without the GELU code, 3 with GELU.
 template <int FMT, int OUT_F32, int EPI>
-__global__ void __launch_bounds__(PairCfg<FMT, EPI == 2 ? 16 : 8>::kThreads, 1)
+__global__ void __launch_bounds__(PairCfg<FMT, EPI >= 2 ? 16 : 8>::kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_sfa,
                      const __grid_constant__ CUtensorMap tmap_sfb,
                      const __grid_constant__ CUtensorMap tmap_d, const PairParams p) {
-  using C = PairCfg<FMT, EPI == 2 ? 16 : 8>;
+  using C = PairCfg<FMT, EPI >= 2 ? 16 : 8>;
   constexpr int kBoxCols = OUT_F32 ? 16 : 32;
   constexpr int kBoxes = C::kWarpCols / kBoxCols;  // per epilogue warp and tile
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -389,8 +389,8 @@ __global__ void __launch_bounds__(PairCfg<FMT, EPI == 2 ? 16 : 8>::kThreads, 1)
                 const int cc = c * 16 + 4 * i + j;  // column within the warp's columns
                 bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc % kBiasPerLane], cc / kBiasPerLane);
               }
-              epilogue_terms<4, 1>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 4 * i,
-                                   bv);
+              epilogue_terms<4, 1, EPI == 3>(
+                  f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 4 * i, bv);
             }
             v[i] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                               __float_as_uint(f[3]));
@@ -411,8 +411,8 @@ __global__ void __launch_bounds__(PairCfg<FMT, EPI == 2 ? 16 : 8>::kThreads, 1)
                 const int cc = c * 32 + 8 * i + j;  // column within the warp's columns
                 bv[j] = __shfl_sync(0xFFFFFFFFu, bias_l[cc % kBiasPerLane], cc / kBiasPerLane);
               }
-              epilogue_terms<8, 0>(f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 8 * i,
-                                   bv);
+              epilogue_terms<8, 0, EPI == 3>(
+                  f, p.epi, static_cast<int64_t>(row0 + lane) * p.n + col0 + 8 * i, bv);
             }
             v[i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(PairCfg<FMT, EPI == 2 ? 16 : 8>::kThreads, 1)
 
 template <int FMT, int OUT_F32, int EPI>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
-  using C = PairCfg<FMT, EPI == 2 ? 16 : 8>;
+  using C = PairCfg<FMT, EPI >= 2 ? 16 : 8>;
   auto kernel = gemm_pair_kernel<FMT, OUT_F32, EPI>;
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
@@ -510,18 +510,23 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 cudaError_t launch_gemm_pair(const GemmArgs &g, cudaStream_t s) {
   const bool f32 = g.out_fp32 || g.split_k > 1;
   // with split-K the reduction applies the epilogue terms; GELU and beta * C
-  // take the 16-warp epilogue, a bias alone the 8-warp one
-  const int epi = g.split_k != 1 ? 0 : (g.epi.gelu || g.epi.c) ? 2 : g.epi.bias ? 1 : 0;
+  // take the 16-warp epilogue (GELU in its own instance, so that the others
+  // compile without it), a bias alone the 8-warp one
+  const int epi = g.split_k != 1 ? 0 : g.epi.gelu ? 3 : g.epi.c ? 2 : g.epi.bias ? 1 : 0;
   cudaError_t e;
   if (g.fmt == 0) {
-    if (epi == 2)
+    if (epi == 3)
+      e = f32 ? launch_typed<0, 1, 3>(g, s) : launch_typed<0, 0, 3>(g, s);
+    else if (epi == 2)
       e = f32 ? launch_typed<0, 1, 2>(g, s) : launch_typed<0, 0, 2>(g, s);
     else if (epi == 1)
       e = f32 ? launch_typed<0, 1, 1>(g, s) : launch_typed<0, 0, 1>(g, s);
     else
       e = f32 ? launch_typed<0, 1, 0>(g, s) : launch_typed<0, 0, 0>(g, s);
   } else {
-    if (epi == 2)
+    if (epi == 3)
+      e = f32 ? launch_typed<1, 1, 3>(g, s) : launch_typed<1, 0, 3>(g, s);
+    else if (epi == 2)
       e = f32 ? launch_typed<1, 1, 2>(g, s) : launch_typed<1, 0, 2>(g, s);
     else if (epi == 1)
       e = f32 ? launch_typed<1, 1, 1>(g, s) : launch_typed<1, 0, 1>(g, s);

@@ -432,6 +432,26 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   return out;
 }
 
+// Packed binary32 pairs (one FFMA2 / FMUL2 issue for two values; each lane
+// is the IEEE operation of the scalar form, so results are identical).
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // GELU(y) = y Phi(y), Phi the standard normal CDF.  For a = |y|,
 // Phi(-a) = erfc(z) / 2 with z = a / sqrt 2, and erfc comes from the Chebyshev
 // fit of Numerical Recipes (Press, Teukolsky, Vetterling, Flannery, 2nd ed.,
@@ -443,35 +463,43 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 // Relative error below 2^-24 (y^2 / 2 + 40): the fit, CUDA's expf (2 ulp)
 // and __fdividef (2 ulp), the Horner rounding and the argument's rounding,
 // which grows with its magnitude y^2 / 2.  One MUFU reciprocal and one
-// exponential per value.
-__device__ __forceinline__ float gelu_f32(float y) {
-  const float a = fabsf(y);
-  const float z = __fmul_rn(a, 0.70710678118654752f);
-  const float t = __fdividef(1.0f, __fmaf_rn(0.5f, z, 1.0f));
-  float p = 0.17087277f;
-  p = __fmaf_rn(p, t, -0.82215223f);
-  p = __fmaf_rn(p, t, 1.48851587f);
-  p = __fmaf_rn(p, t, -1.13520398f);
-  p = __fmaf_rn(p, t, 0.27886807f);
-  p = __fmaf_rn(p, t, -0.18628806f);
-  p = __fmaf_rn(p, t, 0.09678418f);
-  p = __fmaf_rn(p, t, 0.37409196f);
-  p = __fmaf_rn(p, t, 1.00002368f);
-  p = __fmaf_rn(p, t, -1.26551223f);
-  const float h = __fmul_rn(a, a);
-  const float l = __fmaf_rn(a, a, -h);
-  const float arg = __fmaf_rn(-0.5f, h, __fmaf_rn(-0.5f, l, p));
-  const float phi = __fmul_rn(__fmul_rn(0.5f, t), expf(arg));  // Phi(-|y|)
-  const float yp = __fmul_rn(y, phi);
-  return y > 0.0f ? __fsub_rn(y, yp) : yp;
+// exponential per value.  Two values at a time: their multiplies and FMAs
+// are packed pairs; the reciprocal, the exponential and the final select
+// stay per value.
+__device__ __forceinline__ float2 gelu_f32x2(float2 y) {
+  const auto two = [](float v) { return make_float2(v, v); };
+  const float2 a = make_float2(fabsf(y.x), fabsf(y.y));
+  const float2 z = mul_f32x2(a, two(0.70710678118654752f));
+  const float2 den = fma_f32x2(two(0.5f), z, two(1.0f));
+  const float2 t = make_float2(__fdividef(1.0f, den.x), __fdividef(1.0f, den.y));
+  float2 p = two(0.17087277f);
+  p = fma_f32x2(p, t, two(-0.82215223f));
+  p = fma_f32x2(p, t, two(1.48851587f));
+  p = fma_f32x2(p, t, two(-1.13520398f));
+  p = fma_f32x2(p, t, two(0.27886807f));
+  p = fma_f32x2(p, t, two(-0.18628806f));
+  p = fma_f32x2(p, t, two(0.09678418f));
+  p = fma_f32x2(p, t, two(0.37409196f));
+  p = fma_f32x2(p, t, two(1.00002368f));
+  p = fma_f32x2(p, t, two(-1.26551223f));
+  const float2 h = mul_f32x2(a, a);
+  const float2 l = fma_f32x2(a, a, make_float2(-h.x, -h.y));
+  const float2 arg = fma_f32x2(two(-0.5f), h, fma_f32x2(two(-0.5f), l, p));
+  const float2 ex = make_float2(expf(arg.x), expf(arg.y));
+  const float2 phi = mul_f32x2(mul_f32x2(two(0.5f), t), ex);  // Phi(-|y|)
+  const float2 yp = mul_f32x2(y, phi);
+  return make_float2(y.x > 0.0f ? __fsub_rn(y.x, yp.x) : yp.x,
+                     y.y > 0.0f ? __fsub_rn(y.y, yp.y) : yp.y);
 }
 
 // GEMM epilogue of N consecutive outputs of one row (N = 4 or 8; idx = the
 // flat index row * n + col of the first): f = act(f + beta * C + bias), each
 // term only when present (C in the output dtype: FP32 when OUT_F32, else
 // BF16; bv: the N bias values, null when e.bias is null), act = GELU when
-// e.gelu.  Every step but GELU (gelu_f32) is one binary32 operation.
-template <int N, int OUT_F32>
+// e.gelu.  Every step but GELU (gelu_f32x2) is one binary32 operation.  GELU
+// false compiles without the GELU code (for kernel instances that never see
+// e.gelu set, whose other terms then keep their registers).
+template <int N, int OUT_F32, bool GELU = true>
 __device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int64_t idx,
                                                const float *bv) {
   static_assert(N == 4 || N == 8, "groups of 4 or 8 outputs");
@@ -504,9 +532,13 @@ __device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int
 #pragma unroll
     for (int j = 0; j < N; ++j) f[j] = __fadd_rn(f[j], bv[j]);
   }
-  if (e.gelu) {
+  if (GELU && e.gelu) {
 #pragma unroll
-    for (int j = 0; j < N; ++j) f[j] = gelu_f32(f[j]);
+    for (int j = 0; j < N; j += 2) {
+      const float2 g = gelu_f32x2(make_float2(f[j], f[j + 1]));
+      f[j] = g.x;
+      f[j + 1] = g.y;
+    }
   }
 }
 
