@@ -276,3 +276,19 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         _binding.mx_scale_bytes(128, 256, mx.MX_FMT_MXFP4, mx.MX_SCALE_TCGEN05)
     with pytest.raises(RuntimeError, match="is missing"):
         _binding.mx_available()
+
+
+def test_static_workspace_rejects_oversized_partials_before_any_launch(lib):
+    """Split-K partials beyond the fixed array (split_k * M * N * 4 bytes over
+    MX_STATIC_WORKSPACE_BYTES) are refused with MX_ERR_WORKSPACE, and invalid
+    arguments with the codes of mxfp4_gemm; no device is touched for either."""
+    m, n, k = 128, 8192, 8192
+    split = 8
+    assert mx.mx_gemm_workspace_bytes(m, n, k, split) == split * m * n * 4
+    assert split * m * n * 4 > mx.MX_STATIC_WORKSPACE_BYTES
+    rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, m, n, k, 0, 0, split, None)
+    assert rc == mx.MX_ERR_WORKSPACE
+    rc = lib.mxfp4_gemm_static_workspace(None, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, 0, 0, 1, None)
+    assert rc == mx.MX_ERR_INVALID_ARG
+    rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 128, 0, 0, 1, None)
+    assert rc == mx.MX_ERR_UNSUPPORTED_SHAPE
