@@ -5,12 +5,16 @@
                     [--workload NAME]
 
 A step is one pass of the whole hot path over one batch of synthetic input.
-For the default workload (BF16 activations 2048x4096 and weights 4096x4096,
-quantized to MXFP4 and multiplied, BF16 out) a step is: one grouped quantize
-of A and W (scales written straight into the tcgen05 tile order), then the
-GEMM.  `value` is 2*M*N*K per step over the device time of the step, in
-TFLOP/s; the GEMM kernel alone and the quantizer's GB/s are reported beside it
-with their roofline fractions.  The quantize-only workloads (quant2d_*: a
+For the default workload, the LLM MLP up-projection (BF16 activations
+16384x8192 ~N(0,1) and weights 28672x8192 ~N(0,0.015), quantized to MXFP4 and
+multiplied, BF16 out), a step is: one grouped quantize of A and W (scales
+written straight into the tcgen05 tile order), then the GEMM.  `value` is
+2*M*N*K per step over the device time of the step, in TFLOP/s; the GEMM
+kernel alone and the quantizer's GB/s are reported beside it with their
+roofline fractions: against the measured burst bf16 rate times the nominal
+FP4:BF16 ratio, and, per clock, against the FP4 MMA rate this GPU is
+calibrated at in the same run (mx_calibrate_mma) at the SM clock sampled
+while the kernel ran.  The quantize-only workloads (quant2d_*: a
 bidimensional MXFP4 quantize; nvfp4_sr_*: an NVFP4 quantize with stochastic
 rounding; nvfp4_quant2d_sr_*: both; nvfp4_quant2d_*: bidimensional NVFP4 with
 rounding to nearest) have no GEMM and report GB/s of algorithmic bytes instead.
@@ -59,7 +63,7 @@ import numpy as np  # noqa: E402
 
 from block_scaled_fp4_bf16_gb300 import synth  # noqa: E402
 
-DEFAULT_WORKLOAD = "quant_gemm_2048x4096x4096"
+DEFAULT_WORKLOAD = "mlp_up_16384x28672x8192"
 METRIC = "MXFP4 GEMM TFLOPS and % of GB300 dense FP4 peak; quantize GB/s vs HBM"
 
 # Steps that are a quantize alone (no GEMM): their metric is algorithmic GB/s.
@@ -434,23 +438,37 @@ def run_graph_region(wl, graphs, stream, start, end, steps, barrier):
     return start.elapsed_time(end), t0, t1
 
 
-def time_calls(wl, steps, per_graph=40):
+def time_calls(wl, steps, per_graph=40, windows=None, min_seconds=1.5):
     """Per-call device durations: for each C-ABI call of the step, a CUDA graph of
     `per_graph` back-to-back calls over the rotating sets, replayed between two
-    events on the launching stream (no host gaps); returns ms per call."""
+    events on the launching stream (no host gaps); returns ms per call.
+    windows (dict, optional) receives each call's (t0, t1) host-time window, for
+    the clock samples taken while it ran; each call is then replayed for at
+    least min_seconds, so that the window holds a dozen or more samples and the
+    clock has settled under the power limit."""
     torch = wl.torch
     stream = torch.cuda.Stream()
     out = {}
-    reps = max(2, steps // per_graph)
     for label, fn in wl.calls():
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             h = torch.cuda.current_stream().cuda_stream
             for i in range(per_graph):
                 fn(wl.sets[i % len(wl.sets)], h)
+        reps = max(2, steps // per_graph)
         with torch.cuda.stream(stream):
+            w0 = torch.cuda.Event(enable_timing=True)
+            w1 = torch.cuda.Event(enable_timing=True)
+            w0.record(stream)
             g.replay()
             g.replay()
+            w1.record(stream)
+        torch.cuda.synchronize()
+        if windows is not None:
+            per_replay = max(w0.elapsed_time(w1) * 1e-3 / 2, 1e-6)
+            reps = max(reps, int(math.ceil(min_seconds / per_replay)))
+        t0 = time.time()
+        with torch.cuda.stream(stream):
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
             start.record(stream)
@@ -458,6 +476,8 @@ def time_calls(wl, steps, per_graph=40):
                 g.replay()
             end.record(stream)
         torch.cuda.synchronize()
+        if windows is not None:
+            windows[label] = (t0, time.time())
         out[label] = start.elapsed_time(end) / (reps * per_graph)
         del g
     return out
@@ -663,6 +683,36 @@ def recorded_traffic(name, call):
     return None
 
 
+# --------------------------------------------------------------------- MMA ceiling
+
+def mma_ceiling(mx, torch, steps=1 << 15):
+    """Live calibration of the tensor pipe (mx_calibrate_mma): one wave of
+    back-to-back CTA-pair MMAs of the pair GEMM's form and shape per SM pair.
+    Returns its FLOPs per clock per SM (cycle counts of every pair, so it does
+    not depend on the clock), the TFLOP/s and the clock it ran at."""
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    cyc = torch.zeros(nsm, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.current_stream()
+    mx.mx_calibrate_mma(mx.MX_MMA_MXF4, 1, 256, cyc)          # warm-up
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    flops, units = mx.mx_calibrate_mma(mx.MX_MMA_MXF4, 1, steps, cyc)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if mx.mx_device_status() != mx.MX_OK:
+        return None
+    secs = e0.elapsed_time(e1) * 1e-3
+    cycles = statistics.median(cyc[:units].cpu().tolist())
+    mmas = 4 * steps
+    per_sm_flop = 2.0 * 128 * 256 * 64          # each SM's half of a 256x256x64 pair MMA
+    return {"form": "kind::mxf4 block_scale scale_vec::2X, cta_group::2, 256x256x64",
+            "cycles_per_mma": cycles / mmas,
+            "flop_per_clk_sm": per_sm_flop * mmas / cycles,
+            "tflops": flops / secs / 1e12, "mhz": cycles / secs / 1e6, "sms": nsm}
+
+
 # --------------------------------------------------------------------- main (ours)
 
 def main_ours(args):
@@ -709,18 +759,23 @@ def main_ours(args):
             graphs[0].replay()
     torch.cuda.synchronize()
     ms, t0, t1 = run_graph_region(wl, graphs, stream, ev0, ev1, args.steps, barrier)
+    ms_per_step = reduce_max(ms / args.steps, world, "cuda")
+
+    windows = {}
+    per_call = time_calls(wl, args.steps, windows=windows)
     time.sleep(0.3)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    ms_per_step = reduce_max(ms / args.steps, world, "cuda")
-
-    per_call = time_calls(wl, args.steps)
+    call_clocks = {c: sampler.summary(*w) for c, w in windows.items()}
+    ceiling = mma_ceiling(mx, torch)
     e2e_steps = args.e2e_steps or min(args.steps, 200)
     e2e_ms, h2d, d2h = time_e2e(wl, host, e2e_steps)
     e2e_ms = reduce_max(e2e_ms, world, "cuda")
 
     peaks, peak_src = load_peaks()
-    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    # every kernel is timed on its own (back-to-back calls of that kernel): the
+    # burst bf16 figure is the one that applies, times the nominal FP4 ratio
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     hbm_peak = peaks["hbm_gbs"]
     flops = 2.0 * m * n * k
     quant_only = wl.kind in QUANT_KINDS
@@ -745,14 +800,31 @@ def main_ours(args):
         kernels[label]["frac"] = kernels[label]["achieved"] / kernels[label]["peak"]
         kernels[label]["algorithmic_bytes"] = b
         kernels[label]["algorithmic_flops"] = f
+        cc = call_clocks.get(label) or {}
+        kernels[label]["sm_mhz"] = cc.get("sm_mhz")
+        kernels[label]["clock_samples"] = cc.get("samples", 0)
+        if f > 0 and ceiling and cc.get("sm_mhz"):
+            # FLOPs per clock per SM at the clock the kernel ran at, against the
+            # calibrated MMA rate: the tensor-pipe efficiency, independent of
+            # the power cap's clock
+            fpc = f / t_s / (ceiling["sms"] * cc["sm_mhz"] * 1e6)
+            kernels[label]["flop_per_clk_sm"] = fpc
+            kernels[label]["frac_of_mma_ceiling_per_clock"] = fpc / ceiling["flop_per_clk_sm"]
     dom = max(per_call, key=lambda c: per_call[c])
     kd = kernels[dom]
     traffic = recorded_traffic(name, dom)
     roofline = {"bound": kd["bound"], "achieved": kd["achieved"], "peak": kd["peak"],
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": traffic, "kernel": dom,
-                "peak_source": (f"{peak_src} " + ("bf16_tflops_sustained x 6 (nominal FP4:BF16 "
-                                                  "dense ratio)" if kd["bound"] == "tensor"
-                                                  else "hbm_gbs"))}
+                "peak_source": (f"{peak_src} " + ("bf16_tflops (burst) x 6 (nominal FP4:BF16 "
+                                                  "dense ratio); the kernel is timed on its own"
+                                                  if kd["bound"] == "tensor" else "hbm_gbs"))}
+    if kd["bound"] == "tensor":
+        roofline["peak_sustained"] = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+        roofline["frac_of_sustained"] = kd["achieved"] / roofline["peak_sustained"]
+        if ceiling:
+            roofline["mma_ceiling"] = ceiling
+            roofline["sm_mhz"] = kd.get("sm_mhz")
+            roofline["frac_of_mma_ceiling_per_clock"] = kd.get("frac_of_mma_ceiling_per_clock")
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -36,6 +36,10 @@ MX_OUT_FP32 = 1
 MX_STATIC_WORKSPACE_BYTES = 16 << 20
 MX_QUANTIZE_GROUP_MAX = 8
 MX_PHILOX_MAX_ROUNDS = 16
+MX_MMA_MXF4 = 0
+MX_MMA_MXF4NVF4_2X = 1
+MX_MMA_MXF4NVF4_4X = 2
+MX_CALIBRATE_MAX_STEPS = 1 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -54,9 +58,11 @@ class mx_gemm_epilogue(ctypes.Structure):
 
 
 class MXError(RuntimeError):
-    def __init__(self, fn: str, code: int):
+    def __init__(self, fn: str, code: int, detail: str = ""):
         self.code = code
-        super().__init__(f"{fn} failed: {code} ({mx_error_string(code)})")
+        self.detail = detail
+        super().__init__(f"{fn} failed: {code} ({mx_error_string(code)})"
+                         + (f": {detail}" if detail else ""))
 
 
 def lib() -> ctypes.CDLL:
@@ -73,6 +79,8 @@ def lib() -> ctypes.CDLL:
         i64, vp, sz, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
         L.mx_error_string.restype = ctypes.c_char_p
         L.mx_error_string.argtypes = [i32]
+        L.mx_last_error_string.restype = ctypes.c_char_p
+        L.mx_last_error_string.argtypes = []
         L.mx_available.restype = i32
         L.mx_available.argtypes = []
         L.mx_scale_bytes.restype = sz
@@ -116,6 +124,9 @@ def lib() -> ctypes.CDLL:
         L.mx_device_status.argtypes = [vp]
         L.mx_selftest_wait_timeout.restype = i32
         L.mx_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.mx_calibrate_mma.restype = i32
+        L.mx_calibrate_mma.argtypes = [i32, i32, i64, vp, i32, ctypes.POINTER(ctypes.c_double),
+                                       ctypes.POINTER(i32), vp]
         _lib = L
         return L
 
@@ -146,12 +157,17 @@ def _stream(stream):
 
 def _check(fn: str, rc: int) -> int:
     if rc != MX_OK:
-        raise MXError(fn, rc)
+        raise MXError(fn, rc, mx_last_error_string())
     return rc
 
 
 def mx_error_string(code: int) -> str:
     return lib().mx_error_string(code).decode()
+
+
+def mx_last_error_string() -> str:
+    """Detail of the last rejection or failure of a call on this thread."""
+    return lib().mx_last_error_string().decode()
 
 
 def mx_available() -> bool:
@@ -296,3 +312,15 @@ def mx_device_status(stream=None) -> int:
 def mx_selftest_wait_timeout(timeout_ns: int, stream=None):
     return _check("mx_selftest_wait_timeout",
                   lib().mx_selftest_wait_timeout(timeout_ns, _stream(stream)))
+
+
+def mx_calibrate_mma(form: int, pair: int, steps: int, cycles=None, stream=None):
+    """Launch one calibration wave of block-scaled MMAs; returns (flops, units).
+    cycles: None or a device tensor of >= SM-count int64 entries."""
+    flops = ctypes.c_double(0.0)
+    units = ctypes.c_int(0)
+    cap = cycles.numel() if cycles is not None else 0
+    _check("mx_calibrate_mma", lib().mx_calibrate_mma(
+        form, pair, steps, _ptr(cycles), cap, ctypes.byref(flops), ctypes.byref(units),
+        _stream(stream)))
+    return flops.value, units.value

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmxfp4.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "static_ws.cu", "calibrate.cu"]
 HEADERS = ["mx_device.cuh", "mx_internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -129,6 +129,22 @@ int gemm_out_box_cols(int out_fp32, int split_k);
 
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t timeout_ns, cudaStream_t s);
 
+// Device address, in the current context, of the fixed split-K array of
+// mxfp4_gemm_static_workspace (static_ws.cu).
+cudaError_t static_workspace_symbol(void **out);
+
+// mxfp4_gemm_static_workspace: the checks of mxfp4_gemm, the size check
+// against the fixed array, then the GEMM with that array as its workspace
+// (api.cu, where the per-context device addresses live).
+int gemm_static_workspace_call(const void *a_codes, const void *a_scales, const void *b_codes,
+                               const void *b_scales, void *d, int64_t m, int64_t n, int64_t k,
+                               int layout, int out_dtype, int split_k, void *stream);
+
+// One wave of back-to-back block-scaled MMAs per SM (pair == 0) or CTA pair
+// (pair == 1); form: MX_MMA_*.  *units: the CTAs or pairs launched.
+cudaError_t launch_calibrate_mma(int form, int pair, int64_t steps, unsigned long long *cycles,
+                                 uint32_t *status, int num_sms, cudaStream_t s, int *units);
+
 // Launch with programmatic stream serialization (the kernel itself orders
 // its global-memory accesses after its predecessor with griddep_wait).
 template <typename... KArgs, typename... Args>

@@ -11,16 +11,20 @@
 // image instead, so neither the caller nor the library allocates anything.
 //
 // The array holds MX_STATIC_WORKSPACE_BYTES.  CUDA sets it up on a device when
-// the library's device code is loaded there (at the latest on the first call
-// of this entry point on that device) and keeps it until the process exits.
-// Shapes whose split-K partials do not fit are rejected with
-// MX_ERR_WORKSPACE before anything is launched.
+// this file's device code is loaded in a context there, and keeps it until the
+// context goes away (at the latest when the process exits).  The library
+// looks up its device address, with that context current, on the first call
+// of any entry point in the context (cudaGetSymbolAddress, return code
+// checked), and again after the context changes (cudaDeviceReset), so the
+// address the kernels get is always one of the current context.  Shapes
+// whose split-K partials do not fit are rejected with MX_ERR_WORKSPACE before
+// anything is launched, after the same argument checks as mxfp4_gemm.
 #include <cuda_runtime.h>
 
 #include <cstddef>
 #include <cstdint>
-#include <mutex>
 
+#include "mx_internal.h"
 #include "mxfp4.h"
 
 #define MX_API extern "C" __attribute__((visibility("default")))
@@ -32,47 +36,28 @@ namespace {
 // later reads, so nothing in it has to start at zero.
 static __device__ __align__(256) float g_static_workspace[MX_STATIC_WORKSPACE_BYTES / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void *g_workspace_ptr[kMaxDevices] = {};
+}  // namespace
 
-// Device address of the array on the current device.  In host code the
-// array's name stands for a host-side shadow, not device memory, so the
-// address is looked up once per device (with that device current) and cached.
-int static_workspace(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return MX_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_workspace_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return MX_ERR_CUDA;
-    }
-    g_workspace_ptr[dev] = p;
-  }
-  *out = g_workspace_ptr[dev];
-  return MX_OK;
+namespace mx {
+
+// Device address of the array in the current context.  In host code the
+// array's name stands for a host-side shadow, not device memory: only this
+// lookup gives an address a kernel may use.
+cudaError_t static_workspace_symbol(void **out) {
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+  if (e != cudaSuccess) return e;
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  *out = p;
+  return cudaSuccess;
 }
 
-}  // namespace
+}  // namespace mx
 
 MX_API int mxfp4_gemm_static_workspace(const void *a_codes, const void *a_scales,
                                        const void *b_codes, const void *b_scales, void *d,
                                        int64_t m, int64_t n, int64_t k, int layout, int out_dtype,
                                        int split_k, void *stream) {
-  // The scratch this shape and split count needs (0 when no split-K is used
-  // or when the arguments are invalid, which mxfp4_gemm then reports).
-  const size_t need = mx_gemm_workspace_bytes(m, n, k, split_k);
-  if (need > static_cast<size_t>(MX_STATIC_WORKSPACE_BYTES)) return MX_ERR_WORKSPACE;
-  void *ws = nullptr;
-  if (need > 0) {
-    const int rc = static_workspace(&ws);
-    if (rc != MX_OK) return rc;
-  }
-  return mxfp4_gemm(a_codes, a_scales, b_codes, b_scales, d, m, n, k, layout, out_dtype, split_k,
-                    ws, need > 0 ? static_cast<size_t>(MX_STATIC_WORKSPACE_BYTES) : 0, stream);
+  return mx::gemm_static_workspace_call(a_codes, a_scales, b_codes, b_scales, d, m, n, k, layout,
+                                        out_dtype, split_k, stream);
 }

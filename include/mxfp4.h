@@ -80,6 +80,18 @@ extern "C" {
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mx_error_string(int code);
 
+/* What the last call made on this thread rejected or failed on: the entry
+ * point, the argument and the constraint it broke (for instance
+ * "mxfp4_gemm: K = 300 is not a multiple of 256"), or the CUDA error of a
+ * failed launch.  Every entry point that returns a status clears it first, so
+ * after a call that returned MX_OK it reads "no error recorded by the last
+ * call on this thread".  The review of the C API on "Initial integration of
+ * a4w4 GEMM" (ROCm/TransformerEngine #663) asks for errors a caller can tell
+ * apart and explain; the status code says which class, this says where.
+ * Thread-local storage of the library, valid until the thread's next call;
+ * never NULL. */
+const char *mx_last_error_string(void);
+
 /* 1 when the library holds sm_103a kernels and the current device is an
  * sm_103 GPU, 0 otherwise.  Never fails. */
 int mx_available(void);
@@ -364,6 +376,27 @@ int mx_device_status(void *stream);
  * MX_ERR_DEVICE_TIMEOUT in the status word and returns.  Asynchronous; read
  * the result with mx_device_status.  timeout_ns must be in (0, 1e10]. */
 int mx_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* ---- tensor-pipe calibration ------------------------------------------
+ * The pages give no FP4 MMA rate for this GPU, and a data-sheet peak says
+ * nothing about which MMA form reaches it.  This entry point measures it: it
+ * launches one wave in which every SM (MX_MMA pair == 0: one CTA issuing
+ * M=128 x N=256 x K=64 MMAs) or every CTA pair (pair == 1: cta_group::2
+ * MMAs of M=256 x N=256 x K=64, the shape of the GEMM's pair kernel) issues
+ * 4 * steps back-to-back block-scaled MMAs of the given form from shared
+ * memory, on zero operands, with nothing else to do.  Time the call with CUDA
+ * events on `stream`: *flops (host) receives the FLOPs the launch performs
+ * (2 M N K per MMA), *units (host) the CTAs (pair == 0) or CTA pairs it ran.
+ * cycles: null, or a device buffer of cycles_capacity >= the device's SM
+ * count 8-byte entries; entry u receives the SM cycles from unit u's first
+ * issue to the completion of its last MMA (0 if its bounded wait ran out).
+ * steps in [1, MX_CALIBRATE_MAX_STEPS]. */
+#define MX_MMA_MXF4 0         /* kind::mxf4 scale_vec::2X, UE8M0 (MXFP4 GEMM)   */
+#define MX_MMA_MXF4NVF4_2X 1  /* kind::mxf4nvf4 scale_vec::2X, UE8M0            */
+#define MX_MMA_MXF4NVF4_4X 2  /* kind::mxf4nvf4 scale_vec::4X, UE4M3 (NVFP4)    */
+#define MX_CALIBRATE_MAX_STEPS (1 << 20)
+int mx_calibrate_mma(int form, int pair, int64_t steps, unsigned long long *cycles,
+                     int cycles_capacity, double *flops, int *units, void *stream);
 
 #ifdef __cplusplus
 }

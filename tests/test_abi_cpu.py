@@ -292,3 +292,98 @@ def test_static_workspace_rejects_oversized_partials_before_any_launch(lib):
     assert rc == mx.MX_ERR_INVALID_ARG
     rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 128, 0, 0, 1, None)
     assert rc == mx.MX_ERR_UNSUPPORTED_SHAPE
+
+
+def test_static_workspace_checks_arguments_before_the_partials_size(lib):
+    """A call that is both invalid and oversized gets the code mxfp4_gemm gives
+    for the invalid argument, not MX_ERR_WORKSPACE."""
+    m, n, k, split = 128, 8192, 8192, 8
+    assert split * m * n * 4 > mx.MX_STATIC_WORKSPACE_BYTES
+    rc = lib.mxfp4_gemm_static_workspace(None, FAKE, FAKE, FAKE, FAKE, m, n, k, 0, 0, split, None)
+    assert rc == mx.MX_ERR_INVALID_ARG
+    rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, m, n, k, 1, 0, split, None)
+    assert rc == mx.MX_ERR_UNSUPPORTED_FEATURE
+    rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, m, n, k, 0, 5, split, None)
+    assert rc == mx.MX_ERR_UNSUPPORTED_FEATURE
+    rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, m, 8200, k, 0, 0, split,
+                                         None)
+    assert rc == mx.MX_ERR_UNSUPPORTED_SHAPE
+    rc = lib.mxfp4_gemm_static_workspace(FAKE_ODD, FAKE, FAKE, FAKE, FAKE, m, n, k, 0, 0, split,
+                                         None)
+    assert rc == mx.MX_ERR_ALIGNMENT
+
+
+def test_last_error_string_names_the_argument_and_constraint(lib):
+    detail = lambda: lib.mx_last_error_string().decode()  # noqa: E731
+    assert _gemm(lib, k=300) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert detail() == "mxfp4_gemm: K = 300 is not a multiple of 256"
+    assert _gemm(lib, b=None) == mx.MX_ERR_INVALID_ARG
+    assert detail() == "mxfp4_gemm: b_codes is null"
+    assert _gemm(lib, n=40) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert detail() == "mxfp4_gemm: N = 40 is not a multiple of 32"
+    assert _gemm(lib, layout=2) == mx.MX_ERR_UNSUPPORTED_FEATURE
+    assert "layout 2" in detail()
+    # quantize: the block of the format
+    rc = lib.mx_quantize_bf16(FAKE, 4, 40, 40, mx.MX_FMT_NVFP4, 0, FAKE, FAKE, FAKE, FAKE,
+                              4096, None)
+    assert rc == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert detail() == "mx_quantize_bf16: cols = 40 is not a multiple of the NVFP4 block 16"
+    # the NVFP4 amax workspace
+    rc = lib.mx_quantize_bf16(FAKE, 4, 32, 32, mx.MX_FMT_NVFP4, 0, FAKE, FAKE, FAKE, FAKE, 16,
+                              None)
+    assert rc == mx.MX_ERR_WORKSPACE
+    assert detail().startswith("mx_quantize_bf16: NVFP4 needs a workspace of 2048 bytes, got 16")
+    # the static array's size, with the numbers
+    rc = lib.mxfp4_gemm_static_workspace(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 8192, 8192, 0, 0, 8,
+                                         None)
+    assert rc == mx.MX_ERR_WORKSPACE
+    assert detail() == ("mxfp4_gemm_static_workspace: 8 splits of K need 33554432 bytes of "
+                        "partial sums, more than the 16777216 bytes of the static array")
+    # a group names the tensor
+    t = (mx.mx_quantize_tensor * 2)()
+    t[0].x, t[0].rows, t[0].cols, t[0].ld_x, t[0].codes, t[0].scales = FAKE, 4, 64, 64, FAKE, FAKE
+    t[1].x, t[1].rows, t[1].cols, t[1].ld_x, t[1].codes, t[1].scales = FAKE, 4, 64, 32, FAKE, FAKE
+    assert lib.mx_quantize_bf16_group(t, 2, mx.MX_FMT_MXFP4, 0, None, 0, None) == \
+        mx.MX_ERR_INVALID_ARG
+    assert detail().startswith("mx_quantize_bf16_group (tensor 1): rows, cols, ld_x = 4, 64, 32")
+
+
+def test_last_error_string_is_per_thread_and_per_call(lib):
+    import threading
+    detail = lambda: lib.mx_last_error_string().decode()  # noqa: E731
+    assert _gemm(lib, k=300) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    seen = {}
+
+    def other():
+        seen["before"] = detail()
+        _gemm(lib, m=48)
+        seen["after"] = detail()
+
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert seen["before"] == "no error recorded by the last call on this thread"
+    assert seen["after"] == "mxfp4_gemm: M = 48 is not a multiple of 32"
+    assert detail() == "mxfp4_gemm: K = 300 is not a multiple of 256"
+    # the next call replaces it
+    assert lib.mx_selftest_wait_timeout(0, None) == mx.MX_ERR_INVALID_ARG
+    assert detail() == "mx_selftest_wait_timeout: timeout_ns = 0 (1 .. 1e10)"
+
+
+def test_binding_errors_carry_the_detail(lib):
+    with pytest.raises(mx.MXError, match="K = 300 is not a multiple of 256") as ei:
+        mx.mxfp4_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 300, stream=0)
+    assert ei.value.code == mx.MX_ERR_UNSUPPORTED_SHAPE
+
+
+def test_calibrate_argument_validation(lib):
+    flops = ctypes.c_double(0.0)
+    units = ctypes.c_int(0)
+    f, u = ctypes.byref(flops), ctypes.byref(units)
+    assert lib.mx_calibrate_mma(3, 1, 16, None, 0, f, u, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_calibrate_mma(0, 2, 16, None, 0, f, u, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_calibrate_mma(0, 1, 0, None, 0, f, u, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_calibrate_mma(0, 1, mx.MX_CALIBRATE_MAX_STEPS + 1, None, 0, f, u, None) == \
+        mx.MX_ERR_INVALID_ARG
+    assert lib.mx_calibrate_mma(0, 1, 16, None, 0, None, u, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_calibrate_mma(0, 1, 16, FAKE + 4, 152, f, u, None) == mx.MX_ERR_ALIGNMENT

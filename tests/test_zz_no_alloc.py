@@ -3,9 +3,13 @@ device memory (a plugin in a host program that owns all device memory, or a path
 where a new allocation is not allowed).  Its split-K scratch is a fixed array in
 the library instead of a caller-provided workspace.
 
-Checked through the C ABI against mxfp4_gemm with a workspace, on two calls in a
-row, within the FP32 tolerance of the other GEMM tests.  This file is collected
-last, and passes both alone in a fresh process and after the other tests.
+Checked through the C ABI on calls in a row that all use the shared scratch:
+each result is bit-identical to mxfp4_gemm with a caller workspace (the same
+kernels and the same fixed split order, so any stale or missed partial would
+show as a changed bit), and within the tolerances of the other GEMM tests of
+the oracle's D (FP32: 1e-5 * sum |a||b|; BF16: 1 ulp of the correctly rounded
+value).  This file is collected last, and passes both alone in a fresh process
+and after the other tests.
 """
 import numpy as np
 import pytest
@@ -14,7 +18,7 @@ import torch
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import check_fp32, dev_u8
+from tests.gpu_helpers import check_bf16, check_fp32, dev_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -27,38 +31,56 @@ def _inputs(m, n, k, seed):
     return a, sa, b, sb
 
 
-def _run_both(a, sa, b, sb, m, n, k, split_k):
-    """Returns (static-scratch result, workspace result) as host FP32 arrays."""
+def _bits(d: torch.Tensor) -> np.ndarray:
+    """The raw bits of a device result (NaN-safe comparison)."""
+    if d.dtype == torch.float32:
+        return d.view(torch.int32).cpu().numpy().view(np.uint32)
+    return d.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _run_both(a, sa, b, sb, m, n, k, split_k, out_dtype):
+    """Returns the bits of (static-scratch result, workspace result)."""
     da, dsa = dev_u8(a), dev_u8(oracle.scale_tile(sa))
     db, dsb = dev_u8(b), dev_u8(oracle.scale_tile(sb))
-    d_static = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
-    d_ws = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    dt = torch.float32 if out_dtype == mx.MX_OUT_FP32 else torch.bfloat16
+    d_static = torch.full((m, n), float("nan"), dtype=dt, device="cuda")
+    d_ws = torch.full((m, n), float("nan"), dtype=dt, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     rc = mx.lib().mxfp4_gemm_static_workspace(
         da.data_ptr(), dsa.data_ptr(), db.data_ptr(), dsb.data_ptr(), d_static.data_ptr(),
-        m, n, k, mx.MX_LAYOUT_TN, mx.MX_OUT_FP32, split_k, stream)
-    assert rc == mx.MX_OK, mx.mx_error_string(rc)
+        m, n, k, mx.MX_LAYOUT_TN, out_dtype, split_k, stream)
+    assert rc == mx.MX_OK, mx.mx_last_error_string()
     wsb = mx.mx_gemm_workspace_bytes(m, n, k, split_k)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     rc = mx.lib().mxfp4_gemm(
         da.data_ptr(), dsa.data_ptr(), db.data_ptr(), dsb.data_ptr(), d_ws.data_ptr(),
-        m, n, k, mx.MX_LAYOUT_TN, mx.MX_OUT_FP32, split_k, ws.data_ptr(), wsb, stream)
-    assert rc == mx.MX_OK, mx.mx_error_string(rc)
+        m, n, k, mx.MX_LAYOUT_TN, out_dtype, split_k, ws.data_ptr(), wsb, stream)
+    assert rc == mx.MX_OK, mx.mx_last_error_string()
     torch.cuda.synchronize()
     assert mx.mx_device_status() == mx.MX_OK
-    return d_static.cpu().numpy(), d_ws.cpu().numpy()
+    return _bits(d_static), _bits(d_ws)
 
 
-def test_static_workspace_matches_workspace_gemm_twice():
-    # the decode-shaped skinny GEMM (automatic split-K), then an explicit split
-    # count on other data: two calls in a row that both use the shared scratch
-    for m, n, k, split_k, seed in [(32, 8192, 8192, 0, 401), (64, 1024, 4096, 4, 402)]:
+def test_static_workspace_matches_workspace_gemm_and_oracle_on_calls_in_a_row():
+    # the decode-shaped skinny GEMM (automatic split-K), an explicit split count
+    # on other data, then BF16 outputs of a third shape: calls in a row that all
+    # use the shared scratch, each leaving partials the next must not read
+    cases = [(32, 8192, 8192, 0, 401, mx.MX_OUT_BF16),
+             (64, 1024, 4096, 4, 402, mx.MX_OUT_FP32),
+             (96, 2048, 2048, 2, 403, mx.MX_OUT_BF16),
+             (32, 8192, 8192, 0, 404, mx.MX_OUT_FP32)]
+    for m, n, k, split_k, seed, out in cases:
         need = mx.mx_gemm_workspace_bytes(m, n, k, split_k)
         assert 0 < need <= mx.MX_STATIC_WORKSPACE_BYTES      # split-K really runs
         a, sa, b, sb = _inputs(m, n, k, seed)
-        d_static, d_ws = _run_both(a, sa, b, sb, m, n, k, split_k)
-        _, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
-        check_fp32(d_static, d_ws.astype(np.float64), s_abs, f"static scratch {m}x{n}x{k}")
+        d_static, d_ws = _run_both(a, sa, b, sb, m, n, k, split_k, out)
+        what = f"static scratch {m}x{n}x{k} split {split_k}"
+        assert np.array_equal(d_static, d_ws), f"{what}: differs from the workspace GEMM"
+        ref, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
+        if out == mx.MX_OUT_FP32:
+            check_fp32(d_static.view(np.float32), ref, s_abs, what)
+        else:
+            check_bf16(d_static, ref, s_abs, what)
 
 
 def test_static_workspace_rejects_shapes_beyond_its_size():
@@ -73,5 +95,6 @@ def test_static_workspace_rejects_shapes_beyond_its_size():
         mx.mxfp4_gemm_static_workspace(a, sa, b, sb, d, m, n, k, mx.MX_LAYOUT_TN,
                                        mx.MX_OUT_FP32, split_k)
     assert e.value.code == mx.MX_ERR_WORKSPACE
+    assert "more than the 16777216 bytes of the static array" in e.value.detail
     torch.cuda.synchronize()
     assert torch.all(d == 7.0)   # rejected before anything was launched
