@@ -98,6 +98,9 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--calibrate", action="store_true",
+                   help="print the FP4 MMA rate of every form and shape (mx_calibrate_mma), "
+                        "one JSON line each, and exit")
     a = p.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     a.steps = max(a.steps, 1)
@@ -685,7 +688,24 @@ def recorded_traffic(name, call):
 
 # --------------------------------------------------------------------- MMA ceiling
 
-def mma_ceiling(mx, torch, steps=1 << 15):
+def calibrate_all(steps=1 << 16):
+    """`--calibrate`: every MMA form and shape, one JSON line each."""
+    import torch
+    torch.cuda.set_device(0)
+    from block_scaled_fp4_bf16_gb300 import build
+    build.build()
+    import block_scaled_fp4_bf16_gb300 as mx
+    names = {mx.MX_MMA_MXF4: "kind::mxf4 scale_vec::2X (UE8M0)",
+             mx.MX_MMA_MXF4NVF4_2X: "kind::mxf4nvf4 scale_vec::2X (UE8M0)",
+             mx.MX_MMA_MXF4NVF4_4X: "kind::mxf4nvf4 scale_vec::4X (UE4M3)"}
+    for pair in (1, 0):
+        for form, name in names.items():
+            r = mma_ceiling(mx, torch, steps, form=form, pair=pair)
+            r["form"] = name + (", cta_group::2, 256x256x64" if pair else ", cta_group::1, 128x256x64")
+            print(json.dumps(r), flush=True)
+
+
+def mma_ceiling(mx, torch, steps=1 << 15, form=None, pair=1):
     """Live calibration of the tensor pipe (mx_calibrate_mma): one wave of
     back-to-back CTA-pair MMAs of the pair GEMM's form and shape per SM pair.
     Returns its FLOPs per clock per SM (cycle counts of every pair, so it does
@@ -693,12 +713,13 @@ def mma_ceiling(mx, torch, steps=1 << 15):
     nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     cyc = torch.zeros(nsm, dtype=torch.int64, device="cuda")
     stream = torch.cuda.current_stream()
-    mx.mx_calibrate_mma(mx.MX_MMA_MXF4, 1, 256, cyc)          # warm-up
+    form = mx.MX_MMA_MXF4 if form is None else form
+    mx.mx_calibrate_mma(form, pair, 256, cyc)          # warm-up
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
-    flops, units = mx.mx_calibrate_mma(mx.MX_MMA_MXF4, 1, steps, cyc)
+    flops, units = mx.mx_calibrate_mma(form, pair, steps, cyc)
     e1.record(stream)
     torch.cuda.synchronize()
     if mx.mx_device_status() != mx.MX_OK:
@@ -706,7 +727,7 @@ def mma_ceiling(mx, torch, steps=1 << 15):
     secs = e0.elapsed_time(e1) * 1e-3
     cycles = statistics.median(cyc[:units].cpu().tolist())
     mmas = 4 * steps
-    per_sm_flop = 2.0 * 128 * 256 * 64          # each SM's half of a 256x256x64 pair MMA
+    per_sm_flop = 2.0 * 128 * 256 * 64   # one 128x256x64 MMA, or each SM's half of a pair's
     return {"form": "kind::mxf4 block_scale scale_vec::2X, cta_group::2, 256x256x64",
             "cycles_per_mma": cycles / mmas,
             "flop_per_clk_sm": per_sm_flop * mmas / cycles,
@@ -910,7 +931,9 @@ def main_reference(args):
 
 if __name__ == "__main__":
     a = parse_args()
-    if a.impl == "reference":
+    if a.calibrate:
+        calibrate_all()
+    elif a.impl == "reference":
         main_reference(a)
     else:
         main_ours(a)

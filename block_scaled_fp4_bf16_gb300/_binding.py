@@ -13,7 +13,10 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libmxfp4.so")
+# The bounds-checked build (MX_BOUNDS_CHECK=1 in the environment) lives in its
+# own folder, so the release library is never replaced by it.
+LIB_PATH = os.path.join(_HERE, "_build_bounds" if os.environ.get("MX_BOUNDS_CHECK") == "1"
+                        else "_build", "libmxfp4.so")
 
 MX_OK = 0
 MX_ERR_INVALID_ARG = -1
@@ -25,6 +28,7 @@ MX_ERR_ALIGNMENT = -6
 MX_ERR_WORKSPACE = -7
 MX_ERR_CUDA = -8
 MX_ERR_DEVICE_TIMEOUT = -9
+MX_ERR_DEVICE_BOUNDS = -10
 
 MX_FMT_MXFP4 = 0
 MX_FMT_NVFP4 = 1
@@ -40,6 +44,7 @@ MX_MMA_MXF4 = 0
 MX_MMA_MXF4NVF4_2X = 1
 MX_MMA_MXF4NVF4_4X = 2
 MX_CALIBRATE_MAX_STEPS = 1 << 20
+MX_BUILD_BOUNDS_CHECK = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.mx_last_error_string.argtypes = []
         L.mx_available.restype = i32
         L.mx_available.argtypes = []
+        L.mx_build_flags.restype = i32
+        L.mx_build_flags.argtypes = []
         L.mx_scale_bytes.restype = sz
         L.mx_scale_bytes.argtypes = [i64, i64, i32, i32]
         L.mx_quantize_workspace_bytes.restype = sz
@@ -168,6 +175,11 @@ def mx_error_string(code: int) -> str:
 def mx_last_error_string() -> str:
     """Detail of the last rejection or failure of a call on this thread."""
     return lib().mx_last_error_string().decode()
+
+
+def mx_build_flags() -> int:
+    """MX_BUILD_BOUNDS_CHECK when the loaded library is the bounds-checked build."""
+    return int(lib().mx_build_flags())
 
 
 def mx_available() -> bool:

@@ -13,9 +13,14 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-OUT_DIR = os.path.join(PKG, "_build")
+# MX_BOUNDS_CHECK=1 builds the bounds-checked library (-DMX_BOUNDS_CHECK: every
+# plain global access of the kernels checked against its buffer, a test
+# instrument) into its own folder; the binding then loads that one.
+BOUNDS_CHECK = os.environ.get("MX_BOUNDS_CHECK") == "1"
+OUT_DIR = os.path.join(PKG, "_build_bounds" if BOUNDS_CHECK else "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmxfp4.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "static_ws.cu", "calibrate.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "gemm_swap.cu", "static_ws.cu",
+           "calibrate.cu"]
 HEADERS = ["mx_device.cuh", "mx_internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -47,7 +52,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     for src in SOURCES:
         obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc()] + NVCC_FLAGS + list(extra_flags) + ["-c", os.path.join(CSRC, src), "-o", obj]
+        flags = list(extra_flags) + (["-DMX_BOUNDS_CHECK"] if BOUNDS_CHECK else [])
+        cmd = [nvcc()] + NVCC_FLAGS + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd))
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))

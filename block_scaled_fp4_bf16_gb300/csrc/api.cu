@@ -300,12 +300,13 @@ int gemm_common(const char *fn, int fmt, const void *a_codes, const void *a_scal
   DeviceInfo *dev = nullptr;
   const int drc = device_info(&dev);
   if (drc != MX_OK) return drc;
-  int bn = 128, splits = 1, pair = 0;
-  mx::gemm_plan(m, n, k, split_k, dev->num_sms, &bn, &splits, &pair);
+  const mx::GemmPlan plan = mx::gemm_plan(m, n, k, split_k, dev->num_sms);
+  const int bn = plan.bn, splits = plan.splits;
+  const bool pair = plan.kind == mx::kGemmPair, swap = plan.kind == mx::kGemmSwap;
   const size_t d_bytes = static_cast<size_t>(m) * static_cast<size_t>(n) *
                          (out_dtype == MX_OUT_FP32 ? 4u : 2u);
   const Range d_range{reinterpret_cast<uintptr_t>(d), reinterpret_cast<uintptr_t>(d) + d_bytes};
-  if (splits > 1) {
+  if (plan.workspace()) {
     const size_t need = static_cast<size_t>(splits) * static_cast<size_t>(m) *
                         static_cast<size_t>(n) * sizeof(float);
     if (!workspace || workspace_bytes < need)
@@ -319,10 +320,12 @@ int gemm_common(const char *fn, int fmt, const void *a_codes, const void *a_scal
       return fail(MX_ERR_INVALID_ARG, "%s: the workspace overlaps D", fn);
   }
   CUtensorMap tma, tmb, tmd, tmsa, tmsb;
-  // the single-CTA kernel (M <= 128) loads the M rows of A, the pair kernel 128 per CTA
+  // the single-CTA and swapped kernels (M <= 128) load the M rows of A, the
+  // pair kernel 128 per CTA
   if (encode_codes_map(&tma, a_codes, m, k, pair ? 128 : static_cast<int>(m)) != MX_OK)
     return fail(MX_ERR_CUDA, "%s: tensor map of A could not be encoded", fn);
-  // the pair kernel stages half of each 256-row B tile per CTA
+  // the pair kernel stages half of each 256-row B tile per CTA, the swapped
+  // kernel its 128, 64 or 32 rows of B (plan.bn)
   if (encode_codes_map(&tmb, b_codes, n, k, pair ? 128 : bn) != MX_OK)
     return fail(MX_ERR_CUDA, "%s: tensor map of B could not be encoded", fn);
   if (pair) {
@@ -333,8 +336,10 @@ int gemm_common(const char *fn, int fmt, const void *a_codes, const void *a_scal
                          atoms_per_stage) != MX_OK)
       return fail(MX_ERR_CUDA, "%s: tensor map of the scales could not be encoded", fn);
   }
-  const int box_cols = mx::gemm_out_box_cols(out_dtype == MX_OUT_FP32, splits);
-  const int orc = splits > 1
+  const int box_cols = mx::gemm_out_box_cols(out_dtype == MX_OUT_FP32, plan.workspace() ? splits : 1);
+  // (the swapped kernel writes D with plain stores: no output map)
+  const int orc = swap ? MX_OK
+                  : plan.workspace()
                       ? encode_out_map(&tmd, workspace, static_cast<int64_t>(splits) * m, n, true,
                                        box_cols)
                       : encode_out_map(&tmd, d, m, n, out_dtype == MX_OUT_FP32, box_cols);
@@ -346,7 +351,8 @@ int gemm_common(const char *fn, int fmt, const void *a_codes, const void *a_scal
   g.tmap_d = &tmd;
   g.tmap_sfa = pair ? &tmsa : nullptr;
   g.tmap_sfb = pair ? &tmsb : nullptr;
-  g.pair = pair;
+  g.pair = pair ? 1 : 0;
+  g.swap = swap ? 1 : 0;
   g.a_scales = a_scales;
   g.b_scales = b_scales;
   g.a_ts = a_ts;
@@ -367,6 +373,9 @@ int gemm_common(const char *fn, int fmt, const void *a_codes, const void *a_scal
     g.epi.beta = epi->beta;
     g.epi.c = epi->beta != 0.0f ? d : nullptr;  // beta == 0: D stays write-only
   }
+  g.epi.c_elems = m * n;
+  g.epi.bias_elems = n;
+  g.epi.status = dev->status;
   return launch_rc(fn, mx::launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
@@ -384,12 +393,21 @@ MX_API const char *mx_error_string(int code) {
     case MX_ERR_WORKSPACE: return "workspace missing or too small";
     case MX_ERR_CUDA: return "CUDA runtime, driver or launch error";
     case MX_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case MX_ERR_DEVICE_BOUNDS: return "bounds-checked build: a kernel access outside its buffer";
     default: return "unknown status code";
   }
 }
 
 MX_API const char *mx_last_error_string(void) {
   return t_detail[0] != '\0' ? t_detail : "no error recorded by the last call on this thread";
+}
+
+MX_API int mx_build_flags(void) {
+#ifdef MX_BOUNDS_CHECK
+  return MX_BUILD_BOUNDS_CHECK;
+#else
+  return 0;
+#endif
 }
 
 MX_API int mx_available(void) {
@@ -500,6 +518,7 @@ MX_API int mx_quantize_bf16(const void *x, int64_t rows, int64_t cols, int64_t l
   rc = device_info(&dev);
   if (rc != MX_OK) return rc;
   a.num_sms = dev->num_sms;
+  a.status = dev->status;
   return launch_rc(fn, mx::launch_quantize_group(format == MX_FMT_MXFP4 ? 0 : 1, &a, 1,
                                                  static_cast<cudaStream_t>(stream)));
 }
@@ -527,6 +546,7 @@ MX_API int nvfp4_quantize_bf16_sr(const void *x, int64_t rows, int64_t cols, int
   rc = device_info(&dev);
   if (rc != MX_OK) return rc;
   a.num_sms = dev->num_sms;
+  a.status = dev->status;
   const mx::SrArgs sr{seed, philox_rounds, 0u};
   return launch_rc(fn, mx::launch_quantize_group(1, &a, 1, static_cast<cudaStream_t>(stream), &sr));
 }
@@ -592,7 +612,10 @@ MX_API int mx_quantize_bf16_group(const mx_quantize_tensor *tensors, int count, 
   DeviceInfo *dev = nullptr;
   const int rc = device_info(&dev);
   if (rc != MX_OK) return rc;
-  for (int i = 0; i < count; ++i) a[i].num_sms = dev->num_sms;
+  for (int i = 0; i < count; ++i) {
+    a[i].num_sms = dev->num_sms;
+    a[i].status = dev->status;
+  }
   return launch_rc(fn, mx::launch_quantize_group(format == MX_FMT_MXFP4 ? 0 : 1, a, count,
                                                  static_cast<cudaStream_t>(stream)));
 }
@@ -681,7 +704,7 @@ MX_API int mx_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_
   if (rc != MX_OK) return rc;
   return launch_rc(fn, mx::launch_mx_quantize_2d(x, rows, cols, ld_x,
                                                  scale_layout == MX_SCALE_TCGEN05, codes, scales,
-                                                 codes_t, scales_t,
+                                                 codes_t, scales_t, dev->status,
                                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -736,7 +759,7 @@ MX_API int nvfp4_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int
   return launch_rc(fn, mx::launch_nvfp4_quantize_2d(
       x, rows, cols, ld_x, scale_layout == MX_SCALE_TCGEN05, codes, scales, codes_t, scales_t,
       tensor_scale, static_cast<uint32_t *>(workspace), stochastic ? &sr : nullptr, dev->num_sms,
-      static_cast<cudaStream_t>(stream)));
+      dev->status, static_cast<cudaStream_t>(stream)));
 }
 
 MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format,
@@ -760,15 +783,14 @@ MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int 
   const int rc = device_info(&dev);
   if (rc != MX_OK) return rc;
   return launch_rc(fn, mx::launch_scale_relayout(plain, rows, cols / block_of(format), tiled,
-                                                 static_cast<cudaStream_t>(stream)));
+                                                 dev->status, static_cast<cudaStream_t>(stream)));
 }
 
 MX_API size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k) {
   if (m <= 0 || n <= 0 || k <= 0 || k % 256 != 0 || split_k < 0) return 0;
-  int bn = 128, splits = 1, pair = 0;
-  mx::gemm_plan(m, n, k, split_k, num_sms_or_default(), &bn, &splits, &pair);
-  if (splits <= 1) return 0;
-  return static_cast<size_t>(splits) * static_cast<size_t>(m) * static_cast<size_t>(n) *
+  const mx::GemmPlan plan = mx::gemm_plan(m, n, k, split_k, num_sms_or_default());
+  if (!plan.workspace()) return 0;
+  return static_cast<size_t>(plan.splits) * static_cast<size_t>(m) * static_cast<size_t>(n) *
          sizeof(float);
 }
 
@@ -834,6 +856,10 @@ MX_API int mx_device_status(void *stream) {
   if (word & mx::kStatusTimeoutBit)
     return fail(MX_ERR_DEVICE_TIMEOUT,
                 "mx_device_status: a kernel's bounded wait ran out and it abandoned its work");
+  if (word & mx::kStatusBoundsBit)
+    return fail(MX_ERR_DEVICE_BOUNDS,
+                "mx_device_status: a kernel of the bounds-checked build skipped an access outside "
+                "its buffer");
   return MX_OK;
 }
 
@@ -894,11 +920,11 @@ int gemm_static_workspace_call(const void *a_codes, const void *a_scales, const 
   const int arc = gemm_check_args(fn, MX_FMT_MXFP4, a_codes, a_scales, b_codes, b_scales, nullptr,
                                   nullptr, d, m, n, k, layout, out_dtype, split_k, nullptr);
   if (arc != MX_OK) return arc;
-  int bn = 128, splits = 1, pair = 0;
-  mx::gemm_plan(m, n, k, split_k, num_sms_or_default(), &bn, &splits, &pair);
-  const size_t need = splits > 1 ? static_cast<size_t>(splits) * static_cast<size_t>(m) *
-                                       static_cast<size_t>(n) * sizeof(float)
-                                 : 0;
+  const mx::GemmPlan plan = mx::gemm_plan(m, n, k, split_k, num_sms_or_default());
+  const int splits = plan.splits;
+  const size_t need = plan.workspace() ? static_cast<size_t>(splits) * static_cast<size_t>(m) *
+                                             static_cast<size_t>(n) * sizeof(float)
+                                       : 0;
   if (need > static_cast<size_t>(MX_STATIC_WORKSPACE_BYTES))
     return fail(MX_ERR_WORKSPACE,
                 "%s: %d splits of K need %zu bytes of partial sums, more than the %u bytes of the "

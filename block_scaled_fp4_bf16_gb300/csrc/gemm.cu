@@ -339,7 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float bias_l = 0.0f;
         if constexpr (EPI != 0) {
           const int bc = nt * BN + c * kChunk + lane;
-          if (p.epi.bias != nullptr && lane < kChunk && bc < p.n) bias_l = __ldg(p.epi.bias + bc);
+          if (p.epi.bias != nullptr && lane < kChunk && bc < p.n &&
+              in_bounds(bc, 1, p.epi.bias_elems, p.epi.status))
+            bias_l = __ldg(p.epi.bias + bc);
         }
         if constexpr (kChunk == 32) {
           uint32_t r[32];
@@ -461,9 +463,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
   const int64_t n8 = mn >> 3;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (!in_bounds(8 * i, 8, mn, epi.status)) continue;
     const float4 *p0 = reinterpret_cast<const float4 *>(ws) + 2 * i;
     float4 lo = p0[0], hi = p0[1];
     for (int s = 1; s < splits; ++s) {
+      if (!in_bounds(s * mn + 8 * i, 8, static_cast<int64_t>(splits) * mn, epi.status)) continue;
       const float4 *ps = reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(s) * mn) + 2 * i;
       const float4 a = ps[0], b = ps[1];
       lo.x += a.x;
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
     for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], alpha);
     if (epi_on) {
       float bv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-      if (epi.bias != nullptr) {
+      if (epi.bias != nullptr && in_bounds((8 * i) % n, 8, epi.bias_elems, epi.status)) {
         const float4 *b = reinterpret_cast<const float4 *>(epi.bias + (8 * i) % n);
         const float4 b0 = __ldg(b), b1 = __ldg(b + 1);
         bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
@@ -569,23 +573,27 @@ cudaError_t launch_bn(const GemmArgs &g, cudaStream_t s) {
 
 }  // namespace
 
-void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits,
-               int *pair) {
+GemmPlan gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms) {
+  GemmPlan plan{kGemmSingle, 128, 1};
   const int64_t k_stages = k / kStageK;
+  if (split_k == 0 && m <= 64 && m % 32 == 0) {
+    plan.kind = kGemmSwap;
+    gemm_swap_shape(m, n, k, num_sms, &plan.bn, &plan.splits);
+    return plan;
+  }
   int64_t tiles;
   int64_t slots;  // units the GPU runs at once
   if (m > kBM) {
     // CTA pairs with 256 x 256 tiles
-    *pair = 1;
-    *bn = 256;
+    plan.kind = kGemmPair;
+    plan.bn = 256;
     tiles = ((m + 255) / 256) * ((n + 255) / 256);
     slots = num_sms / 2;
   } else {
-    *pair = 0;
     const int64_t m_tiles = (m + kBM - 1) / kBM;
     const int64_t tiles256 = m_tiles * ((n + 255) / 256);
-    *bn = (tiles256 >= 2 * num_sms) ? 256 : 128;
-    tiles = m_tiles * ((n + *bn - 1) / *bn);
+    plan.bn = (tiles256 >= 2 * num_sms) ? 256 : 128;
+    tiles = m_tiles * ((n + plan.bn - 1) / plan.bn);
     slots = num_sms;
   }
   int s = split_k;
@@ -599,7 +607,8 @@ void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *b
   if (s < 1) s = 1;
   // Every split must own at least one stage: shrink s until it does.
   while (s > 1 && (k_stages + s - 1) / s * (s - 1) >= k_stages) --s;
-  *splits = s;
+  plan.splits = s;
+  return plan;
 }
 
 int gemm_out_box_cols(int out_fp32, int split_k) { return (out_fp32 || split_k > 1) ? 16 : 32; }
@@ -619,6 +628,7 @@ cudaError_t launch_splitk_reduce(const GemmArgs &g, cudaStream_t s) {
 }
 
 cudaError_t launch_gemm(const GemmArgs &g, cudaStream_t s) {
+  if (g.swap) return launch_gemm_swap(g, s);
   if (g.pair) return launch_gemm_pair(g, s);
   if (g.fmt == 0) return g.bn == 256 ? launch_bn<0, 256>(g, s) : launch_bn<0, 128>(g, s);
   return g.bn == 256 ? launch_bn<1, 256>(g, s) : launch_bn<1, 128>(g, s);

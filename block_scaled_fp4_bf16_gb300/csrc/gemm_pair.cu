@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(PairCfg<FMT, EPI >= 2 ? 16 : 8>::kThreads, 1)
       for (int j = 0; j < kBiasPerLane; ++j) bias_l[j] = 0.0f;
       if constexpr (EPI != 0) {
         const int bc = nt * 256 + h * C::kWarpCols + kBiasPerLane * lane;
-        if (p.epi.bias != nullptr && bc < p.n) {
+        if (p.epi.bias != nullptr && bc < p.n &&
+            in_bounds(bc, kBiasPerLane, p.epi.bias_elems, p.epi.status)) {
 #pragma unroll
           for (int j = 0; j < kBiasPerLane; ++j) bias_l[j] = __ldg(p.epi.bias + bc + j);
         }

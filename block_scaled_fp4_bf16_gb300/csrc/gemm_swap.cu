@@ -1,0 +1,526 @@
+// Block-scaled FP4 GEMM for skinny M (M <= 64, the decode shapes), with the
+// operands swapped: D^T[N, M] = B[N, K] A[M, K]^T, so that the weight rows
+// fill the tensor core's 128-row side and the few activation rows are its
+// narrow N side.  Same contract and arithmetic as the other GEMM kernels
+// ("Integrate MXFP4 hipblaslt GEMM support", ROCm/TransformerEngine #697;
+// NVFP4 from NVIDIA/TransformerEngine #3809); the split of K is the linear
+// split count of "Initial integration of a4w4 GEMM" (ROCm/TransformerEngine
+// #663), here S = 1, 2 or 4 CTAs of one thread-block cluster.
+//
+// Why: a skinny GEMM streams the weights once from HBM, so it needs enough
+// SMs streaming at once and nothing between the last weight byte and the
+// output.  One CTA owns 128 weight rows and 1/S of K; the S CTAs of a cluster
+// own the same rows, and their FP32 partial sums meet in the shared memory of
+// the cluster's first CTA, added in rank order (deterministic, one rounding
+// of the sum at the end), with no workspace and no second kernel.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: before waiting for the previous kernel, the
+//               first stages of its weight rows are prefetched into L2
+//               (weights rarely depend on the previous kernel, and the
+//               prefetch is safe when they do: L2 is the coherence point);
+//               then the weight tile (128 rows), the activation tile (M rows)
+//               and both operands' scale atoms of every stage of its K range
+//               into a 7-stage ring.
+//   warp 1      allocates tensor memory; per stage, tcgen05.cp of the scale
+//               atoms into the stage's own columns and four K=64 MMAs
+//               (M = 128, N = M) into the M-column accumulator.
+//   warps 2..5  one tensor-memory lane quarter each (32 weight rows = 32
+//               output columns, all M output rows): load the accumulator.
+//               CTAs of rank > 0 park their partials in their own idle stage
+//               ring and push them with one bulk copy into rank 0's (once rank
+//               0 has said its ring is idle); rank 0 adds them in rank order,
+//               applies alpha and the epilogue terms, and writes D straight
+//               from registers (a warp writes 32 consecutive columns of a row
+//               per store).
+// Every wait is bounded; the CTAs of a cluster meet at a cluster barrier
+// before leaving, so no remote copy or arrival targets a finished CTA.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "mx_device.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+namespace {
+
+constexpr int kSwThreads = 192;
+constexpr int kSwMaxM = 64;
+constexpr int kSwRows = 128;        // rows of the MMA's weight tile (its M)
+constexpr int kSwStageKBytes = 128; // 256 FP4 codes of K per stage
+constexpr int kSwMaxSlots = 32;
+constexpr int kSwSmemBytes = 232448;
+constexpr int kSwSfCol = kSwMaxM;   // tensor memory: accumulator (<= 64 columns), then scales
+constexpr int kSwTmemCols = 512;
+
+// Shared memory of a CTA, laid out by the host for (format, M, weight rows R):
+//   weights     a ring of `slots` slices of R rows x 128 bytes, with
+//               (128 - R) x 128 guard bytes before and after: the MMA reads
+//               each stage as a 128-row window whose rows h * R .. are that
+//               stage's slice (the other rows are neighbouring slices or
+//               guard bytes; their accumulator rows are never stored), and
+//               the guards keep every window inside the allocation;
+//   activations a ring of M x 128-byte tiles;
+//   scales      a ring of both operands' scale atoms per stage;
+//   barriers    full[slots], empty[slots], tfull, ring_free, partials, then
+//               the tensor-memory slot and the abort flag.
+// A stage therefore takes R x 128 bytes of weight space, not 128 x 128, and
+// a CTA keeps 13 to 28 stages (about 200 KB) of loads in flight.
+template <int FMT>
+struct SwapCfg {
+  static constexpr int kAtomsK = FMT == 0 ? 2 : 4;  // 4-scale atoms per stage along K
+  static constexpr int kSfBytes = kAtomsK * 512;    // one operand's atoms of a stage
+  static constexpr int kSfSetCols = 2 * kAtomsK * 4;
+};
+
+struct SwapParams {
+  const uint8_t *sfw;   // weight (B) scales, tile order
+  const uint8_t *sfx;   // activation (A) scales, tile order
+  const float *a_ts;    // NVFP4 tensor scales or null
+  const float *b_ts;
+  uint32_t *status;
+  void *d;              // D [M, N], BF16 or FP32
+  int m, n;             // M (<= 64, % 32) and N
+  int k_stages, stages_per_split;
+  int katoms;           // scale atoms along K per 128-row tile
+  int wrows;            // weight rows per CTA: 128, 64 or 32 (a part of a 128-row atom)
+  int splits;           // CTAs per cluster (1, 2 or 4), one K range each
+  int slots;            // stages in flight
+  int w_off, x_off, sf_off, bar_off;  // shared-memory layout (bytes; w_off: slot 0's slice)
+  EpiParams epi;        // bias / beta / GELU (applied by rank 0 after the sum)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// MT: M / 32 (1 or 2), so that the accumulator rows of a thread are
+// registers indexed by compile-time constants.
+template <int FMT, int OUT_F32, int MT>
+__global__ void __launch_bounds__(kSwThreads, 1)
+    gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                     const __grid_constant__ CUtensorMap tmap_x, const SwapParams p) {
+  using C = SwapCfg<FMT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned stages
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusTimeout);
+    return;
+  }
+  const int slots = p.slots;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + slots;
+  uint64_t *tfull = bars + 2 * slots;
+  uint64_t *ring_free = tfull + 1;  // ranks > 0: rank 0's ring may take partials
+  uint64_t *partials = tfull + 2;   // rank 0: the other ranks' partials are in (bytes)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull + 3);
+  volatile uint32_t *abort = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.splits;
+  const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
+  // The CTA's weight rows n0 .. n0 + wrows - 1 are part `h` of the 128-row
+  // scale atom starting at row n_atom.  They are loaded into rows
+  // h * wrows .. of the 128-row tile, so that tile row i is atom row i and the
+  // atom's scale layout holds unchanged; the tile's other rows keep whatever
+  // shared memory held (their accumulator rows are never stored: the MMA
+  // keeps rows apart).
+  const int n0 = (static_cast<int>(blockIdx.x) / S) * p.wrows;
+  const int n_atom = n0 & ~(kSwRows - 1);
+  const int h_row = n0 - n_atom;                  // = h * wrows
+  const int nb = n_atom / kSwRows;
+  const int k0 = static_cast<int>(rank) * p.stages_per_split;
+  const int k1 = min(k0 + p.stages_per_split, p.k_stages);
+  constexpr int m = 32 * MT;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < slots; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(tfull), 1);
+    mbar_init(smem_u32(ring_free), 1);
+    mbar_init(smem_u32(partials), 1);
+    // rank 0 expects the partials of the S - 1 other ranks as bytes
+    if (S > 1 && rank == 0)
+      mbar_arrive_expect_tx(smem_u32(partials), static_cast<uint32_t>((S - 1) * m * kSwRows * 4));
+    *abort = 0u;
+    fence_barrier_init();
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kSwTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  if (S > 1)
+    cluster_sync();  // barriers initialised in every CTA before any remote arrival
+  else
+    __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // the first stages of the CTA's weights and of their scale atoms into L2
+    // (safe before the wait; it shortens the first loads after it)
+    if (elect_one()) {
+      const int pre = min(k1, k0 + slots);
+      for (int ks = k0; ks < pre; ++ks) {
+        tma_prefetch_l2_2d(&tmap_w, ks * kSwStageKBytes, n0);
+        tma_prefetch_l2_2d(&tmap_x, ks * kSwStageKBytes, 0);
+      }
+      bulk_prefetch_l2(p.sfw + (static_cast<size_t>(nb) * p.katoms + k0 * C::kAtomsK) * 512,
+                       static_cast<uint32_t>((pre - k0) * C::kSfBytes));
+      bulk_prefetch_l2(p.sfx + static_cast<size_t>(k0 * C::kAtomsK) * 512,
+                       static_cast<uint32_t>((pre - k0) * C::kSfBytes));
+    }
+    __syncwarp();
+    griddep_wait();
+    uint32_t it = 0, s = 0, ph = 0;
+    const uint32_t bytes =
+        static_cast<uint32_t>((p.wrows + m) * kSwStageKBytes + 2 * C::kSfBytes);
+    for (int ks = k0; ks < k1; ++ks, ++it) {
+      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u, abort, p.status)) break;
+      if (elect_one()) {
+        const uint32_t fb = smem_u32(&full[s]);
+        const uint32_t sf = smem_u32(smem + p.sf_off + s * 2 * C::kSfBytes);
+        mbar_arrive_expect_tx(fb, bytes);
+        tma_load_2d(smem_u32(smem + p.w_off + s * p.wrows * kSwStageKBytes), &tmap_w,
+                    ks * kSwStageKBytes, n0, fb);
+        tma_load_2d(smem_u32(smem + p.x_off + s * m * kSwStageKBytes), &tmap_x,
+                    ks * kSwStageKBytes, 0, fb);
+        bulk_load(sf, p.sfw + (static_cast<size_t>(nb) * p.katoms + ks * C::kAtomsK) * 512,
+                  C::kSfBytes, fb);
+        bulk_load(sf + C::kSfBytes, p.sfx + static_cast<size_t>(ks * C::kAtomsK) * 512,
+                  C::kSfBytes, fb);
+      }
+      __syncwarp();
+      if (++s == static_cast<uint32_t>(slots)) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    // Wait (bounded) for the copies of the stages still in flight, so that
+    // none lands after the CTA's ring has been reused or the CTA has left.
+    const uint32_t inflight = it < static_cast<uint32_t>(slots) ? it : static_cast<uint32_t>(slots);
+    for (uint32_t j = it - inflight; j < it; ++j)
+      mbar_drain(smem_u32(&full[j % slots]), (j / slots) & 1u);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    const uint32_t idesc0 = mma_idesc<FMT>(kSwRows, static_cast<uint32_t>(m), 0);
+    const uint32_t idesc2 = mma_idesc<FMT>(kSwRows, static_cast<uint32_t>(m), 2);
+    for (int ks = k0; ks < k1; ++ks) {
+      if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        // the stage's 128-row weight window: its slice is rows h_row ..
+        const uint32_t w_win =
+            smem_u32(smem + p.w_off + s * p.wrows * kSwStageKBytes - h_row * kSwStageKBytes);
+        const uint32_t x_tile = smem_u32(smem + p.x_off + s * m * kSwStageKBytes);
+        const uint32_t sfw_s = smem_u32(smem + p.sf_off + s * 2 * C::kSfBytes);
+        const uint32_t sfx_s = sfw_s + C::kSfBytes;
+        const uint32_t sfw_t = tmem + kSwSfCol + s * C::kSfSetCols;
+        const uint32_t sfx_t = sfw_t + C::kAtomsK * 4;
+#pragma unroll
+        for (int a = 0; a < C::kAtomsK; ++a) {
+          tc_cp_32x128b_warpx4(sfw_t + a * 4, smem_desc_scale_block(sfw_s + a * 512));
+          tc_cp_32x128b_warpx4(sfx_t + a * 4, smem_desc_scale_block(sfx_s + a * 512));
+        }
+        const uint64_t w_desc = smem_desc_sw128_kmajor(w_win);
+        const uint64_t x_desc = smem_desc_sw128_kmajor(x_tile);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int ka = FMT == 0 ? (kk >> 1) : kk;
+          const uint32_t idesc = (FMT == 0 && (kk & 1)) ? idesc2 : idesc0;
+          tc_mma_block_scaled<FMT>(tmem, w_desc + 2u * kk, x_desc + 2u * kk, idesc, sfw_t + ka * 4,
+                                   sfx_t + ka * 4, (ks > k0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&empty[s]));
+      }
+      __syncwarp();
+      if (++s == static_cast<uint32_t>(slots)) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    // The accumulator is complete (or, after an abort, the MMAs issued have
+    // finished) when tfull completes.
+    if (elect_one()) tc_commit(smem_u32(tfull));
+    __syncwarp();
+    if (!ok) mbar_drain(smem_u32(tfull), 0u);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    griddep_wait();
+    const int q = warp & 3;                 // tensor-memory lane quarter of this warp
+    const int col = n_atom + q * 32 + lane;  // output column of this lane (weight row)
+    // this warp's accumulator rows hold the CTA's weight rows
+    const bool mine = q * 32 >= h_row && q * 32 < h_row + p.wrows;
+    float acc[m];
+    bool ok = mbar_wait(smem_u32(tfull), 0u, abort, p.status);
+    ok = __all_sync(0xFFFFFFFFu, ok) && !*abort;
+    if (ok) {
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      uint32_t r[32];
+      tc_ld_32x32b_x32(taddr, r);
+      tc_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+      if constexpr (MT == 2) {
+        tc_ld_32x32b_x32(taddr + 32, r);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[32 + j] = __uint_as_float(r[j]);
+      }
+    }
+    // rank 0's ring is idle once its accumulator is complete: let the other
+    // ranks copy their partials there
+    float *recv = reinterpret_cast<float *>(smem);  // [S - 1][m][128]
+    if (S > 1 && rank == 0 && warp == 2 && lane == 0 && ok) {
+      for (int r2 = 1; r2 < S; ++r2)
+        mbar_arrive_cluster_release(mapa_shared(smem_u32(ring_free), static_cast<uint32_t>(r2)));
+    }
+    if (S > 1 && rank > 0) {
+      // park the partials [m][128] in this CTA's idle ring, then one thread
+      // copies them to rank 0 once its ring is free
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < m; ++j) recv[j * kSwRows + q * 32 + lane] = acc[j];
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
+      if (warp == 2) {
+        if (ok) ok = mbar_wait_acq_cluster(smem_u32(ring_free), 0u, abort, p.status);
+        if (__all_sync(0xFFFFFFFFu, ok) && lane == 0)
+          bulk_copy_to_cluster(
+              mapa_shared(smem_u32(recv), 0) + static_cast<uint32_t>((rank - 1) * m * kSwRows * 4),
+              smem_u32(recv), static_cast<uint32_t>(m * kSwRows * 4),
+              mapa_shared(smem_u32(partials), 0));
+      }
+    } else if (ok) {
+      if (S > 1) {
+        ok = mbar_wait(smem_u32(partials), 0u, abort, p.status);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) {
+          // the sum in rank order: ((acc_0 + acc_1) + acc_2) + acc_3
+          for (int r2 = 1; r2 < S; ++r2)
+#pragma unroll
+            for (int j = 0; j < m; ++j)
+              acc[j] = __fadd_rn(acc[j], recv[((r2 - 1) * m + j) * kSwRows + q * 32 + lane]);
+        }
+      }
+      if (ok && mine && col - lane < p.n) {  // N % 32 == 0: a warp's columns are all in or out
+        float alpha = 1.0f;
+        if (FMT == 1) alpha = __fmul_rn(*p.a_ts, *p.b_ts);
+        float bias = 0.0f;
+        if (p.epi.bias != nullptr && in_bounds(col, 1, p.epi.bias_elems, p.epi.status))
+          bias = __ldg(p.epi.bias + col);
+        const int64_t mn = static_cast<int64_t>(m) * p.n;
+        // this warp's m x 32 outputs, staged after the received partials
+        uint32_t *box = reinterpret_cast<uint32_t *>(smem + (S - 1) * m * kSwRows * 4 +
+                                                     (warp - 2) * (m * 32 * 4));
+#pragma unroll
+        for (int j = 0; j < m; j += 2) {
+          const int64_t i0 = static_cast<int64_t>(j) * p.n + col, i1 = i0 + p.n;
+          float f0 = acc[j], f1 = acc[j + 1];
+          if (FMT == 1) {
+            f0 = __fmul_rn(f0, alpha);
+            f1 = __fmul_rn(f1, alpha);
+          }
+          if (p.epi.c != nullptr) {
+            float c0 = 0.0f, c1 = 0.0f;
+            if (in_bounds(i0, 1, p.epi.c_elems, p.epi.status) &&
+                in_bounds(i1, 1, p.epi.c_elems, p.epi.status)) {
+              if constexpr (OUT_F32) {
+                c0 = static_cast<const float *>(p.epi.c)[i0];
+                c1 = static_cast<const float *>(p.epi.c)[i1];
+              } else {
+                c0 = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(p.epi.c)[i0]) << 16);
+                c1 = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(p.epi.c)[i1]) << 16);
+              }
+            }
+            f0 = __fmaf_rn(p.epi.beta, c0, f0);
+            f1 = __fmaf_rn(p.epi.beta, c1, f1);
+          }
+          if (p.epi.bias != nullptr) {
+            f0 = __fadd_rn(f0, bias);
+            f1 = __fadd_rn(f1, bias);
+          }
+          if (p.epi.gelu) {
+            const float2 g = gelu_f32x2(make_float2(f0, f1));
+            f0 = g.x;
+            f1 = g.y;
+          }
+          // rows j, j + 1 of this warp's 32 columns, staged in shared memory
+          // (the ring is idle: rank 0's received partials were already added)
+          if constexpr (OUT_F32) {
+            box[j * 32 + lane] = __float_as_uint(f0);
+            box[(j + 1) * 32 + lane] = __float_as_uint(f1);
+          } else {
+            const uint32_t pk = pack_bf16x2(f0, f1);
+            reinterpret_cast<uint16_t *>(box)[j * 32 + lane] = static_cast<uint16_t>(pk & 0xFFFFu);
+            reinterpret_cast<uint16_t *>(box)[(j + 1) * 32 + lane] = static_cast<uint16_t>(pk >> 16);
+          }
+        }
+        __syncwarp();
+        // 16-byte stores: a row of the box is 32 outputs (64 or 128 bytes)
+        constexpr int kVecPerRow = OUT_F32 ? 8 : 4;  // 16-byte vectors per row
+        const int c0 = col - lane;                   // the warp's first column
+#pragma unroll
+        for (int v = lane; v < m * kVecPerRow; v += 32) {
+          const int j = v / kVecPerRow, e = (v % kVecPerRow) * (OUT_F32 ? 4 : 8);
+          const int64_t gi = static_cast<int64_t>(j) * p.n + c0 + e;
+          const uint4 val = *reinterpret_cast<const uint4 *>(
+              reinterpret_cast<const uint8_t *>(box) + (j * 32 + e) * (OUT_F32 ? 4 : 2));
+          if (in_bounds(gi, OUT_F32 ? 4 : 8, mn, p.status)) {
+            if constexpr (OUT_F32)
+              *reinterpret_cast<uint4 *>(static_cast<float *>(p.d) + gi) = val;
+            else
+              *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.d) + gi) = val;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (S > 1) cluster_sync();  // no CTA leaves while another may still write to it
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kSwTmemCols);
+  }
+}
+
+template <int FMT, int OUT_F32, int MT>
+cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
+  using C = SwapCfg<FMT>;
+  auto kernel = gemm_swap_kernel<FMT, OUT_F32, MT>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  SwapParams p{};
+  p.sfw = static_cast<const uint8_t *>(g.b_scales);
+  p.sfx = static_cast<const uint8_t *>(g.a_scales);
+  p.a_ts = g.a_ts;
+  p.b_ts = g.b_ts;
+  p.status = g.status;
+  p.d = g.d;
+  p.m = static_cast<int>(g.m);
+  p.n = static_cast<int>(g.n);
+  p.k_stages = static_cast<int>(g.k / 256);
+  p.splits = g.split_k;
+  p.stages_per_split = (p.k_stages + g.split_k - 1) / g.split_k;
+  p.katoms = static_cast<int>(g.k / (FMT == 0 ? 128 : 64));
+  p.wrows = g.bn;  // the plan's weight rows per CTA
+  p.epi = g.epi;
+  // shared-memory layout (see SwapCfg): as many slots as shared and tensor
+  // memory hold
+  const int m = 32 * MT;
+  const int guard = (kSwRows - p.wrows) * kSwStageKBytes;
+  const int per_slot = (p.wrows + m) * kSwStageKBytes + 2 * C::kSfBytes;
+  const int fixed = 2 * guard + 1024 /* alignment of the activation ring */ + 256 /* barriers */;
+  int slots = (kSwSmemBytes - fixed - 16 * kSwMaxSlots) / per_slot;
+  slots = slots < kSwMaxSlots ? slots : kSwMaxSlots;
+  const int tmem_slots = (kSwTmemCols - kSwSfCol) / C::kSfSetCols;
+  slots = slots < tmem_slots ? slots : tmem_slots;
+  if (slots < 2) return cudaErrorInvalidValue;
+  p.slots = slots;
+  p.w_off = guard;
+  const int w_end = guard + slots * p.wrows * kSwStageKBytes + guard;
+  p.x_off = (w_end + 1023) / 1024 * 1024;
+  p.sf_off = p.x_off + slots * m * kSwStageKBytes;
+  p.bar_off = p.sf_off + slots * 2 * C::kSfBytes;
+  const int smem_bytes = p.bar_off + 8 * (2 * slots + 3) + 16;
+  // after the main loop the weight ring holds rank 0's received partials
+  // ([S - 1][m][128] FP32 at offset 0), then the four warps' output boxes
+  // (m x 32 each, at most FP32)
+  if (smem_bytes > kSwSmemBytes || (g.split_k - 1) * m * kSwRows * 4 + 4 * m * 32 * 4 > w_end)
+    return cudaErrorInvalidValue;
+  const int blocks = static_cast<int>((g.n + g.bn - 1) / g.bn);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(g.split_k);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks * g.split_k), 1, 1);
+  cfg.blockDim = dim3(kSwThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kernel, *g.tmap_b, *g.tmap_a, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+// Shape of the swapped kernel for N weight rows: rows per CTA (128, 64 or 32)
+// and CTAs per cluster (1, 2 or 4; 4 only for M = 32, whose partials fit the
+// ring three times).  Preference order: whole 128-row slices first (measured
+// on GB300: a CTA streaming 128-row slices reaches about twice the HBM rate of
+// one streaming 64-row slices), split along K over a cluster before the slices
+// get thinner; the first shape whose CTAs fill at least three quarters of the
+// SMs and fit on them at one per SM (each split keeping >= 4 stages of K),
+// else the one with the most CTAs that fit.
+void gemm_swap_shape(int64_t m, int64_t n, int64_t k, int num_sms, int *wrows, int *splits) {
+  const int64_t stages = k / 256;
+  const int64_t want = num_sms - num_sms / 4;
+  const int smax = m <= 32 ? 4 : 2;
+  int best_r = 128, best_s = 1;
+  int64_t best_ctas = 0;
+  for (int r = 128; r >= 32; r /= 2) {
+    for (int sp = 1; sp <= smax; sp *= 2) {
+      if (sp > 1 && stages < 4 * sp) break;
+      const int64_t ctas = (n + r - 1) / r * sp;
+      if (ctas > num_sms) break;
+      if (ctas >= want) {
+        *wrows = r;
+        *splits = sp;
+        return;
+      }
+      if (ctas > best_ctas) {
+        best_ctas = ctas;
+        best_r = r;
+        best_s = sp;
+      }
+    }
+  }
+  *wrows = best_r;
+  *splits = best_s;
+}
+
+cudaError_t launch_gemm_swap(const GemmArgs &g, cudaStream_t s) {
+  if (g.m > kSwMaxM || g.m % 32 != 0 || (g.split_k != 1 && g.split_k != 2 && g.split_k != 4) ||
+      (g.m > 32 && g.split_k > 2) || (g.bn != 128 && g.bn != 64 && g.bn != 32))
+    return cudaErrorInvalidValue;
+  if (g.m == 32) {
+    if (g.fmt == 0) return g.out_fp32 ? launch_typed<0, 1, 1>(g, s) : launch_typed<0, 0, 1>(g, s);
+    return g.out_fp32 ? launch_typed<1, 1, 1>(g, s) : launch_typed<1, 0, 1>(g, s);
+  }
+  if (g.fmt == 0) return g.out_fp32 ? launch_typed<0, 1, 2>(g, s) : launch_typed<0, 0, 2>(g, s);
+  return g.out_fp32 ? launch_typed<1, 1, 2>(g, s) : launch_typed<1, 0, 2>(g, s);
+}
+
+}  // namespace mx

@@ -13,10 +13,36 @@ namespace mx {
 
 // Bit recorded in the device status word when a bounded wait runs out.
 constexpr uint32_t kStatusTimeout = kStatusTimeoutBit;
+// Bit recorded by the bounds-checked build for an access outside its buffer.
+constexpr uint32_t kStatusBounds = kStatusBoundsBit;
 // Longest a kernel waits on one barrier phase before it gives up.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 // Bound on the clean-up waits after an abort.
 constexpr uint64_t kDrainTimeoutNs = 100000000ull;
+
+// Is the access [off, off + len) inside a buffer of `extent` units?  In the
+// library built with -DMX_BOUNDS_CHECK every plain global load and store
+// whose address comes from index arithmetic asks this first: an access
+// outside its buffer is skipped (a load reads zeros) and recorded as
+// kStatusBounds in the device status word, which mx_device_status reports as
+// MX_ERR_DEVICE_BOUNDS.  Nothing traps or faults.  In the release build this
+// is `true` and the checks compile away.  TMA copies need no check: their
+// tensor maps clip them to the tensor.
+__device__ __forceinline__ bool in_bounds(int64_t off, int64_t len, int64_t extent,
+                                          uint32_t *status) {
+#ifdef MX_BOUNDS_CHECK
+  if (off < 0 || off + len > extent) {
+    if (status != nullptr) atomicOr(status, kStatusBounds);
+    return false;
+  }
+#else
+  (void)off;
+  (void)len;
+  (void)extent;
+  (void)status;
+#endif
+  return true;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -342,6 +368,81 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Store to shared memory of another CTA of the cluster (cluster_addr from
+// mapa_shared).
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
+// Arrival on a barrier of any CTA of the cluster, releasing this thread's
+// earlier memory operations (its stores to that CTA included) at cluster
+// scope.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// As mbar_wait, with acquire ordering at cluster scope: for a barrier that
+// other CTAs of the cluster arrive on after writing this CTA's memory.
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity,
+                                                      volatile uint32_t *abort, uint32_t *status) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_acq_cluster(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort = 1u;
+      if (status) atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Copy from this CTA's shared memory to another CTA's of the cluster
+// (dst_cluster and mbar_cluster from mapa_shared); the bytes complete on the
+// destination CTA's barrier.  16-byte aligned addresses, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Brings `bytes` (a multiple of 16) of contiguous global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Brings a tile of a tensor into L2 (no shared memory, no completion to wait
+// for).  Safe before griddep_wait even when the previous kernel writes the
+// tensor: L2 is the point of coherence, so the later loads see its writes.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *tm, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Arrival on a barrier of the peer CTA, without release ordering.  Used to
 // hand tensor memory back after tcgen05.ld: tcgen05.wait::ld has already
 // completed those loads (the values are in registers) before this thread
@@ -505,7 +606,10 @@ __device__ __forceinline__ void epilogue_terms(float *f, const EpiParams &e, int
   static_assert(N == 4 || N == 8, "groups of 4 or 8 outputs");
   if (e.c != nullptr) {
     float cv[N];
-    if constexpr (OUT_F32) {
+    if (!in_bounds(idx, N, e.c_elems, e.status)) {
+#pragma unroll
+      for (int j = 0; j < N; ++j) cv[j] = 0.0f;
+    } else if constexpr (OUT_F32) {
       const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(e.c) + idx);
 #pragma unroll
       for (int i = 0; i < N / 4; ++i) {

@@ -37,6 +37,9 @@ constexpr int kAmaxPartials = 512;
 
 // Bit of the device status word set when a bounded device wait runs out.
 constexpr uint32_t kStatusTimeoutBit = 1u;
+// Bit set by the library built with -DMX_BOUNDS_CHECK when a kernel found a
+// global access outside its buffer (and skipped it).
+constexpr uint32_t kStatusBoundsBit = 2u;
 
 struct QuantizeArgs {
   const void *x;
@@ -47,6 +50,7 @@ struct QuantizeArgs {
   float *tensor_scale;  // NVFP4 only
   uint32_t *partials;   // NVFP4 only: kAmaxPartials words
   int num_sms;
+  uint32_t *status;     // device status word (bounds-checked build)
 };
 
 // Most tensors one quantize launch takes (MX_QUANTIZE_GROUP_MAX).
@@ -72,7 +76,7 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
 // cols % 32 == 0).
 cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld, int tiled,
                                   void *codes, void *scales, void *codes_t, void *scales_t,
-                                  cudaStream_t s);
+                                  uint32_t *status, cudaStream_t s);
 // Bidimensional NVFP4 quantize (rows, cols % 16): the amax pass into
 // `partials` (kAmaxPartials words), then rowwise codes/scales of x and of
 // x^T under one s_t; sr: stochastic rounding (direction 0 rowwise, 1
@@ -80,9 +84,10 @@ cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int
 cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld,
                                      int tiled, void *codes, void *scales, void *codes_t,
                                      void *scales_t, float *tensor_scale, uint32_t *partials,
-                                     const SrArgs *sr, int num_sms, cudaStream_t s);
+                                     const SrArgs *sr, int num_sms, uint32_t *status,
+                                     cudaStream_t s);
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
-                                  cudaStream_t s);
+                                  uint32_t *status, cudaStream_t s);
 
 // Optional GEMM epilogue: D = act(alpha * acc + beta * C + bias), act = GELU
 // (y * Phi(y)) or the identity.  c: the prior contents of D (same dtype and
@@ -92,6 +97,9 @@ struct EpiParams {
   const void *c;
   float beta;
   int gelu;
+  int64_t c_elems;     // elements of c (M * N), for the bounds-checked build
+  int64_t bias_elems;  // elements of bias (N)
+  uint32_t *status;    // device status word (bounds-checked build)
 };
 
 struct GemmArgs {
@@ -108,8 +116,9 @@ struct GemmArgs {
   int64_t m, n, k;
   int split_k;   // >= 1, already resolved
   EpiParams epi; // all null / 0: plain epilogue
-  int bn;        // single-CTA kernel: 128 or 256
+  int bn;        // single-CTA kernel: 128 or 256; swapped kernel: weight rows per CTA
   int pair;      // 1: CTA-pair kernel with 256 x 256 tiles
+  int swap;      // 1: swapped-operand kernel for M <= 64 (split_k = CTAs per cluster)
   float *workspace;
   uint32_t *status;
   int num_sms;
@@ -117,12 +126,24 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s);
 cudaError_t launch_gemm_pair(const GemmArgs &a, cudaStream_t s);
+cudaError_t launch_gemm_swap(const GemmArgs &a, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const GemmArgs &a, cudaStream_t s);
 
-// Kernel (single CTA with tile width bn, or CTA pair) and split count the
-// GEMM uses for a shape (split_k 0 = auto).
-void gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms, int *bn, int *splits,
-               int *pair);
+// The kernel a GEMM shape runs on, and its split of K.
+enum GemmKind { kGemmSingle = 0, kGemmPair = 1, kGemmSwap = 2 };
+struct GemmPlan {
+  int kind;    // GemmKind
+  int bn;      // single-CTA kernel: tile width 128 or 256; swap: weight rows per CTA
+  int splits;  // K ranges (swap: CTAs of a cluster, summed in shared memory)
+  // FP32 partials [splits, M, N] in the caller's workspace (then the reduce kernel)
+  bool workspace() const { return kind != kGemmSwap && splits > 1; }
+};
+// split_k 0 = auto: M <= 64 takes the swapped kernel; otherwise the pair
+// kernel for M > 128, the single-CTA kernel (with split-K when its tiles
+// cannot fill the GPU) for M <= 128.  An explicit split_k keeps the
+// workspace-and-reduce path of the single-CTA or pair kernel.
+GemmPlan gemm_plan(int64_t m, int64_t n, int64_t k, int split_k, int num_sms);
+void gemm_swap_shape(int64_t m, int64_t n, int64_t k, int num_sms, int *wrows, int *splits);
 
 // Columns per output box of the GEMM epilogue (64 bytes of BF16 or FP32).
 int gemm_out_box_cols(int out_fp32, int split_k);

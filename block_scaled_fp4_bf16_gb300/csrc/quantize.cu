@@ -66,10 +66,13 @@ struct QTensor {
   uint32_t katoms;
   FastDiv kbdiv;                // kb = cols / block
   int tiled;
+  int64_t x_elems;              // extents of x (elements), codes and scales (bytes)
+  int64_t codes_bytes, scales_bytes;
 };
 
 struct QGroup {
   int count;
+  uint32_t *status;             // device status word (bounds-checked build)
   // NVFP4 stochastic rounding (the kernels instantiated for it read these)
   uint32_t sr_key0, sr_key1, sr_direction;
   int sr_rounds;
@@ -103,6 +106,27 @@ __device__ __forceinline__ void load32(const void *p, uint32_t *w) {
     asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
                  : "l"(static_cast<const uint8_t *>(p) + 16));
+  }
+}
+
+// A global store or a 16-element x load of the quantize kernels, checked
+// against its buffer's extent in the bounds-checked build (in_bounds; a
+// load outside reads zeros).
+template <typename T>
+__device__ __forceinline__ void st_g(uint8_t *base, int64_t off, T v, int64_t extent,
+                                     uint32_t *status) {
+  if (in_bounds(off, static_cast<int64_t>(sizeof(T)), extent, status))
+    *reinterpret_cast<T *>(base + off) = v;
+}
+
+template <bool WIDE>
+__device__ __forceinline__ void load32_x(const uint16_t *x, int64_t off, int64_t x_elems,
+                                         uint32_t *status, uint32_t *w) {
+  if (in_bounds(off, 16, x_elems, status)) {
+    load32<WIDE>(x + off, w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0u;
   }
 }
 
@@ -172,10 +196,10 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const __grid_cons
   uint8_t *__restrict__ scales = t.scales;
   uint32_t sbyte = 0;
   if (r < t.rows) {
-    const uint16_t *src = t.x + static_cast<int64_t>(r) * t.ld + j * 32u;
+    const int64_t xo = static_cast<int64_t>(r) * t.ld + j * 32u;
     uint32_t w[16];
-    load32<WIDE>(src, &w[0]);
-    load32<WIDE>(src + 16, &w[8]);
+    load32_x<WIDE>(t.x, xo, t.x_elems, g.status, &w[0]);
+    load32_x<WIDE>(t.x, xo + 16, t.x_elems, g.status, &w[8]);
     const uint32_t amax = block_amax<16>(w);
     const int e = amax ? max(bf16_floor_log2(amax) - 2, -127) : -127;
     const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
@@ -184,15 +208,17 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_kernel(const __grid_cons
     out.y = scale_to_e2m1x8(&w[4], inv);
     out.z = scale_to_e2m1x8(&w[8], inv);
     out.w = scale_to_e2m1x8(&w[12], inv);
-    *reinterpret_cast<uint4 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 16u) = out;
+    st_g(t.codes, static_cast<int64_t>(r) * (t.cols >> 1) + j * 16u, out, t.codes_bytes, g.status);
     sbyte = static_cast<uint32_t>(e + 127);
   }
   if (t.tiled) {
-    scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sbyte);
+    st_g(scales, tiled_offset(r, j, t.katoms), static_cast<uint8_t>(sbyte), t.scales_bytes, g.status);
     if (j == kb - 1)
-      for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
+      for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj)
+        st_g(scales, tiled_offset(r, jj, t.katoms), uint8_t(0), t.scales_bytes, g.status);
   } else {
-    scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sbyte);
+    st_g(scales, static_cast<int64_t>(r) * kb + j, static_cast<uint8_t>(sbyte), t.scales_bytes,
+         g.status);
   }
 }
 
@@ -214,7 +240,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const __grid_const
     for (int q = 0; q < 4; ++q) {
       const uint32_t bq = b + q * stride;
       const uint32_t r = fast_div(bq, t.kbdiv);
-      load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + (bq - r * t.kbdiv.d) * 16u, w[q]);
+      load32_x<WIDE>(t.x, static_cast<int64_t>(r) * t.ld + (bq - r * t.kbdiv.d) * 16u, t.x_elems,
+                     g.status, w[q]);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) m = max(m, block_amax<8>(w[q]));
@@ -222,7 +249,8 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const __grid_const
   for (; b < t.real_total; b += stride) {
     const uint32_t r = fast_div(b, t.kbdiv);
     uint32_t w[8];
-    load32<WIDE>(t.x + static_cast<int64_t>(r) * t.ld + (b - r * t.kbdiv.d) * 16u, w);
+    load32_x<WIDE>(t.x, static_cast<int64_t>(r) * t.ld + (b - r * t.kbdiv.d) * 16u, t.x_elems,
+                   g.status, w);
     m = max(m, block_amax<8>(w));
   }
 #pragma unroll
@@ -234,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_amax_kernel(const __grid_const
     uint32_t v = 0;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) v = max(v, warp_max[w]);
-    t.partials[blockIdx.x] = v;
+    if (in_bounds(blockIdx.x, 1, kAmaxPartials, g.status)) t.partials[blockIdx.x] = v;
   }
 }
 
@@ -540,7 +568,8 @@ __device__ __forceinline__ void nv_load_chunk(const QGroup &g, uint32_t chunk, N
 #pragma unroll
   for (int q = 0; q < kNvBlocksPerThread; ++q)
     if (k.b0 + q < t.total && k.r[q] < t.rows)
-      load32<WIDE>(t.x + static_cast<int64_t>(k.r[q]) * t.ld + k.j[q] * 16u, k.w[q]);
+      load32_x<WIDE>(t.x, static_cast<int64_t>(k.r[q]) * t.ld + k.j[q] * 16u, t.x_elems, g.status,
+                     k.w[q]);
 }
 
 template <bool WIDE, int SR>
@@ -579,16 +608,17 @@ __global__ void __launch_bounds__(kThreads, nv_ctas_per_sm(SR)) nvfp4_quantize_k
                            g.sr_key0, g.sr_key1, g.sr_rounds, o0);
         sb1 = nv_block<SR>(cur.w[1], c, den_tab[cur.ti], rcp_tab[cur.ti], j + 1, r,
                            g.sr_direction, g.sr_key0, g.sr_key1, g.sr_rounds, o1);
-        *reinterpret_cast<uint4 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) =
-            make_uint4(o0.x, o0.y, o1.x, o1.y);
+        st_g(t.codes, static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u,
+             make_uint4(o0.x, o0.y, o1.x, o1.y), t.codes_bytes, g.status);
       }
       const uint16_t s2 = static_cast<uint16_t>(sb0 | (sb1 << 8));
       if (t.tiled) {
-        *reinterpret_cast<uint16_t *>(scales + tiled_offset(r, j, t.katoms)) = s2;
+        st_g(scales, tiled_offset(r, j, t.katoms), s2, t.scales_bytes, g.status);
         if (j + 2 == kb)
-          for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
+          for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj)
+            st_g(scales, tiled_offset(r, jj, t.katoms), uint8_t(0), t.scales_bytes, g.status);
       } else {
-        *reinterpret_cast<uint16_t *>(scales + static_cast<int64_t>(r) * kb + j) = s2;
+        st_g(scales, static_cast<int64_t>(r) * kb + j, s2, t.scales_bytes, g.status);
       }
       continue;
     }
@@ -601,14 +631,18 @@ __global__ void __launch_bounds__(kThreads, nv_ctas_per_sm(SR)) nvfp4_quantize_k
         uint2 out;
         sb = nv_block<SR>(cur.w[q], c, den_tab[cur.ti], rcp_tab[cur.ti], j, r, g.sr_direction,
                           g.sr_key0, g.sr_key1, g.sr_rounds, out);
-        *reinterpret_cast<uint2 *>(t.codes + static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u) = out;
+        st_g(t.codes, static_cast<int64_t>(r) * (t.cols >> 1) + j * 8u, out, t.codes_bytes,
+             g.status);
       }
       if (t.tiled) {
-        scales[tiled_offset(r, j, t.katoms)] = static_cast<uint8_t>(sb);
+        st_g(scales, tiled_offset(r, j, t.katoms), static_cast<uint8_t>(sb), t.scales_bytes,
+             g.status);
         if (j == kb - 1)
-          for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj) scales[tiled_offset(r, jj, t.katoms)] = 0;
+          for (uint32_t jj = kb; jj < t.katoms * 4u; ++jj)
+            st_g(scales, tiled_offset(r, jj, t.katoms), uint8_t(0), t.scales_bytes, g.status);
       } else {
-        scales[static_cast<int64_t>(r) * kb + j] = static_cast<uint8_t>(sb);
+        st_g(scales, static_cast<int64_t>(r) * kb + j, static_cast<uint8_t>(sb), t.scales_bytes,
+             g.status);
       }
     }
   }
@@ -644,6 +678,9 @@ struct Q2dArgs {
   uint32_t kb, kbt;             // scale columns of x and of x^T (cols / 32, rows / 32)
   uint32_t katoms, katoms_t;    // 4-scale atoms along a row of x and of x^T
   uint32_t rows_pad, cols_pad;  // rows of x and of x^T with tiled padding
+  int64_t x_elems, codes_bytes; // extents (bounds-checked build): x, each code buffer,
+  int64_t scales_bytes, scales_t_bytes;  // the scales of x and of x^T
+  uint32_t *status;
 };
 
 // Codes and scale byte of one 32-element block given as 16 BF16x2 words.
@@ -674,9 +711,9 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_2d_kernel(const __grid_c
     const bool inside = r < a.rows && j < a.kb;
     uint32_t w[16];
     if (inside) {
-      const uint16_t *src = a.x + static_cast<int64_t>(r) * a.ld + j * 32u;
-      load32<WIDE>(src, &w[0]);
-      load32<WIDE>(src + 16, &w[8]);
+      const int64_t xo = static_cast<int64_t>(r) * a.ld + j * 32u;
+      load32_x<WIDE>(a.x, xo, a.x_elems, a.status, &w[0]);
+      load32_x<WIDE>(a.x, xo + 16, a.x_elems, a.status, &w[8]);
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) w[i] = 0u;
@@ -690,13 +727,16 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_2d_kernel(const __grid_c
     if (inside) {
       uint4 out;
       sbyte = mx_block_codes(w, out);
-      *reinterpret_cast<uint4 *>(a.codes + static_cast<int64_t>(r) * (a.cols >> 1) + j * 16u) = out;
+      st_g(a.codes, static_cast<int64_t>(r) * (a.cols >> 1) + j * 16u, out, a.codes_bytes,
+           a.status);
     }
     if (a.tiled) {
       if (r < a.rows_pad && j < a.katoms * 4u)
-        a.scales[tiled_offset(r, j, a.katoms)] = static_cast<uint8_t>(sbyte);
+        st_g(a.scales, tiled_offset(r, j, a.katoms), static_cast<uint8_t>(sbyte), a.scales_bytes,
+             a.status);
     } else if (inside) {
-      a.scales[static_cast<int64_t>(r) * a.kb + j] = static_cast<uint8_t>(sbyte);
+      st_g(a.scales, static_cast<int64_t>(r) * a.kb + j, static_cast<uint8_t>(sbyte),
+           a.scales_bytes, a.status);
     }
   }
   __syncthreads();
@@ -721,13 +761,16 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_2d_kernel(const __grid_c
     if (inside) {
       uint4 out;
       sbyte = mx_block_codes(qc ? hi : lo, out);
-      *reinterpret_cast<uint4 *>(a.codes_t + static_cast<int64_t>(col) * (a.rows >> 1) + i * 16u) = out;
+      st_g(a.codes_t, static_cast<int64_t>(col) * (a.rows >> 1) + i * 16u, out, a.codes_bytes,
+           a.status);
     }
     if (a.tiled) {
       if (col < a.cols_pad && i < a.katoms_t * 4u)
-        a.scales_t[tiled_offset(col, i, a.katoms_t)] = static_cast<uint8_t>(sbyte);
+        st_g(a.scales_t, tiled_offset(col, i, a.katoms_t), static_cast<uint8_t>(sbyte),
+             a.scales_t_bytes, a.status);
     } else if (inside) {
-      a.scales_t[static_cast<int64_t>(col) * a.kbt + i] = static_cast<uint8_t>(sbyte);
+      st_g(a.scales_t, static_cast<int64_t>(col) * a.kbt + i, static_cast<uint8_t>(sbyte),
+           a.scales_t_bytes, a.status);
     }
   }
 }
@@ -761,6 +804,9 @@ struct Nv2dArgs {
   uint32_t key0, key1;          // Philox key (stochastic rounding)
   int rounds;
   uint32_t tiles_x, tiles;      // tiles along a row, and in all
+  int64_t x_elems, codes_bytes; // extents (bounds-checked build): x, each code buffer,
+  int64_t scales_bytes, scales_t_bytes;  // the scales of x and of x^T
+  uint32_t *status;
 };
 
 // Loads the row blocks of tile `tile` (zeros outside x).
@@ -772,7 +818,7 @@ __device__ __forceinline__ void nv2d_load_tile(const Nv2dArgs &a, uint32_t tile,
     const uint32_t idx = threadIdx.x + h * kThreads;
     const uint32_t r = r0 + (idx >> 4), j = c0 / 16 + (idx & 15);
     if (r < a.rows && j < a.kb) {
-      load32<WIDE>(a.x + static_cast<int64_t>(r) * a.ld + j * 16u, w[h]);
+      load32_x<WIDE>(a.x, static_cast<int64_t>(r) * a.ld + j * 16u, a.x_elems, a.status, w[h]);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[h][i] = 0u;
@@ -812,13 +858,16 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __
       if (inside) {
         uint2 out;
         sb = nv_block<SR>(w[h], c, den_tab, rcp_tab, j, r, 0u, a.key0, a.key1, a.rounds, out);
-        *reinterpret_cast<uint2 *>(a.codes + static_cast<int64_t>(r) * (a.cols >> 1) + j * 8u) = out;
+        st_g(a.codes, static_cast<int64_t>(r) * (a.cols >> 1) + j * 8u, out, a.codes_bytes,
+             a.status);
       }
       if (a.tiled) {
         if (r < a.rows_pad && j < a.katoms * 4u)
-          a.scales[tiled_offset(r, j, a.katoms)] = static_cast<uint8_t>(sb);
+          st_g(a.scales, tiled_offset(r, j, a.katoms), static_cast<uint8_t>(sb), a.scales_bytes,
+               a.status);
       } else if (inside) {
-        a.scales[static_cast<int64_t>(r) * a.kb + j] = static_cast<uint8_t>(sb);
+        st_g(a.scales, static_cast<int64_t>(r) * a.kb + j, static_cast<uint8_t>(sb),
+             a.scales_bytes, a.status);
       }
     }
     __syncthreads();
@@ -848,13 +897,16 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __
           uint2 out;
           sb = nv_block<SR>(qc ? hi : lo, c, den_tab, rcp_tab, i, col, 1u, a.key0, a.key1, a.rounds,
                             out);
-          *reinterpret_cast<uint2 *>(a.codes_t + static_cast<int64_t>(col) * (a.rows >> 1) + i * 8u) = out;
+          st_g(a.codes_t, static_cast<int64_t>(col) * (a.rows >> 1) + i * 8u, out, a.codes_bytes,
+               a.status);
         }
         if (a.tiled) {
           if (col < a.cols_pad && i < a.katoms_t * 4u)
-            a.scales_t[tiled_offset(col, i, a.katoms_t)] = static_cast<uint8_t>(sb);
+            st_g(a.scales_t, tiled_offset(col, i, a.katoms_t), static_cast<uint8_t>(sb),
+                 a.scales_t_bytes, a.status);
         } else if (inside) {
-          a.scales_t[static_cast<int64_t>(col) * a.kbt + i] = static_cast<uint8_t>(sb);
+          st_g(a.scales_t, static_cast<int64_t>(col) * a.kbt + i, static_cast<uint8_t>(sb),
+               a.scales_t_bytes, a.status);
         }
       }
     }
@@ -868,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 4) nvfp4_quantize_2d_kernel(const __
 // Plain [rows, kb] -> tiled order; one thread per output byte (padding 0).
 __global__ void __launch_bounds__(kThreads) scale_relayout_kernel(
     const uint8_t *__restrict__ plain, int64_t rows, int64_t kb, uint8_t *__restrict__ tiled,
-    int64_t total) {
+    int64_t total, uint32_t *status) {
   griddep_launch_dependents();
   griddep_wait();
   const int64_t katoms = (kb + 3) >> 2;
@@ -879,7 +931,9 @@ __global__ void __launch_bounds__(kThreads) scale_relayout_kernel(
     const int64_t rt = atom / katoms, ka = atom - rt * katoms;
     const int64_t r = rt * 128 + (w >> 4) + ((w >> 2) & 3) * 32;
     const int64_t c = ka * 4 + (w & 3);
-    tiled[o] = (r < rows && c < kb) ? plain[r * kb + c] : static_cast<uint8_t>(0);
+    uint8_t v = 0;
+    if (r < rows && c < kb && in_bounds(r * kb + c, 1, rows * kb, status)) v = plain[r * kb + c];
+    if (in_bounds(o, 1, total, status)) tiled[o] = v;
   }
 }
 
@@ -897,6 +951,7 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
   const uint32_t block = fmt == 0 ? 32u : 16u;
   QGroup g{};
   g.count = count;
+  g.status = tensors[0].status;
   if (sr) {
     g.sr_key0 = static_cast<uint32_t>(sr->seed);
     g.sr_key1 = static_cast<uint32_t>(sr->seed >> 32);
@@ -926,6 +981,9 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
     t.katoms = (kb + 3) / 4;
     t.kbdiv = make_fastdiv(kb);
     t.tiled = a.tiled;
+    t.x_elems = (a.rows - 1) * a.ld + a.cols;
+    t.codes_bytes = a.rows * a.cols / 2;
+    t.scales_bytes = static_cast<int64_t>(a.tiled ? rows_pad * (t.katoms * 4u) : t.rows * kb);
     const uint32_t per_cta = kThreads * (fmt == 0 ? 1u : static_cast<uint32_t>(kNvBlocksPerThread));
     t.nchunks = (t.total + per_cta - 1) / per_cta;
     ctas += t.nchunks;
@@ -956,7 +1014,7 @@ cudaError_t launch_quantize_group(int fmt, const QuantizeArgs *tensors, int coun
 
 cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld, int tiled,
                                   void *codes, void *scales, void *codes_t, void *scales_t,
-                                  cudaStream_t s) {
+                                  uint32_t *status, cudaStream_t s) {
   Q2dArgs a{};
   a.x = static_cast<const uint16_t *>(x);
   a.ld = ld;
@@ -973,6 +1031,11 @@ cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int
   a.katoms_t = (a.kbt + 3) / 4;
   a.rows_pad = tiled ? (a.rows + 127) / 128 * 128 : a.rows;
   a.cols_pad = tiled ? (a.cols + 127) / 128 * 128 : a.cols;
+  a.x_elems = (rows - 1) * ld + cols;
+  a.codes_bytes = rows * cols / 2;
+  a.scales_bytes = static_cast<int64_t>(a.rows_pad) * (tiled ? a.katoms * 4 : a.kb);
+  a.scales_t_bytes = static_cast<int64_t>(a.cols_pad) * (tiled ? a.katoms_t * 4 : a.kbt);
+  a.status = status;
   // the tiles cover the tiled padding of both outputs
   const uint32_t gx = (a.cols_pad + k2dCols - 1) / k2dCols;
   const uint32_t gy = (a.rows_pad + k2dRows - 1) / k2dRows;
@@ -986,7 +1049,8 @@ cudaError_t launch_mx_quantize_2d(const void *x, int64_t rows, int64_t cols, int
 cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, int64_t ld,
                                      int tiled, void *codes, void *scales, void *codes_t,
                                      void *scales_t, float *tensor_scale, uint32_t *partials,
-                                     const SrArgs *sr, int num_sms, cudaStream_t s) {
+                                     const SrArgs *sr, int num_sms, uint32_t *status,
+                                     cudaStream_t s) {
   if (sr && (sr->rounds < 1 || sr->rounds > kPhiloxMaxRounds)) return cudaErrorInvalidValue;
   const bool wide = wide_ok(x, ld);
   // pass 1: the tensor's partial maxima
@@ -1000,6 +1064,8 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
   t.cols = static_cast<uint32_t>(cols);
   t.real_total = t.rows * (t.cols / 16u);
   t.kbdiv = make_fastdiv(t.cols / 16u);
+  t.x_elems = (rows - 1) * ld + cols;
+  g.status = status;
   cudaError_t e = launch_pdl(wide ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>,
                              dim3(kAmaxPartials, 1), dim3(kThreads), 0, s, g);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -1022,6 +1088,11 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
   a.katoms_t = (a.kbt + 3) / 4;
   a.rows_pad = tiled ? (a.rows + 127) / 128 * 128 : a.rows;
   a.cols_pad = tiled ? (a.cols + 127) / 128 * 128 : a.cols;
+  a.x_elems = (rows - 1) * ld + cols;
+  a.codes_bytes = rows * cols / 2;
+  a.scales_bytes = static_cast<int64_t>(a.rows_pad) * (tiled ? a.katoms * 4 : a.kb);
+  a.scales_t_bytes = static_cast<int64_t>(a.cols_pad) * (tiled ? a.katoms_t * 4 : a.kbt);
+  a.status = status;
   if (sr) {
     a.key0 = static_cast<uint32_t>(sr->seed);
     a.key1 = static_cast<uint32_t>(sr->seed >> 32);
@@ -1045,14 +1116,14 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
 }
 
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
-                                  cudaStream_t s) {
+                                  uint32_t *status, cudaStream_t s) {
   const int64_t total = (rows + 127) / 128 * 128 * ((kb + 3) / 4 * 4);
   int64_t grid = (total + kThreads - 1) / kThreads;
   if (grid > 65536) grid = 65536;
   const cudaError_t e =
       launch_pdl(scale_relayout_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
                  static_cast<const uint8_t *>(plain), rows, kb, static_cast<uint8_t *>(tiled),
-                 total);
+                 total, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

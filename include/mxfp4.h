@@ -64,6 +64,8 @@ extern "C" {
 #define MX_ERR_WORKSPACE (-7)           /* workspace missing or too small         */
 #define MX_ERR_CUDA (-8)                /* CUDA runtime / driver / launch error   */
 #define MX_ERR_DEVICE_TIMEOUT (-9)      /* a bounded device-side wait ran out     */
+#define MX_ERR_DEVICE_BOUNDS (-10)      /* bounds-checked build: an access outside
+                                           its buffer was found and skipped     */
 
 /* ---- enums ----------------------------------------------------------- */
 #define MX_FMT_MXFP4 0    /* UE8M0 scale per 32 elements                      */
@@ -76,6 +78,15 @@ extern "C" {
 
 #define MX_OUT_BF16 0
 #define MX_OUT_FP32 1
+
+/* How the library was built: MX_BUILD_BOUNDS_CHECK is set in the build made
+ * with -DMX_BOUNDS_CHECK, whose kernels check every plain global load and
+ * store computed from an index against the extent of its buffer; an access
+ * outside is skipped (loads read 0) and mx_device_status then returns
+ * MX_ERR_DEVICE_BOUNDS.  That build is a test instrument (a memory checker
+ * where none can run); the release build has no checks. */
+#define MX_BUILD_BOUNDS_CHECK 1
+int mx_build_flags(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *mx_error_string(int code);

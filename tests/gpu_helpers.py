@@ -18,6 +18,43 @@ import oracle
 
 FP32_REL_TOL = 1e-5
 
+# Guard bands: every output a helper hands to the library sits between two
+# GUARD_BYTES runs of GUARD_FILL bytes, checked after the call, so a write past
+# either end of a buffer (a ragged tile, a padding row, a split-K partial)
+# fails the test even when it lands in memory nothing else reads.  With
+# compute-sanitizer unavailable, this and the bounds-checked build
+# (-DMX_BOUNDS_CHECK) stand in for its memcheck.
+GUARD_BYTES = 4096
+GUARD_FILL = 0x5A
+
+
+def guarded(n: int, dtype=torch.uint8, fill=None) -> torch.Tensor:
+    """A contiguous device tensor of n elements with guard bands on both sides;
+    the body is filled with `fill` (left at the guard pattern when None)."""
+    esize = torch.empty((), dtype=dtype).element_size()
+    nbytes = n * esize
+    raw = torch.full((nbytes + 2 * GUARD_BYTES,), GUARD_FILL, dtype=torch.uint8, device="cuda")
+    body = raw[GUARD_BYTES:GUARD_BYTES + nbytes].view(dtype)
+    if fill is not None:
+        body.fill_(fill)
+    body._mx_guard = (raw, nbytes)
+    return body
+
+
+def check_guards(*tensors, what: str = ""):
+    """Assert that no guard byte of the given guarded tensors changed."""
+    for t in tensors:
+        if t is None or not hasattr(t, "_mx_guard"):
+            continue
+        raw, nbytes = t._mx_guard
+        for name, band in (("before", raw[:GUARD_BYTES]), ("after", raw[GUARD_BYTES + nbytes:])):
+            bad = (band != GUARD_FILL).nonzero()
+            if bad.numel():
+                off = int(bad[0]) - (GUARD_BYTES if name == "before" else 0)
+                raise AssertionError(f"{what}: {bad.numel()} byte(s) written {name} a buffer of "
+                                     f"{nbytes} bytes (first at offset {off} from its "
+                                     f"{'start' if name == 'before' else 'end'})")
+
 
 def dev_u8(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
@@ -38,16 +75,15 @@ def gpu_quantize(x_bits: np.ndarray, fmt: int, layout: int, ld: int | None = Non
         padded = np.zeros((rows, ld), np.uint16)
         padded[:, :cols] = x_bits
         x = dev_bf16(padded)
-    codes = torch.empty(rows * cols // 2, dtype=torch.uint8, device="cuda")
-    scales = torch.empty(mx.mx_scale_bytes(rows, cols, fmt, layout), dtype=torch.uint8,
-                         device="cuda")
+    codes = guarded(rows * cols // 2, fill=0xAB)
+    scales = guarded(mx.mx_scale_bytes(rows, cols, fmt, layout), fill=0xAB)
     ts = ws = None
     if fmt == mx.MX_FMT_NVFP4:
-        ts = torch.empty(1, dtype=torch.float32, device="cuda")
-        ws = torch.empty(mx.mx_quantize_workspace_bytes(rows, cols, fmt), dtype=torch.uint8,
-                         device="cuda")
+        ts = guarded(1, torch.float32, -1.0)
+        ws = guarded(mx.mx_quantize_workspace_bytes(rows, cols, fmt))
     mx.mx_quantize_bf16(x, rows, cols, ld, fmt, layout, codes, scales, ts, ws)
     torch.cuda.synchronize()
+    check_guards(codes, scales, ts, ws, what=f"quantize {rows}x{cols}")
     s_t = None if ts is None else np.float32(ts.item())
     return codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(), s_t
 
@@ -62,14 +98,13 @@ def gpu_quantize_sr(x_bits: np.ndarray, seed: int, rounds: int = 10, layout: int
     padded[:, :cols] = x_bits
     x = dev_bf16(padded)
     fmt = mx.MX_FMT_NVFP4
-    codes = torch.full((rows * cols // 2,), 0xAB, dtype=torch.uint8, device="cuda")
-    scales = torch.full((mx.mx_scale_bytes(rows, cols, fmt, layout),), 0xAB, dtype=torch.uint8,
-                        device="cuda")
-    ts = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
-    ws = torch.empty(mx.mx_quantize_workspace_bytes(rows, cols, fmt), dtype=torch.uint8,
-                     device="cuda")
+    codes = guarded(rows * cols // 2, fill=0xAB)
+    scales = guarded(mx.mx_scale_bytes(rows, cols, fmt, layout), fill=0xAB)
+    ts = guarded(1, torch.float32, -1.0)
+    ws = guarded(mx.mx_quantize_workspace_bytes(rows, cols, fmt))
     mx.nvfp4_quantize_bf16_sr(x, rows, cols, ld, layout, codes, scales, ts, seed, rounds, ws)
     torch.cuda.synchronize()
+    check_guards(codes, scales, ts, ws, what=f"stochastic quantize {rows}x{cols}")
     return (codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(),
             np.float32(ts.item()))
 
@@ -86,17 +121,19 @@ def gpu_quantize_group(xs, fmt: int, layout: int, lds=None):
         padded = np.zeros((rows, ld), np.uint16)
         padded[:, :cols] = x_bits
         x = dev_bf16(padded)
-        codes = torch.full((rows * cols // 2,), 0xAB, dtype=torch.uint8, device="cuda")
-        scales = torch.full((mx.mx_scale_bytes(rows, cols, fmt, layout),), 0xAB,
-                            dtype=torch.uint8, device="cuda")
-        ts = torch.full((1,), -1.0, dtype=torch.float32, device="cuda") if fmt == mx.MX_FMT_NVFP4 else None
+        codes = guarded(rows * cols // 2, fill=0xAB)
+        scales = guarded(mx.mx_scale_bytes(rows, cols, fmt, layout), fill=0xAB)
+        ts = guarded(1, torch.float32, -1.0) if fmt == mx.MX_FMT_NVFP4 else None
         keep.append(x)
         tensors.append((x, rows, cols, ld, codes, scales, ts))
         outs.append((rows, cols, codes, scales, ts))
     wsb = mx.mx_quantize_group_workspace_bytes(len(xs), fmt)
-    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+    ws = guarded(wsb) if wsb else None
     mx.mx_quantize_bf16_group(tensors, fmt, layout, ws)
     torch.cuda.synchronize()
+    for rows, cols, codes, scales, ts in outs:
+        check_guards(codes, scales, ts, what=f"group quantize {rows}x{cols}")
+    check_guards(ws, what="group quantize workspace")
     return [(codes.cpu().numpy().reshape(rows, cols // 2), scales.cpu().numpy(),
              None if ts is None else np.float32(ts.item())) for rows, cols, codes, scales, ts in outs]
 
@@ -111,7 +148,7 @@ def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
     padded = np.zeros((rows, ld), np.uint16)
     padded[:, :cols] = x_bits
     x = dev_bf16(padded)
-    fill = lambda n: torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")
+    fill = lambda n: guarded(n, fill=0xAB)  # noqa: E731
     fmt = mx.MX_FMT_MXFP4
     codes, codes_t = fill(rows * cols // 2), fill(rows * cols // 2)
     scales = fill(mx.mx_scale_bytes(rows, cols, fmt, layout))
@@ -120,6 +157,7 @@ def gpu_quantize_2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
         codes = scales = None
     mx.mx_quantize_bf16_2d(x, rows, cols, ld, fmt, layout, codes, scales, codes_t, scales_t)
     torch.cuda.synchronize()
+    check_guards(codes, scales, codes_t, scales_t, what=f"bidimensional quantize {rows}x{cols}")
     return (None if codes is None else codes.cpu().numpy().reshape(rows, cols // 2),
             None if scales is None else scales.cpu().numpy(),
             codes_t.cpu().numpy().reshape(cols, rows // 2), scales_t.cpu().numpy())
@@ -135,19 +173,20 @@ def gpu_quantize_nv2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
     padded = np.zeros((rows, ld), np.uint16)
     padded[:, :cols] = x_bits
     x = dev_bf16(padded)
-    fill = lambda n: torch.full((n,), 0xAB, dtype=torch.uint8, device="cuda")
+    fill = lambda n: guarded(n, fill=0xAB)  # noqa: E731
     fmt = mx.MX_FMT_NVFP4
     codes, codes_t = fill(rows * cols // 2), fill(rows * cols // 2)
     scales = fill(mx.mx_scale_bytes(rows, cols, fmt, layout))
     scales_t = fill(mx.mx_scale_bytes(cols, rows, fmt, layout))
-    ts = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
-    ws = torch.empty(mx.mx_quantize_workspace_bytes(rows, cols, fmt), dtype=torch.uint8,
-                     device="cuda")
+    ts = guarded(1, torch.float32, -1.0)
+    ws = guarded(mx.mx_quantize_workspace_bytes(rows, cols, fmt))
     if columnwise_only:
         codes = scales = None
     mx.nvfp4_quantize_bf16_2d(x, rows, cols, ld, layout, codes, scales, codes_t, scales_t, ts,
                               0 if seed is None else 1, 0 if seed is None else seed, rounds, ws)
     torch.cuda.synchronize()
+    check_guards(codes, scales, codes_t, scales_t, ts, ws,
+                 what=f"bidimensional NVFP4 quantize {rows}x{cols}")
     return (None if codes is None else codes.cpu().numpy().reshape(rows, cols // 2),
             None if scales is None else scales.cpu().numpy(),
             codes_t.cpu().numpy().reshape(cols, rows // 2), scales_t.cpu().numpy(),
@@ -155,9 +194,10 @@ def gpu_quantize_nv2d(x_bits: np.ndarray, layout: int, ld: int | None = None,
 
 
 def gpu_relayout(plain: np.ndarray, rows: int, cols: int, fmt: int) -> torch.Tensor:
-    tiled = torch.full((mx.mx_scale_bytes(rows, cols, fmt, mx.MX_SCALE_TCGEN05),), 0xAB,
-                       dtype=torch.uint8, device="cuda")
+    tiled = guarded(mx.mx_scale_bytes(rows, cols, fmt, mx.MX_SCALE_TCGEN05), fill=0xAB)
     mx.mx_scale_relayout(dev_u8(plain), rows, cols, fmt, tiled)
+    torch.cuda.synchronize()
+    check_guards(tiled, what=f"scale relayout {rows}x{cols}")
     return tiled
 
 
@@ -168,11 +208,11 @@ def gpu_gemm(fmt, a_codes, a_scales_tiled, b_codes, b_scales_tiled, m, n, k, out
     def on_dev(a):
         return a if isinstance(a, torch.Tensor) else dev_u8(a)
     dt = torch.float32 if out_fp32 else torch.bfloat16
-    d = torch.empty((m, n), dtype=dt, device="cuda")
-    if prefill_nan:
-        d.fill_(float("nan"))
+    body = guarded(m * n, dt, float("nan") if prefill_nan else 0.0)
+    d = body.view(m, n)
+    d._mx_guard = body._mx_guard
     wsb = mx.mx_gemm_workspace_bytes(m, n, k, split_k)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
+    ws = guarded(max(wsb, 16)) if wsb else None
     od = mx.MX_OUT_FP32 if out_fp32 else mx.MX_OUT_BF16
     if fmt == mx.MX_FMT_MXFP4:
         mx.mxfp4_gemm(on_dev(a_codes), on_dev(a_scales_tiled), on_dev(b_codes),
@@ -186,6 +226,7 @@ def gpu_gemm(fmt, a_codes, a_scales_tiled, b_codes, b_scales_tiled, m, n, k, out
                       on_dev(b_scales_tiled), ta, tb, d, m, n, k, mx.MX_LAYOUT_TN, od, split_k, ws)
     torch.cuda.synchronize()
     assert mx.mx_device_status() == mx.MX_OK
+    check_guards(d, ws, what=f"GEMM {m}x{n}x{k} split {split_k}")
     if out_fp32:
         return d.cpu().numpy()
     return d.view(torch.int16).cpu().numpy().view(np.uint16)

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_error_strings(lib):
-    codes = [0, -1, -2, -3, -4, -5, -6, -7, -8, -9]
+    codes = [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10]
     texts = [mx.mx_error_string(c) for c in codes]
     assert len(set(texts)) == len(codes)
     assert mx.mx_error_string(-100) == "unknown status code"

@@ -22,7 +22,8 @@ import torch
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import FP32_REL_TOL, bf16_bits_to_f64, dev_u8, gpu_quantize
+from tests.gpu_helpers import (FP32_REL_TOL, bf16_bits_to_f64, check_guards, dev_u8, gpu_quantize,
+                               guarded)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,13 +41,14 @@ def _bf16_ulp_at(v):
 def _run(fmt, ops, m, n, k, out_fp32, split_k, bias, beta, gelu, d_in):
     """GEMM with an epilogue; d_in: host values D holds before the call (or None: NaN)."""
     dt = torch.float32 if out_fp32 else torch.bfloat16
-    if d_in is None:
-        d = torch.full((m, n), float("nan"), dtype=dt, device="cuda")
-    else:
-        d = torch.from_numpy(np.asarray(d_in, np.float32)).to("cuda").to(dt)
+    body = guarded(m * n, dt, float("nan"))
+    d = body.view(m, n)
+    d._mx_guard = body._mx_guard
+    if d_in is not None:
+        d.copy_(torch.from_numpy(np.asarray(d_in, np.float32)).to("cuda").to(dt))
     b = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to("cuda")
     wsb = mx.mx_gemm_workspace_bytes(m, n, k, split_k)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
+    ws = guarded(max(wsb, 16)) if wsb else None
     od = mx.MX_OUT_FP32 if out_fp32 else mx.MX_OUT_BF16
     if fmt == MX:
         a, sa, bb, sb = ops
@@ -60,6 +62,7 @@ def _run(fmt, ops, m, n, k, out_fp32, split_k, bias, beta, gelu, d_in):
                          mx.MX_LAYOUT_TN, od, split_k, b, beta, gelu, ws)
     torch.cuda.synchronize()
     assert mx.mx_device_status() == mx.MX_OK
+    check_guards(d, ws, what=f"GEMM epilogue {m}x{n}x{k} split {split_k}")
     if out_fp32:
         return d.cpu().numpy().astype(np.float64)
     return bf16_bits_to_f64(d.view(torch.int16).cpu().numpy().view(np.uint16))
@@ -111,8 +114,11 @@ def _inputs(ref, n, seed, out_fp32):
     return bias, c.astype(np.float64)
 
 
-# (m, n, k, split_k): the CTA-pair kernel, the single-CTA kernel, and split-K
-SHAPES = [(256, 512, 1024, 1), (96, 384, 512, 1), (96, 384, 2048, 3), (320, 288, 1024, 2)]
+# (m, n, k, split_k): the CTA-pair kernel, the single-CTA kernel, split-K, and
+# the swapped-operand kernel for M <= 64 (automatic split: one CTA, and a
+# cluster of CTAs whose partials meet in shared memory)
+SHAPES = [(256, 512, 1024, 1), (96, 384, 512, 1), (96, 384, 2048, 3), (320, 288, 1024, 2),
+          (32, 640, 1024, 0), (64, 4224, 4096, 0)]
 # (bias, beta, gelu)
 TERMS = [(True, 0.0, False), (False, 0.0, True), (True, 0.0, True), (False, 1.0, False),
          (True, 0.5, True), (True, -2.0, False)]
@@ -131,7 +137,8 @@ def test_mxfp4_epilogue_matches_oracle(m, n, k, split_k, out_fp32, use_bias, bet
            f"mxfp4 {m}x{n}x{k} split {split_k} fp32={out_fp32} bias={use_bias} beta={beta} gelu={gelu}")
 
 
-@pytest.mark.parametrize("m,n,k,split_k", [(256, 320, 1024, 1), (64, 512, 2048, 3), (32, 640, 1024, 1)])
+@pytest.mark.parametrize("m,n,k,split_k", [(256, 320, 1024, 1), (64, 512, 2048, 3), (32, 640, 1024, 1),
+                                           (32, 4096, 4096, 0)])
 @pytest.mark.parametrize("out_fp32", [True, False])
 def test_nvfp4_epilogue_matches_oracle(m, n, k, split_k, out_fp32):
     xa = synth.bf16_normal(m, k, 1.0, seed=m * 3 + k)

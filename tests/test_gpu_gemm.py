@@ -156,17 +156,21 @@ def test_mxfp4_m_up_to_128_partial_a_tile(m, n, k, split_k, out_fp32):
     _run_and_check_mx(a, sa, b, sb, m, n, k, out_fp32, split_k=split_k)
 
 
-def test_skinny_32x8192x8192_split_k_full():
-    """Decode-shaped skinny GEMM with split-K: every output against the oracle,
-    and bit-identical across runs (fixed reduction order)."""
+@pytest.mark.parametrize("split_k", [0, 2])
+def test_skinny_32x8192x8192_split_k_full(split_k):
+    """Decode-shaped skinny GEMM split along K: every output against the oracle,
+    and bit-identical across runs (fixed reduction order).  Automatic split:
+    the swapped-operand kernel, whose clusters sum their partials in shared
+    memory (no workspace); split_k = 2: partials in the workspace and the
+    reduce kernel."""
     w = synth.workload_inputs("skinny_32x8192x8192")
     m, n, k = 32, 8192, 8192
     d1 = _run_and_check_mx(w["a_codes"], w["a_scales"], w["b_codes"], w["b_scales"], m, n, k,
-                           out_fp32=False, split_k=0)
+                           out_fp32=False, split_k=split_k)
     d2 = gpu_gemm(MX, w["a_codes"], oracle.scale_tile(w["a_scales"]), w["b_codes"],
-                  oracle.scale_tile(w["b_scales"]), m, n, k, out_fp32=False, split_k=0)
+                  oracle.scale_tile(w["b_scales"]), m, n, k, out_fp32=False, split_k=split_k)
     assert np.array_equal(d1, d2)
-    assert mx.mx_gemm_workspace_bytes(m, n, k, 0) > 0   # split-K is in use
+    assert (mx.mx_gemm_workspace_bytes(m, n, k, split_k) > 0) == (split_k > 1)
 
 
 def test_backward_gemm_with_columnwise_codes():

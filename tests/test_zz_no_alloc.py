@@ -62,13 +62,15 @@ def _run_both(a, sa, b, sb, m, n, k, split_k, out_dtype):
 
 
 def test_static_workspace_matches_workspace_gemm_and_oracle_on_calls_in_a_row():
-    # the decode-shaped skinny GEMM (automatic split-K), an explicit split count
-    # on other data, then BF16 outputs of a third shape: calls in a row that all
-    # use the shared scratch, each leaving partials the next must not read
-    cases = [(32, 8192, 8192, 0, 401, mx.MX_OUT_BF16),
+    # the decode-shaped skinny GEMM with two and four splits, an explicit split
+    # count on other data, and the automatic split of M = 96: calls in a row that
+    # all use the shared scratch, each leaving partials the next must not read.
+    # (M <= 64 with the automatic split needs no scratch: its partial sums meet
+    # in shared memory.)
+    cases = [(32, 8192, 8192, 2, 401, mx.MX_OUT_BF16),
              (64, 1024, 4096, 4, 402, mx.MX_OUT_FP32),
-             (96, 2048, 2048, 2, 403, mx.MX_OUT_BF16),
-             (32, 8192, 8192, 0, 404, mx.MX_OUT_FP32)]
+             (96, 2048, 2048, 0, 403, mx.MX_OUT_BF16),
+             (32, 8192, 8192, 4, 404, mx.MX_OUT_FP32)]
     for m, n, k, split_k, seed, out in cases:
         need = mx.mx_gemm_workspace_bytes(m, n, k, split_k)
         assert 0 < need <= mx.MX_STATIC_WORKSPACE_BYTES      # split-K really runs
