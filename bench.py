@@ -98,6 +98,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--min-call-seconds", type=float, default=1.5,
+                   help="least time each call's own timing loop runs (0 for runs under ncu)")
     p.add_argument("--calibrate", action="store_true",
                    help="print the FP4 MMA rate of every form and shape (mx_calibrate_mma), "
                         "one JSON line each, and exit")
@@ -651,7 +653,7 @@ def gemm_block(f, m, n):
 
 # Source files that define the kernels of each call of the step.
 CALL_SOURCES = {
-    "gemm": ["gemm.cu", "gemm_pair.cu", "mx_device.cuh", "mx_internal.h"],
+    "gemm": ["gemm.cu", "gemm_pair.cu", "gemm_swap.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize_2d": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize_sr": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
@@ -783,7 +785,7 @@ def main_ours(args):
     ms_per_step = reduce_max(ms / args.steps, world, "cuda")
 
     windows = {}
-    per_call = time_calls(wl, args.steps, windows=windows)
+    per_call = time_calls(wl, args.steps, windows=windows, min_seconds=args.min_call_seconds)
     time.sleep(0.3)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
