@@ -102,6 +102,10 @@ WORKLOADS = {
     # The same bidimensional NVFP4 quantize with rounding to nearest.
     "nvfp4_quant2d_16384x8192": dict(kind="quant2d", fmt="nvfp4", sr=False, m=16384, n=0,
                                      k=8192, sigma_a=1e-3, out="codes", split_k=1),
+    # The NVFP4 workload's shape and inputs in MXFP4: the two formats' GEMM
+    # kernels side by side.
+    "mxfp4_4096x4096x4096": dict(kind="bf16", fmt="mxfp4", m=4096, n=4096, k=4096,
+                                 sigma_a=1.0, sigma_b=1.0, out="fp32", split_k=1),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 

@@ -233,13 +233,15 @@ def _quant_gemm_check(name, n_rows, n_cols):
     rb, rsb = oracle.mx_quantize(w["b"])
     assert np.array_equal(ca, ra) and np.array_equal(cb, rb)
     del w
-    d = gpu_gemm(MX, ca, sa_t, cb, sb_t, m, n, k, out_fp32=False)
+    out_fp32 = wl["out"] == "fp32"
+    check = check_fp32 if out_fp32 else check_bf16
+    d = gpu_gemm(MX, ca, sa_t, cb, sb_t, m, n, k, out_fp32=out_fp32)
     rows = sample_indices(m, n_rows, 128, seed=1)
     cols = sample_indices(n, n_cols, 256, seed=2)
     ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k, rows=rows)
-    st = check_bf16(d[rows], ref, s_abs, f"{name} sampled rows")
+    st = check(d[rows], ref, s_abs, f"{name} sampled rows")
     ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k, cols=cols)
-    check_bf16(d[:, cols], ref, s_abs, f"{name} sampled cols")
+    check(d[:, cols], ref, s_abs, f"{name} sampled cols")
     assert np.count_nonzero(d) > 0.99 * d.size
     return st
 
@@ -250,6 +252,10 @@ def test_quant_gemm_2048x4096x4096_bf16():
 
 def test_mlp_up_16384x28672x8192_bf16_sampled():
     _quant_gemm_check("mlp_up_16384x28672x8192", 32, 24)
+
+
+def test_mxfp4_4096_cubed_fp32_sampled():
+    _quant_gemm_check("mxfp4_4096x4096x4096", 96, 64)
 
 
 # ------------------------------------------------------------ NVFP4 parity
