@@ -559,14 +559,20 @@ __device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
 // section 6.2, erfcc; fractional error below 1.2e-7 for every z >= 0):
 //   erfc(z) ~ t exp(-z^2 + P(t)),  t = 1 / (1 + z / 2),  P of degree 9.
 // The exponent -z^2 = -a^2 / 2 is taken as -(h + l) / 2 with h = RN(a^2) and
-// l = a^2 - h exact (one FMA), so that only the final FMA of the argument
-// rounds; then GELU(y) = y Phi(-a) for y <= 0 and y - y Phi(-a) for y > 0.
-// Relative error below 2^-24 (y^2 / 2 + 40): the fit, CUDA's expf (2 ulp)
-// and __fdividef (2 ulp), the Horner rounding and the argument's rounding,
-// which grows with its magnitude y^2 / 2.  One MUFU reciprocal and one
-// exponential per value.  Two values at a time: their multiplies and FMAs
-// are packed pairs; the reciprocal, the exponential and the final select
-// stay per value.
+// l = a^2 - h exact (one FMA): arg = RN(-h / 2 + q), q = RN(p - l / 2).  The
+// rounding error of that last sum is recovered exactly as
+// r = q - (h / 2 + arg) (Fast2Sum: h / 2 dominates |q| <= 1.27 once
+// a >= 1.6, and below that the argument is small), and the exponential is
+// taken as exp(arg) (1 + r), whose error r^2 / 2 is negligible.  So the
+// argument's rounding no longer grows with its magnitude y^2 / 2.  The halving
+// of erfc is folded into the fit's constant term (-1.26551223 - ln 2), so
+// Phi(-a) = t exp(-z^2 + P(t) - ln 2) takes no separate multiply.  Then
+// GELU(y) = y Phi(-a) for y <= 0 and y - y Phi(-a) for y > 0.  Relative error
+// below 2^-24 * 44: the fit, CUDA's expf (2 ulp) and __fdividef (2 ulp), the
+// Horner and product roundings, the rounding of q and of the correction.  One
+// MUFU reciprocal and one exponential per value.  Two values at a time: their
+// multiplies and FMAs are packed pairs; the reciprocal, the exponential and
+// the final select stay per value.
 __device__ __forceinline__ float2 gelu_f32x2(float2 y) {
   const auto two = [](float v) { return make_float2(v, v); };
   const float2 a = make_float2(fabsf(y.x), fabsf(y.y));
@@ -582,12 +588,16 @@ __device__ __forceinline__ float2 gelu_f32x2(float2 y) {
   p = fma_f32x2(p, t, two(0.09678418f));
   p = fma_f32x2(p, t, two(0.37409196f));
   p = fma_f32x2(p, t, two(1.00002368f));
-  p = fma_f32x2(p, t, two(-1.26551223f));
+  p = fma_f32x2(p, t, two(-1.95865941f));  // -1.26551223 - ln 2
   const float2 h = mul_f32x2(a, a);
   const float2 l = fma_f32x2(a, a, make_float2(-h.x, -h.y));
-  const float2 arg = fma_f32x2(two(-0.5f), h, fma_f32x2(two(-0.5f), l, p));
-  const float2 ex = make_float2(expf(arg.x), expf(arg.y));
-  const float2 phi = mul_f32x2(mul_f32x2(two(0.5f), t), ex);  // Phi(-|y|)
+  const float2 q = fma_f32x2(two(-0.5f), l, p);
+  const float2 arg = fma_f32x2(two(-0.5f), h, q);
+  const float2 d = fma_f32x2(two(0.5f), h, arg);    // h / 2 + arg, exact
+  const float2 r = fma_f32x2(d, two(-1.0f), q);     // the rounding error of arg
+  float2 ex = make_float2(expf(arg.x), expf(arg.y));
+  ex = fma_f32x2(ex, r, ex);                         // exp(arg + r)
+  const float2 phi = mul_f32x2(t, ex);  // Phi(-|y|)
   const float2 yp = mul_f32x2(y, phi);
   return make_float2(y.x > 0.0f ? __fsub_rn(y.x, yp.x) : yp.x,
                      y.y > 0.0f ? __fsub_rn(y.y, yp.y) : yp.y);
