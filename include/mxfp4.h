@@ -290,7 +290,9 @@ int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format,
 
 /* Workspace bytes that mxfp4_gemm / nvfp4_gemm need for this shape and
  * split count (split_k = 0 means the automatic choice): split_k * m * n * 4
- * when more than one split is used, else 0. */
+ * when more than one split is used with a workspace, else 0.  The automatic
+ * choice for M <= 64 (M % 32 == 0) needs none: its splits are summed on
+ * chip. */
 size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k);
 
 /* MXFP4 GEMM, D[M, N] = sum_k A[m, k] * B[n, k] ("Integrate MXFP4 hipblaslt
@@ -303,7 +305,12 @@ size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k);
  *   layout: MX_LAYOUT_TN only;
  *   split_k: 0 = automatic, else the linear number of K splits (each split
  *     a multiple of 256 along K); more than one split writes FP32 partials
- *     to `workspace` and a reduction kernel sums them in split order;
+ *     to `workspace` and a reduction kernel sums them in split order.  With
+ *     split_k = 0 and M <= 64 the operands are swapped (the weight rows on
+ *     the MMA's 128-row side) and the automatic splits of K run as one
+ *     thread-block cluster whose partial sums meet in shared memory, added
+ *     in split order: no workspace, no second kernel, the same bits on every
+ *     run;
  *   K % 256 == 0, M % 32 == 0, N % 32 == 0, M, N, K > 0. */
 int mxfp4_gemm(const void *a_codes, const void *a_scales, const void *b_codes,
                const void *b_scales, void *d, int64_t m, int64_t n, int64_t k, int layout,
