@@ -18,4 +18,4 @@ from ._binding import (  # noqa: F401
     mx_quantize_bf16_2d, nvfp4_quantize_bf16_sr, MX_PHILOX_MAX_ROUNDS, nvfp4_quantize_bf16_2d,
     mx_gemm_epilogue, mxfp4_gemm_ex, nvfp4_gemm_ex, mx_calibrate_mma, MX_MMA_MXF4,
     MX_MMA_MXF4NVF4_2X, MX_MMA_MXF4NVF4_4X, MX_CALIBRATE_MAX_STEPS, MX_ERR_DEVICE_BOUNDS,
-    MX_BUILD_BOUNDS_CHECK, mx_build_flags)
+    MX_BUILD_BOUNDS_CHECK, mx_build_flags, mx_fp4_transpose)

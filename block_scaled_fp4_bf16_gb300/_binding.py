@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
                                     sz, vp]
         L.mx_scale_relayout.restype = i32
         L.mx_scale_relayout.argtypes = [vp, i64, i64, i32, vp, vp]
+        L.mx_fp4_transpose.restype = i32
+        L.mx_fp4_transpose.argtypes = [vp, i64, i64, vp, vp]
         L.mx_gemm_workspace_bytes.restype = sz
         L.mx_gemm_workspace_bytes.argtypes = [i64, i64, i64, i32]
         L.mxfp4_gemm.restype = i32
@@ -255,6 +257,11 @@ def nvfp4_quantize_bf16_2d(x, rows, cols, ld_x, scale_layout, codes, scales, cod
 def mx_scale_relayout(plain, rows, cols, fmt, tiled, stream=None):
     return _check("mx_scale_relayout", lib().mx_scale_relayout(
         _ptr(plain), rows, cols, fmt, _ptr(tiled), _stream(stream)))
+
+
+def mx_fp4_transpose(codes, rows, cols, out, stream=None):
+    return _check("mx_fp4_transpose", lib().mx_fp4_transpose(
+        _ptr(codes), rows, cols, _ptr(out), _stream(stream)))
 
 
 def mxfp4_gemm(a_codes, a_scales, b_codes, b_scales, d, m, n, k, layout=MX_LAYOUT_TN,

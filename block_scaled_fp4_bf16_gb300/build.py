@@ -20,7 +20,7 @@ BOUNDS_CHECK = os.environ.get("MX_BOUNDS_CHECK") == "1"
 OUT_DIR = os.path.join(PKG, "_build_bounds" if BOUNDS_CHECK else "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmxfp4.so")
 SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "gemm_swap.cu", "static_ws.cu",
-           "calibrate.cu"]
+           "calibrate.cu", "transpose.cu"]
 HEADERS = ["mx_device.cuh", "mx_internal.h"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -786,6 +786,36 @@ MX_API int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int 
                                                  dev->status, static_cast<cudaStream_t>(stream)));
 }
 
+MX_API int mx_fp4_transpose(const void *codes, int64_t rows, int64_t cols, void *out,
+                            void *stream) {
+  clear_detail();
+  const char *fn = "mx_fp4_transpose";
+  if (!codes || !out)
+    return fail(MX_ERR_INVALID_ARG, "%s: %s is null", fn, !codes ? "codes" : "out");
+  if (rows <= 0 || cols <= 0)
+    return fail(MX_ERR_INVALID_ARG, "%s: rows, cols = %lld, %lld (both positive)", fn,
+                static_cast<long long>(rows), static_cast<long long>(cols));
+  if (rows % 32 != 0 || cols % 32 != 0)
+    return fail(MX_ERR_UNSUPPORTED_SHAPE, "%s: rows, cols = %lld, %lld (both multiples of 32)",
+                fn, static_cast<long long>(rows), static_cast<long long>(cols));
+  if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31) ||
+      (rows + 63) / 64 > 65535)
+    return fail(MX_ERR_UNSUPPORTED_SHAPE,
+                "%s: cols must be below 2^31 and rows below 64 * 65536", fn);
+  if (!aligned16(codes) || !aligned16(out))
+    return fail(MX_ERR_ALIGNMENT, "%s: %s is not 16-byte aligned", fn,
+                !aligned16(codes) ? "codes" : "out");
+  const uintptr_t ci = reinterpret_cast<uintptr_t>(codes), oi = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t bytes = static_cast<uintptr_t>(rows) * static_cast<uintptr_t>(cols) / 2;
+  if (overlap(Range{ci, ci + bytes}, Range{oi, oi + bytes}))
+    return fail(MX_ERR_INVALID_ARG, "%s: out overlaps codes", fn);
+  DeviceInfo *dev = nullptr;
+  const int rc = device_info(&dev);
+  if (rc != MX_OK) return rc;
+  return launch_rc(fn, mx::launch_fp4_transpose(codes, rows, cols, out, dev->status,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 MX_API size_t mx_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int split_k) {
   if (m <= 0 || n <= 0 || k <= 0 || k % 256 != 0 || split_k < 0) return 0;
   const mx::GemmPlan plan = mx::gemm_plan(m, n, k, split_k, num_sms_or_default());

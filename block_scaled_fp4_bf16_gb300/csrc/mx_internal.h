@@ -86,6 +86,9 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
                                      void *scales_t, float *tensor_scale, uint32_t *partials,
                                      const SrArgs *sr, int num_sms, uint32_t *status,
                                      cudaStream_t s);
+// FP4 codes [rows, cols / 2] -> [cols, rows / 2] (rows, cols % 32 == 0).
+cudaError_t launch_fp4_transpose(const void *codes, int64_t rows, int64_t cols, void *out,
+                                 uint32_t *status, cudaStream_t s);
 cudaError_t launch_scale_relayout(const void *plain, int64_t rows, int64_t kb, void *tiled,
                                   uint32_t *status, cudaStream_t s);
 

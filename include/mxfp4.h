@@ -288,6 +288,22 @@ int nvfp4_quantize_bf16_2d(const void *x, int64_t rows, int64_t cols, int64_t ld
 int mx_scale_relayout(const void *plain, int64_t rows, int64_t cols, int format, void *tiled,
                       void *stream);
 
+/* Transpose of an FP4 code matrix (either format): codes [rows, cols / 2]
+ * -> out [cols, rows / 2], two codes a byte, element 2t of a row in the low
+ * nibble of byte t in both.  The GEMMs take K-contiguous operands only (the
+ * tensor cores read FP4 operands K-major), so an operand quantized with its
+ * blocks along K but stored M- or N-contiguous ([K, M / 2] codes) is brought
+ * to [M, K / 2] by this call; its scales stay as they are, since they are
+ * indexed by (operand row, block along K) in either storage.  With it the
+ * NN, NT and TT products of pre-quantized operands run through the TN GEMM
+ * ("Integrate MXFP4 hipblaslt GEMM support", Takeaways: the full four-layout
+ * set).  rows, cols: multiples of 32 (cols < 2^31, rows < 64 * 65536); codes
+ * and out 16-byte aligned, caller-owned device buffers of rows * cols / 2
+ * bytes that do not overlap.  Errors: MX_ERR_INVALID_ARG (null, non-positive
+ * size, overlap), MX_ERR_UNSUPPORTED_SHAPE, MX_ERR_ALIGNMENT; nothing is
+ * written on a rejection. */
+int mx_fp4_transpose(const void *codes, int64_t rows, int64_t cols, void *out, void *stream);
+
 /* Workspace bytes that mxfp4_gemm / nvfp4_gemm need for this shape and
  * split count (split_k = 0 means the automatic choice): split_k * m * n * 4
  * when more than one split is used with a workspace, else 0.  The automatic

@@ -352,6 +352,20 @@ def scale_tile(plain: np.ndarray) -> np.ndarray:
     return out
 
 
+def fp4_transpose(codes: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Codes [rows, cols / 2] -> [cols, rows / 2] (the element-wise transpose of
+    the FP4 matrix), both packed with element 2t of a row in the low nibble of
+    byte t (R2).  "Integrate MXFP4 hipblaslt GEMM support", Takeaways: the
+    operand layouts other than TN come down to the transpose of one operand;
+    the scales, indexed by (operand row, K block), are not touched."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(rows, cols // 2)
+    elems = np.empty((rows, cols), dtype=np.uint8)   # one code per entry
+    elems[:, 0::2] = c & 0xF
+    elems[:, 1::2] = c >> 4
+    t = np.ascontiguousarray(elems.T)                # [cols, rows]
+    return (t[:, 0::2] | (t[:, 1::2] << 4)).astype(np.uint8)
+
+
 # ----------------------------------------------------------------- helpers
 
 def e2m1_decode_array(codes: np.ndarray, k: int) -> np.ndarray:

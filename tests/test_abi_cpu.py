@@ -259,6 +259,19 @@ def test_relayout_and_selftest_validation(lib):
     assert lib.mx_selftest_wait_timeout(0, None) == mx.MX_ERR_INVALID_ARG
 
 
+def test_fp4_transpose_argument_validation(lib):
+    t = lib.mx_fp4_transpose
+    assert t(None, 64, 64, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert t(FAKE, 64, 64, None, None) == mx.MX_ERR_INVALID_ARG
+    assert t(FAKE, 0, 64, FAKE + (1 << 20), None) == mx.MX_ERR_INVALID_ARG
+    assert t(FAKE, 48, 64, FAKE + (1 << 20), None) == mx.MX_ERR_UNSUPPORTED_SHAPE   # rows % 32
+    assert t(FAKE, 64, 80, FAKE + (1 << 20), None) == mx.MX_ERR_UNSUPPORTED_SHAPE   # cols % 32
+    assert t(FAKE_ODD, 64, 64, FAKE + (1 << 20), None) == mx.MX_ERR_ALIGNMENT
+    assert t(FAKE, 64, 64, FAKE + 1024, None) == mx.MX_ERR_INVALID_ARG             # overlap
+    assert "overlaps" in mx.mx_last_error_string()
+    assert t(FAKE, 64 * 65536, 64, FAKE + (1 << 36), None) == mx.MX_ERR_UNSUPPORTED_SHAPE
+
+
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host without a GPU only")
 def test_no_gpu_reports_unavailable(lib):
     assert mx.mx_available() is False

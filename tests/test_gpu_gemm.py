@@ -9,9 +9,9 @@ import torch
 import block_scaled_fp4_bf16_gb300 as mx
 import oracle
 from block_scaled_fp4_bf16_gb300 import synth
-from tests.gpu_helpers import (bf16_bits_to_f64, check_bf16, check_fp32, dev_u8, gpu_gemm,
-                               gpu_quantize_2d,
-                               gpu_quantize, gpu_relayout, sample_indices)
+from tests.gpu_helpers import (bf16_bits_to_f64, check_bf16, check_fp32, check_guards, dev_u8,
+                               gpu_gemm, gpu_quantize_2d, gpu_quantize, gpu_relayout, guarded,
+                               sample_indices)
 
 pytestmark = pytest.mark.gpu
 
@@ -221,6 +221,46 @@ def test_four_operand_layouts_through_the_quantizer(layout):
     assert np.array_equal(d, d_tn)
     ref, s_abs = oracle.mx_gemm(ra, rsa, rb, rsb, m, n, k)
     check_bf16(d, ref, s_abs, f"layout {layout}")
+
+
+# ------------------------------------------------------------ FP4 code transpose
+
+def _gpu_transpose(codes, rows, cols):
+    out = guarded(rows * cols // 2, fill=0xAB)
+    mx.mx_fp4_transpose(dev_u8(codes), rows, cols, out)
+    torch.cuda.synchronize()
+    check_guards(out, what=f"FP4 transpose {rows}x{cols}")
+    return out.cpu().numpy().reshape(cols, rows // 2)
+
+
+@pytest.mark.parametrize("rows,cols", [(32, 32), (64, 128), (96, 4128), (160, 96), (4096, 1056),
+                                       (8192, 8192)])
+def test_fp4_transpose_matches_oracle(rows, cols):
+    """Bit-exact against the oracle: one and several 64 x 128 tiles, ragged
+    tails in both directions, and a full 8192 x 8192 weight."""
+    codes = synth.fp4_codes(rows, cols, seed=rows * 7 + cols)
+    assert np.array_equal(_gpu_transpose(codes, rows, cols),
+                          oracle.fp4_transpose(codes, rows, cols))
+
+
+@pytest.mark.parametrize("stored_mn", ["A", "B", "AB"])
+def test_gemm_of_operands_stored_mn_contiguous(stored_mn):
+    """Operands quantized along K but stored M- or N-contiguous (the NN, NT and
+    TT layouts): the GPU transpose brings them to K-contiguous codes, equal to
+    the original ones, and the TN GEMM then gives the same bits as on the
+    original operands, within the tolerances of the oracle."""
+    m, n, k = 160, 288, 512
+    a, sa, b, sb = _codes_case(m, n, k, seed=77)
+    a_in = oracle.fp4_transpose(a, m, k) if "A" in stored_mn else a      # [K, M/2] when stored MN
+    b_in = oracle.fp4_transpose(b, n, k) if "B" in stored_mn else b
+    a_km = _gpu_transpose(a_in, k, m) if "A" in stored_mn else a_in
+    b_km = _gpu_transpose(b_in, k, n) if "B" in stored_mn else b_in
+    assert np.array_equal(a_km, a) and np.array_equal(b_km, b)
+    d = gpu_gemm(MX, a_km, oracle.scale_tile(sa), b_km, oracle.scale_tile(sb), m, n, k, True)
+    d_tn = gpu_gemm(MX, a, oracle.scale_tile(sa), b, oracle.scale_tile(sb), m, n, k, True)
+    assert np.array_equal(d.view(np.uint32), d_tn.view(np.uint32))
+    ref, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
+    check_fp32(d, ref, s_abs, f"operands stored MN-contiguous: {stored_mn}")
 
 
 def _quant_gemm_check(name, n_rows, n_cols):
