@@ -66,14 +66,18 @@ from block_scaled_fp4_bf16_gb300 import synth  # noqa: E402
 DEFAULT_WORKLOAD = "mlp_up_16384x28672x8192"
 METRIC = "MXFP4 GEMM TFLOPS and % of GB300 dense FP4 peak; quantize GB/s vs HBM"
 
-# Steps that are a quantize alone (no GEMM): their metric is algorithmic GB/s.
-QUANT_KINDS = ("quant2d", "quant_sr")
+# Steps with no GEMM (a quantize alone, or the FP4 code transpose): their
+# metric is algorithmic GB/s.
+QUANT_KINDS = ("quant2d", "quant_sr", "transpose")
 # Philox seed of the stochastic-rounding quantize step
 SR_SEED = 0x5EED5EED
 
 
 def quant_step_bytes(w, m, k):
-    """Algorithmic bytes of a quantize-only step (workload w) over a BF16 [m, k] tensor."""
+    """Algorithmic bytes of a step without a GEMM (workload w) over an [m, k]
+    tensor: a quantize of BF16, or the transpose of FP4 codes."""
+    if w["kind"] == "transpose":            # codes read once, written once
+        return m * k * (0.5 + 0.5)
     nv = w["fmt"] == "nvfp4"
     amax = 2 if nv else 0                   # NVFP4: the amax pass reads x once more
     blk = 16 if nv else 32
@@ -236,6 +240,8 @@ class DeviceWorkload:
         if self.kind == "bf16":
             ha = torch.from_numpy(host_inputs["a"].view(np.int16)).view(torch.bfloat16)
             hb = torch.from_numpy(host_inputs["b"].view(np.int16)).view(torch.bfloat16)
+        elif self.kind == "transpose":
+            hc = torch.from_numpy(host_inputs["a_codes"])
         elif self.kind in QUANT_KINDS:
             ha = torch.from_numpy(host_inputs["a"].view(np.int16)).view(torch.bfloat16)
         else:
@@ -248,6 +254,11 @@ class DeviceWorkload:
                 tiled[key] = t
         for _ in range(nsets):
             s = {}
+            if self.kind == "transpose":
+                s["codes_in"] = hc.to(dev)
+                s["codes_t"] = torch.empty(m * k // 2, dtype=u8, device=dev)
+                self.sets.append(s)
+                continue
             if self.kind == "quant2d":
                 s["x_a"] = ha.to(dev)
                 s["codes_a"] = torch.empty(m * k // 2, dtype=u8, device=dev)
@@ -301,6 +312,10 @@ class DeviceWorkload:
         mx = self.mx
         m, n, k, fmt = self.m, self.n, self.k, self.fmt
         out = []
+        if self.kind == "transpose":
+            def tr(s, st):
+                mx.mx_fp4_transpose(s["codes_in"], m, k, s["codes_t"], stream=st)
+            return [("transpose", tr)]
         if self.kind == "quant2d" and fmt == mx.MX_FMT_NVFP4:
             sr = 1 if self.w.get("sr") else 0
 
@@ -348,6 +363,8 @@ class DeviceWorkload:
     def kernels_per_call(self):
         """Kernel launches of each call of the step (matches the library's launches)."""
         mx = self.mx
+        if self.kind == "transpose":
+            return {"transpose": 1}
         if self.kind == "quant2d":
             return {"quantize_2d": 1 if self.fmt == mx.MX_FMT_MXFP4 else 2}
         if self.kind == "quant_sr":
@@ -363,6 +380,8 @@ class DeviceWorkload:
         """Algorithmic work of each call: (bytes, flops)."""
         m, n, k = self.m, self.n, self.k
         blk = 32 if self.fmt == self.mx.MX_FMT_MXFP4 else 16
+        if self.kind == "transpose":
+            return {"transpose": (quant_step_bytes(self.w, m, k), 0.0)}
         if self.kind == "quant2d":
             # BF16 read once, codes and scales written for x and for x^T
             return {"quantize_2d": (quant_step_bytes(self.w, m, k), 0.0)}
@@ -498,7 +517,9 @@ def time_e2e(wl, host_inputs, steps):
     read back, and each set has its own pinned result buffers."""
     torch = wl.torch
     pinned = {}
-    if wl.kind in ("bf16",) + QUANT_KINDS:
+    if wl.kind == "transpose":
+        pinned["codes_in"] = torch.from_numpy(host_inputs["a_codes"]).pin_memory()
+    elif wl.kind in ("bf16",) + QUANT_KINDS:
         pinned["x_a"] = torch.from_numpy(host_inputs["a"].view(np.int16)).view(
             torch.bfloat16).pin_memory()
     if wl.kind == "bf16":
@@ -510,7 +531,8 @@ def time_e2e(wl, host_inputs, steps):
         pinned["codes_a"] = torch.from_numpy(host_inputs["a_codes"]).pin_memory()
         pinned["codes_b"] = torch.from_numpy(host_inputs["b_codes"]).pin_memory()
     # the step's result read back: D, or the code outputs of a quantize step
-    result_keys = {"quant2d": ["codes_a", "codes_t"], "quant_sr": ["codes_a"]}.get(wl.kind, ["d"])
+    result_keys = {"quant2d": ["codes_a", "codes_t"], "quant_sr": ["codes_a"],
+                   "transpose": ["codes_t"]}.get(wl.kind, ["d"])
     nset = len(wl.sets)
     results = [{key: torch.empty(st[key].shape, dtype=st[key].dtype).pin_memory()
                 for key in result_keys} for st in wl.sets]
@@ -582,6 +604,10 @@ def oracle_step_sample(name, host, frac, prepared):
     if w["kind"] == "quant_sr":
         oracle.nvfp4_quantize_sr(host["a"][:mr], SR_SEED, 10)
         return time.perf_counter() - t0, mr / m
+    if w["kind"] == "transpose":
+        mr = max(32, mr // 32 * 32)
+        oracle.fp4_transpose(host["a_codes"][:mr], mr, k)
+        return time.perf_counter() - t0, mr / m
     rows, cols = np.arange(dm), np.arange(dn)
     if w["kind"] == "bf16":
         if w["fmt"] == "mxfp4":
@@ -633,7 +659,8 @@ def cpu_baseline(name, host, target_s):
     kind = synth.WORKLOADS[name]["kind"]
     if kind in QUANT_KINDS:
         gbs = quant_step_bytes(synth.WORKLOADS[name], m, k) * f / t / 1e9
-        what = "both directions" if kind == "quant2d" else "stochastic rounding"
+        what = {"quant2d": "both directions", "quant_sr": "stochastic rounding",
+                "transpose": "FP4 code transpose"}[kind]
         return {"value": gbs, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
                 "sample": f"{f:.4f} of one step ({int(round(f * m))} of {m} rows, {what}), "
                           f"{t:.1f} s on the host CPU"}
@@ -657,6 +684,7 @@ CALL_SOURCES = {
     "quantize_2d": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
     "quantize_sr": ["quantize.cu", "mx_device.cuh", "mx_internal.h"],
+    "transpose": ["transpose.cu", "mx_device.cuh", "mx_internal.h"],
 }
 
 
@@ -852,7 +880,8 @@ def main_ours(args):
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 -> e2m1 (quantize only)" if quant_only else "e2m1 (fp32 accumulate)",
+        "dtype": ("u8 (e2m1 code bytes)" if wl.kind == "transpose" else
+                  "bf16 -> e2m1 (quantize only)" if quant_only else "e2m1 (fp32 accumulate)"),
         "data": "synthetic",
         "config": {"workload": name, "m": m, "n": n, "k": k, "format": w["fmt"],
                    "out": w["out"], "rotating_sets": nsets,

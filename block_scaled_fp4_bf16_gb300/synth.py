@@ -106,6 +106,11 @@ WORKLOADS = {
     # kernels side by side.
     "mxfp4_4096x4096x4096": dict(kind="bf16", fmt="mxfp4", m=4096, n=4096, k=4096,
                                  sigma_a=1.0, sigma_b=1.0, out="fp32", split_k=1),
+    # FP4 codes of the MLP weight stored K x N (N contiguous, the NN / TN
+    # operand order of a layer's weight) transposed to N x K for the GEMM:
+    # no GEMM (n = 0), HBM bound.  Codes uniform over all 16 values.
+    "fp4_transpose_8192x28672": dict(kind="transpose", fmt="mxfp4", m=8192, n=0, k=28672,
+                                     out="codes", split_k=1),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
@@ -122,6 +127,7 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
                     for a workload with a bias)
     kind == "codes": {"a_codes", "a_scales", "b_codes", "b_scales"} (plain scales)
     kind == "quant2d" or "quant_sr": {"a": BF16 bits [m, k]}
+    kind == "transpose": {"a_codes": FP4 codes [m, k / 2]}
     """
     w = WORKLOADS[name]
     m = w["m"] if m is None else m
@@ -137,6 +143,8 @@ def workload_inputs(name: str, m: int | None = None, n: int | None = None,
         return out
     if w["kind"] in ("quant2d", "quant_sr"):
         return {"a": bf16_normal(m, k, w["sigma_a"], seed + 1)}
+    if w["kind"] == "transpose":
+        return {"a_codes": fp4_codes(m, k, seed + 1)}
     kb = k // 32
     return {"a_codes": fp4_codes(m, k, seed + 1),
             "a_scales": scale_bytes(m, kb, w["scale_lo"], w["scale_hi"], seed + 2),

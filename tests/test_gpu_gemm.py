@@ -243,6 +243,16 @@ def test_fp4_transpose_matches_oracle(rows, cols):
                           oracle.fp4_transpose(codes, rows, cols))
 
 
+def test_fp4_transpose_workload_full_size():
+    """The transpose workload as bench.py runs it (the MLP weight's codes
+    stored 8192 x 28672), every byte."""
+    name = "fp4_transpose_8192x28672"
+    wl = synth.WORKLOADS[name]
+    codes = synth.workload_inputs(name)["a_codes"]
+    assert np.array_equal(_gpu_transpose(codes, wl["m"], wl["k"]),
+                          oracle.fp4_transpose(codes, wl["m"], wl["k"]))
+
+
 @pytest.mark.parametrize("stored_mn", ["A", "B", "AB"])
 def test_gemm_of_operands_stored_mn_contiguous(stored_mn):
     """Operands quantized along K but stored M- or N-contiguous (the NN, NT and
