@@ -13,6 +13,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <vector>
 
 #include "mx_internal.h"
 #include "mxfp4.h"
@@ -938,6 +939,42 @@ MX_API int mx_calibrate_mma(int form, int pair, int64_t steps, unsigned long lon
 }
 
 namespace mx {
+
+namespace {
+struct SetupRecord {
+  const void *func;
+  CUcontext ctx;
+  int value;
+};
+std::mutex g_setup_mutex;
+std::vector<SetupRecord> g_setup;  // one per kernel instance and context: a few dozen
+}  // namespace
+
+bool kernel_setup_get(const void *func, int *value) {
+  const CUcontext ctx = current_context();
+  if (ctx == nullptr) return false;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  for (const SetupRecord &r : g_setup) {
+    if (r.func == func && r.ctx == ctx) {
+      if (value) *value = r.value;
+      return true;
+    }
+  }
+  return false;
+}
+
+void kernel_setup_put(const void *func, int value) {
+  const CUcontext ctx = current_context();
+  if (ctx == nullptr) return;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  for (SetupRecord &r : g_setup) {
+    if (r.func == func && r.ctx == ctx) {
+      r.value = value;
+      return;
+    }
+  }
+  g_setup.push_back(SetupRecord{func, ctx, value});
+}
 
 int gemm_static_workspace_call(const void *a_codes, const void *a_scales, const void *b_codes,
                                const void *b_scales, void *d, int64_t m, int64_t n, int64_t k,

@@ -520,15 +520,12 @@ __global__ void wait_selftest_kernel(uint32_t *status, uint64_t timeout_ns) {
 template <int FMT, int BN, int OUT_F32, int EPI>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   using C = Cfg<FMT, BN>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, OUT_F32, EPI>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  auto kernel = gemm_kernel<FMT, BN, OUT_F32, EPI>;
+  cudaError_t e = cudaSuccess;
+  if (!kernel_setup_get(reinterpret_cast<const void *>(kernel), nullptr)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    kernel_setup_put(reinterpret_cast<const void *>(kernel), 0);
   }
   Params p{};
   p.sfa = static_cast<const uint8_t *>(g.a_scales);

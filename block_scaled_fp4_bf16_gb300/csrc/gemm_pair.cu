@@ -467,11 +467,7 @@ template <int FMT, int OUT_F32, int EPI>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   using C = PairCfg<FMT, EPI >= 2 ? 16 : 8>;
   auto kernel = gemm_pair_kernel<FMT, OUT_F32, EPI>;
-  static bool attr_set[64] = {};
-  static int max_clusters[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -485,15 +481,16 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (dev < 64 && !attr_set[dev]) {
+  int max_clusters = 0;  // CTA pairs resident at once
+  if (!kernel_setup_get(reinterpret_cast<const void *>(kernel), &max_clusters)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(2 * (g.num_sms / 2), 1, 1);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
-    max_clusters[dev] = n > 0 ? n : 1;
-    attr_set[dev] = true;
+    max_clusters = n > 0 ? n : 1;
+    kernel_setup_put(reinterpret_cast<const void *>(kernel), max_clusters);
   }
   PairParams p{};
   p.a_ts = g.a_ts;
@@ -519,7 +516,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
     const int boxes = C::kWarpCols / ((g.out_fp32 || g.split_k > 1) ? 16 : 32);
     p.pace_cycles = static_cast<uint32_t>(0.95 * 512.0 * p.stages_per_split / boxes);
   }
-  const int clusters = p.num_units < max_clusters[dev] ? p.num_units : max_clusters[dev];
+  const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.numAttrs = 2;  // cluster shape + programmatic stream serialization
   e = cudaLaunchKernelEx(&cfg, kernel, *g.tmap_a, *g.tmap_b, *g.tmap_sfa, *g.tmap_sfb, *g.tmap_d,

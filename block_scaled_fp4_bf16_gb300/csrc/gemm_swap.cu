@@ -408,14 +408,11 @@ template <int FMT, int OUT_F32, int MT>
 cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   using C = SwapCfg<FMT>;
   auto kernel = gemm_swap_kernel<FMT, OUT_F32, MT>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
+  cudaError_t e = cudaSuccess;
+  if (!kernel_setup_get(reinterpret_cast<const void *>(kernel), nullptr)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    kernel_setup_put(reinterpret_cast<const void *>(kernel), 0);
   }
   SwapParams p{};
   p.sfw = static_cast<const uint8_t *>(g.b_scales);

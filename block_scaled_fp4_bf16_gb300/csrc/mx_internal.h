@@ -86,6 +86,15 @@ cudaError_t launch_nvfp4_quantize_2d(const void *x, int64_t rows, int64_t cols, 
                                      void *scales_t, float *tensor_scale, uint32_t *partials,
                                      const SrArgs *sr, int num_sms, uint32_t *status,
                                      cudaStream_t s);
+// One-time set-up of a kernel in the current CUDA context (its dynamic
+// shared-memory limit; for the pair GEMM also its cluster occupancy, kept as
+// `value`).  Records are kept per (kernel, context), so that a context made
+// anew after cudaDeviceReset sets its kernels up again; thread-safe.
+// kernel_setup_get returns false when the kernel has no record in the
+// current context.
+bool kernel_setup_get(const void *func, int *value);
+void kernel_setup_put(const void *func, int value);
+
 // FP4 codes [rows, cols / 2] -> [cols, rows / 2] (rows, cols % 32 == 0).
 cudaError_t launch_fp4_transpose(const void *codes, int64_t rows, int64_t cols, void *out,
                                  uint32_t *status, cudaStream_t s);
