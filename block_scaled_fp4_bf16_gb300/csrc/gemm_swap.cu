@@ -14,7 +14,12 @@
 // the cluster's first CTA, added in rank order (deterministic, one rounding
 // of the sum at the end), with no workspace and no second kernel.
 //
-// Roles (192 threads, one CTA per SM):
+// One CTA per SM, with a stage ring as deep as shared memory allows; or, when
+// the CTAs outnumber the SMs (more than num_sms 128-row weight slices), two
+// CTAs per SM, each with half the shared and tensor memory, so that all of
+// them stream in one wave.
+//
+// Roles (192 threads):
 //   warp 0      TMA producer: before waiting for the previous kernel, the
 //               first stages of its weight rows are prefetched into L2
 //               (weights rarely depend on the previous kernel, and the
@@ -51,8 +56,12 @@ constexpr int kSwRows = 128;        // rows of the MMA's weight tile (its M)
 constexpr int kSwStageKBytes = 128; // 256 FP4 codes of K per stage
 constexpr int kSwMaxSlots = 32;
 constexpr int kSwSmemBytes = 232448;
+// Two CTAs per SM (when the CTAs outnumber the SMs): each takes half of an
+// SM's shared memory (less the 1 KB the runtime reserves per CTA) and half of
+// its tensor memory.
+constexpr int kSwSmemBytesDense = 233472 / 2 - 1024;
 constexpr int kSwSfCol = kSwMaxM;   // tensor memory: accumulator (<= 64 columns), then scales
-constexpr int kSwTmemCols = 512;
+constexpr int kSwTmemCols = 512;  // one CTA per SM; 256 with two
 
 // Shared memory of a CTA, laid out by the host for (format, M, weight rows R):
 //   weights     a ring of `slots` slices of R rows x 128 bytes, with
@@ -87,6 +96,7 @@ struct SwapParams {
   int wrows;            // weight rows per CTA: 128, 64 or 32 (a part of a 128-row atom)
   int splits;           // CTAs per cluster (1, 2 or 4), one K range each
   int slots;            // stages in flight
+  int tmem_cols;        // tensor-memory columns allocated (512, or 256 with two CTAs an SM)
   int w_off, x_off, sf_off, bar_off;  // shared-memory layout (bytes; w_off: slot 0's slice)
   EpiParams epi;        // bias / beta / GELU (applied by rank 0 after the sum)
 };
@@ -99,7 +109,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // MT: M / 32 (1 or 2), so that the accumulator rows of a thread are
 // registers indexed by compile-time constants.
 template <int FMT, int OUT_F32, int MT>
-__global__ void __launch_bounds__(kSwThreads, 1)
+__global__ void __launch_bounds__(kSwThreads, 2)
     gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_x, const SwapParams p) {
   using C = SwapCfg<FMT>;
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     prefetch_tmap(&tmap_x);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kSwTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
     tmem_relinquish();
   }
   tc_fence_before();
@@ -400,7 +410,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kSwTmemCols);
+    tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
   }
 }
 
@@ -429,15 +439,24 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   p.katoms = static_cast<int>(g.k / (FMT == 0 ? 128 : 64));
   p.wrows = g.bn;  // the plan's weight rows per CTA
   p.epi = g.epi;
+  // More CTAs than SMs (a weight of more than num_sms 128-row slices): two
+  // CTAs per SM, each with half the ring, so that all of them stream at once
+  // instead of in two waves (measured, 32 x 28672 x 8192: 27.8 -> 21.3 us;
+  // the grids that fit one CTA per SM keep the deeper ring, which is faster
+  // for them).
+  const int64_t blocks = (g.n + g.bn - 1) / g.bn;
+  const bool dense = blocks * g.split_k > g.num_sms;
+  const int smem_budget = dense ? kSwSmemBytesDense : kSwSmemBytes;
+  p.tmem_cols = dense ? kSwTmemCols / 2 : kSwTmemCols;
   // shared-memory layout (see SwapCfg): as many slots as shared and tensor
   // memory hold
   const int m = 32 * MT;
   const int guard = (kSwRows - p.wrows) * kSwStageKBytes;
   const int per_slot = (p.wrows + m) * kSwStageKBytes + 2 * C::kSfBytes;
   const int fixed = 2 * guard + 1024 /* alignment of the activation ring */ + 256 /* barriers */;
-  int slots = (kSwSmemBytes - fixed - 16 * kSwMaxSlots) / per_slot;
+  int slots = (smem_budget - fixed - 16 * kSwMaxSlots) / per_slot;
   slots = slots < kSwMaxSlots ? slots : kSwMaxSlots;
-  const int tmem_slots = (kSwTmemCols - kSwSfCol) / C::kSfSetCols;
+  const int tmem_slots = (p.tmem_cols - kSwSfCol) / C::kSfSetCols;
   slots = slots < tmem_slots ? slots : tmem_slots;
   if (slots < 2) return cudaErrorInvalidValue;
   p.slots = slots;
@@ -450,9 +469,8 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   // after the main loop the weight ring holds rank 0's received partials
   // ([S - 1][m][128] FP32 at offset 0), then the four warps' output boxes
   // (m x 32 each, at most FP32)
-  if (smem_bytes > kSwSmemBytes || (g.split_k - 1) * m * kSwRows * 4 + 4 * m * 32 * 4 > w_end)
+  if (smem_bytes > smem_budget || (g.split_k - 1) * m * kSwRows * 4 + 4 * m * 32 * 4 > w_end)
     return cudaErrorInvalidValue;
-  const int blocks = static_cast<int>((g.n + g.bn - 1) / g.bn);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -480,7 +498,9 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 // one streaming 64-row slices), split along K over a cluster before the slices
 // get thinner; the first shape whose CTAs fill at least three quarters of the
 // SMs and fit on them at one per SM (each split keeping >= 4 stages of K),
-// else the one with the most CTAs that fit.
+// else the one with the most CTAs that fit; when none fits (more 128-row
+// slices than SMs), 128-row slices with no split, which launch_gemm_swap then
+// runs at two CTAs per SM.
 void gemm_swap_shape(int64_t m, int64_t n, int64_t k, int num_sms, int *wrows, int *splits) {
   const int64_t stages = k / 256;
   const int64_t want = num_sms - num_sms / 4;

@@ -111,6 +111,10 @@ WORKLOADS = {
     # no GEMM (n = 0), HBM bound.  Codes uniform over all 16 values.
     "fp4_transpose_8192x28672": dict(kind="transpose", fmt="mxfp4", m=8192, n=0, k=28672,
                                      out="codes", split_k=1),
+    # Decode step of the MLP up-projection: 32 tokens x the 28672 x 8192
+    # weight, HBM bound on the weight (more 128-row slices than SMs).
+    "decode_mlp_up_32x28672x8192": dict(kind="codes", fmt="mxfp4", m=32, n=28672, k=8192,
+                                        scale_lo=122, scale_hi=130, out="bf16", split_k=0),
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 

@@ -118,7 +118,7 @@ def _inputs(ref, n, seed, out_fp32):
 # the swapped-operand kernel for M <= 64 (automatic split: one CTA, and a
 # cluster of CTAs whose partials meet in shared memory)
 SHAPES = [(256, 512, 1024, 1), (96, 384, 512, 1), (96, 384, 2048, 3), (320, 288, 1024, 2),
-          (32, 640, 1024, 0), (64, 4224, 4096, 0)]
+          (32, 640, 1024, 0), (64, 4224, 4096, 0), (32, 20480, 512, 0)]
 # (bias, beta, gelu)
 TERMS = [(True, 0.0, False), (False, 0.0, True), (True, 0.0, True), (False, 1.0, False),
          (True, 0.5, True), (True, -2.0, False)]

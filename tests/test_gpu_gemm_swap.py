@@ -33,9 +33,11 @@ def _check(d, ref, s_abs, out_fp32, what):
 
 
 # (m, n, k): cluster of 1 (one stage; one block with 96 rows past N), of 2, of 4,
-# ragged N, M = 64, and more blocks than SMs
+# ragged N, M = 64, and more 128-row blocks than SMs (two CTAs per SM, also
+# with a ragged last block and with more blocks than two per SM hold)
 SHAPES = [(32, 32, 256), (32, 8192, 8192), (32, 4096, 4096), (64, 4224, 2048),
-          (32, 1056, 1024), (64, 640, 1024), (32, 28672, 512)]
+          (32, 1056, 1024), (64, 640, 1024), (32, 28672, 512), (64, 28672, 1024),
+          (32, 24608, 2048), (32, 45056, 512)]
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
@@ -48,7 +50,8 @@ def test_swap_mxfp4_matches_oracle(m, n, k, out_fp32):
     _check(d, ref, s_abs, out_fp32, f"swap mxfp4 {m}x{n}x{k}")
 
 
-@pytest.mark.parametrize("m,n,k", [(32, 4096, 4096), (64, 1152, 2048), (32, 96, 512)])
+@pytest.mark.parametrize("m,n,k", [(32, 4096, 4096), (64, 1152, 2048), (32, 96, 512),
+                                   (32, 28672, 1024), (64, 20480, 512)])
 @pytest.mark.parametrize("out_fp32", [True, False])
 def test_swap_nvfp4_matches_oracle(m, n, k, out_fp32):
     xa = synth.bf16_normal(m, k, 1.0, seed=m * 3 + k)
@@ -75,6 +78,19 @@ def test_swap_is_deterministic_and_agrees_with_the_workspace_path(out_fp32):
     ref, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
     _check(d1, ref, s_abs, out_fp32, "swap, cluster of 4")
     _check(d_ws, ref, s_abs, out_fp32, "workspace split 4")
+
+
+def test_swap_decode_mlp_workload_full_size():
+    """The decode-shaped MLP up-projection (224 weight slices, two CTAs per SM)
+    as the benchmark runs it, every output."""
+    name = "decode_mlp_up_32x28672x8192"
+    w = synth.workload_inputs(name)
+    m, n, k = 32, 28672, 8192
+    d = gpu_gemm(MX, w["a_codes"], oracle.scale_tile(w["a_scales"]), w["b_codes"],
+                 oracle.scale_tile(w["b_scales"]), m, n, k, out_fp32=False)
+    ref, s_abs = oracle.mx_gemm(w["a_codes"], w["a_scales"], w["b_codes"], w["b_scales"], m, n, k)
+    stats = check_bf16(d, ref, s_abs, f"{name} (swapped kernel, two CTAs per SM)")
+    assert stats["exact"] > 0.9 * stats["total"]
 
 
 def test_swap_skinny_workload_full_size():
