@@ -26,7 +26,8 @@
 //               prefetch is safe when they do: L2 is the coherence point);
 //               then the weight tile (128 rows), the activation tile (M rows)
 //               and both operands' scale atoms of every stage of its K range
-//               into a 7-stage ring.
+//               into a ring of as many stages as shared and tensor memory
+//               hold (computed on the host).
 //   warp 1      allocates tensor memory; per stage, tcgen05.cp of the scale
 //               atoms into the stage's own columns and four K=64 MMAs
 //               (M = 128, N = M) into the M-column accumulator.
