@@ -33,12 +33,14 @@
 //               (M = 128, N = M) into the M-column accumulator.
 //   warps 2..5  one tensor-memory lane quarter each (32 weight rows = 32
 //               output columns, all M output rows): load the accumulator.
-//               CTAs of rank > 0 park their partials in their own idle stage
-//               ring and push them with one bulk copy into rank 0's (once rank
-//               0 has said its ring is idle); rank 0 adds them in rank order,
-//               applies alpha and the epilogue terms, and writes D straight
-//               from registers (a warp writes 32 consecutive columns of a row
-//               per store).
+//               With S > 1 the S CTAs reduce-scatter by columns: lane
+//               quarter q belongs to rank q * S / 4.  A warp whose quarter
+//               another rank owns parks its partials in the idle stage ring
+//               and sends them with one bulk copy into the owner's receive
+//               buffer (shared memory kept out of the ring, so no handshake
+//               is needed); the owner's warp adds the S partials in rank
+//               order, applies alpha and the epilogue terms, and writes its
+//               columns of D (32 consecutive columns of a row per store).
 // Every wait is bounded; the CTAs of a cluster meet at a cluster barrier
 // before leaving, so no remote copy or arrival targets a finished CTA.
 #include <cuda_bf16.h>
@@ -73,8 +75,10 @@ constexpr int kSwTmemCols = 512;  // one CTA per SM; 256 with two
 //               the guards keep every window inside the allocation;
 //   activations a ring of M x 128-byte tiles;
 //   scales      a ring of both operands' scale atoms per stage;
-//   barriers    full[slots], empty[slots], tfull, ring_free, partials, then
-//               the tensor-memory slot and the abort flag.
+//   receive     with S > 1, the partials of this rank's lane quarters from
+//               the other ranks: [S - 1][4 / S][M][32] FP32;
+//   barriers    full[slots], empty[slots], tfull, partials, then the
+//               tensor-memory slot and the abort flag.
 // A stage therefore takes R x 128 bytes of weight space, not 128 x 128, and
 // a CTA keeps 13 to 28 stages (about 200 KB) of loads in flight.
 template <int FMT>
@@ -98,7 +102,7 @@ struct SwapParams {
   int splits;           // CTAs per cluster (1, 2 or 4), one K range each
   int slots;            // stages in flight
   int tmem_cols;        // tensor-memory columns allocated (512, or 256 with two CTAs an SM)
-  int w_off, x_off, sf_off, bar_off;  // shared-memory layout (bytes; w_off: slot 0's slice)
+  int w_off, x_off, sf_off, rx_off, bar_off;  // shared-memory layout (bytes; w_off: slot 0's slice)
   EpiParams epi;        // bias / beta / GELU (applied by rank 0 after the sum)
 };
 
@@ -124,9 +128,8 @@ __global__ void __launch_bounds__(kSwThreads, 2)
   uint64_t *full = bars;
   uint64_t *empty = bars + slots;
   uint64_t *tfull = bars + 2 * slots;
-  uint64_t *ring_free = tfull + 1;  // ranks > 0: rank 0's ring may take partials
-  uint64_t *partials = tfull + 2;   // rank 0: the other ranks' partials are in (bytes)
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull + 3);
+  uint64_t *partials = tfull + 1;  // the other ranks' partials of this rank's quarters are in
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull + 2);
   volatile uint32_t *abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -153,11 +156,11 @@ __global__ void __launch_bounds__(kSwThreads, 2)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(tfull), 1);
-    mbar_init(smem_u32(ring_free), 1);
     mbar_init(smem_u32(partials), 1);
-    // rank 0 expects the partials of the S - 1 other ranks as bytes
-    if (S > 1 && rank == 0)
-      mbar_arrive_expect_tx(smem_u32(partials), static_cast<uint32_t>((S - 1) * m * kSwRows * 4));
+    // each rank expects the other S - 1 ranks' partials of its 4 / S lane
+    // quarters, as bytes
+    if (S > 1)
+      mbar_arrive_expect_tx(smem_u32(partials), static_cast<uint32_t>((S - 1) * m * kSwRows * 4 / S));
     *abort = 0u;
     fence_barrier_init();
     prefetch_tmap(&tmap_w);
@@ -295,40 +298,51 @@ __global__ void __launch_bounds__(kSwThreads, 2)
         for (int j = 0; j < 32; ++j) acc[32 + j] = __uint_as_float(r[j]);
       }
     }
-    // rank 0's ring is idle once its accumulator is complete: let the other
-    // ranks copy their partials there
-    float *recv = reinterpret_cast<float *>(smem);  // [S - 1][m][128]
-    if (S > 1 && rank == 0 && warp == 2 && lane == 0 && ok) {
-      for (int r2 = 1; r2 < S; ++r2)
-        mbar_arrive_cluster_release(mapa_shared(smem_u32(ring_free), static_cast<uint32_t>(r2)));
-    }
-    if (S > 1 && rank > 0) {
-      // park the partials [m][128] in this CTA's idle ring, then one thread
-      // copies them to rank 0 once its ring is free
+    // Lane quarter q of every CTA's accumulator belongs to rank q / qpr.
+    // Its place in the idle ring, [4][m][32] FP32 by quarter, holds the
+    // partials a sender parks there, or the owner's output box.
+    const int qpr = 4 / S;  // lane quarters per rank
+    const uint32_t owner = static_cast<uint32_t>(q / qpr);
+    uint32_t *box = reinterpret_cast<uint32_t *>(smem + q * (m * 32 * 4));
+    if (S > 1 && owner != rank) {
+      // park this quarter's partials and send them to slot (this rank, less
+      // one if above the owner) of the owner's receive buffer
       if (ok) {
 #pragma unroll
-        for (int j = 0; j < m; ++j) recv[j * kSwRows + q * 32 + lane] = acc[j];
+        for (int j = 0; j < m; ++j) box[j * 32 + lane] = __float_as_uint(acc[j]);
       }
       fence_proxy_async_smem();
-      named_barrier_sync(1, 128);
-      if (warp == 2) {
-        if (ok) ok = mbar_wait_acq_cluster(smem_u32(ring_free), 0u, abort, p.status);
-        if (__all_sync(0xFFFFFFFFu, ok) && lane == 0)
-          bulk_copy_to_cluster(
-              mapa_shared(smem_u32(recv), 0) + static_cast<uint32_t>((rank - 1) * m * kSwRows * 4),
-              smem_u32(recv), static_cast<uint32_t>(m * kSwRows * 4),
-              mapa_shared(smem_u32(partials), 0));
+      __syncwarp();
+      if (__all_sync(0xFFFFFFFFu, ok) && lane == 0) {
+        const uint32_t slot = rank < owner ? rank : rank - 1u;
+        const uint32_t qq = static_cast<uint32_t>(q) - owner * qpr;
+        const uint32_t bytes = static_cast<uint32_t>(m * 32 * 4);
+        bulk_copy_to_cluster(
+            mapa_shared(smem_u32(smem + p.rx_off), owner) + (slot * qpr + qq) * bytes,
+            smem_u32(box), bytes, mapa_shared(smem_u32(partials), owner));
       }
     } else if (ok) {
       if (S > 1) {
         ok = mbar_wait(smem_u32(partials), 0u, abort, p.status);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (ok) {
-          // the sum in rank order: ((acc_0 + acc_1) + acc_2) + acc_3
-          for (int r2 = 1; r2 < S; ++r2)
+          // the sum in rank order, ((p_0 + p_1) + p_2) + p_3, with p_rank the
+          // accumulator: first e = ((p_0 + p_1) + ...) + p_(rank-1) in
+          // receive slot 0, then e + p_rank (= p_rank + e), then the rest
+          float *rxq = reinterpret_cast<float *>(smem + p.rx_off) + (q - rank * qpr) * m * 32 + lane;
+          const int slot_stride = qpr * m * 32;
+          for (int r2 = 1; r2 < static_cast<int>(rank); ++r2)
 #pragma unroll
             for (int j = 0; j < m; ++j)
-              acc[j] = __fadd_rn(acc[j], recv[((r2 - 1) * m + j) * kSwRows + q * 32 + lane]);
+              rxq[j * 32] = __fadd_rn(rxq[j * 32], rxq[r2 * slot_stride + j * 32]);
+          if (rank > 0) {
+#pragma unroll
+            for (int j = 0; j < m; ++j) acc[j] = __fadd_rn(acc[j], rxq[j * 32]);
+          }
+          for (int r2 = static_cast<int>(rank) + 1; r2 < S; ++r2)
+#pragma unroll
+            for (int j = 0; j < m; ++j)
+              acc[j] = __fadd_rn(acc[j], rxq[(r2 - 1) * slot_stride + j * 32]);
         }
       }
       if (ok && mine && col - lane < p.n) {  // N % 32 == 0: a warp's columns are all in or out
@@ -338,9 +352,7 @@ __global__ void __launch_bounds__(kSwThreads, 2)
         if (p.epi.bias != nullptr && in_bounds(col, 1, p.epi.bias_elems, p.epi.status))
           bias = __ldg(p.epi.bias + col);
         const int64_t mn = static_cast<int64_t>(m) * p.n;
-        // this warp's m x 32 outputs, staged after the received partials
-        uint32_t *box = reinterpret_cast<uint32_t *>(smem + (S - 1) * m * kSwRows * 4 +
-                                                     (warp - 2) * (m * 32 * 4));
+        // this warp's m x 32 outputs are staged in its quarter's box
 #pragma unroll
         for (int j = 0; j < m; j += 2) {
           const int64_t i0 = static_cast<int64_t>(j) * p.n + col, i1 = i0 + p.n;
@@ -374,7 +386,6 @@ __global__ void __launch_bounds__(kSwThreads, 2)
             f1 = g.y;
           }
           // rows j, j + 1 of this warp's 32 columns, staged in shared memory
-          // (the ring is idle: rank 0's received partials were already added)
           if constexpr (OUT_F32) {
             box[j * 32 + lane] = __float_as_uint(f0);
             box[(j + 1) * 32 + lane] = __float_as_uint(f1);
@@ -408,6 +419,9 @@ __global__ void __launch_bounds__(kSwThreads, 2)
   tc_fence_before();
   __syncthreads();
   if (S > 1) cluster_sync();  // no CTA leaves while another may still write to it
+  // After an abort a copy into this CTA may still be in flight (its sender
+  // did not know): wait (bounded) for the bytes before shared memory goes.
+  if (S > 1 && threadIdx.x == 64 && *abort) mbar_drain(smem_u32(partials), 0u);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -455,7 +469,10 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   const int guard = (kSwRows - p.wrows) * kSwStageKBytes;
   const int per_slot = (p.wrows + m) * kSwStageKBytes + 2 * C::kSfBytes;
   const int fixed = 2 * guard + 1024 /* alignment of the activation ring */ + 256 /* barriers */;
-  int slots = (smem_budget - fixed - 16 * kSwMaxSlots) / per_slot;
+  // with a split, the receive buffer: the other ranks' partials of this
+  // rank's 4 / S lane quarters
+  const int rx_bytes = (g.split_k - 1) * m * kSwRows * 4 / g.split_k;
+  int slots = (smem_budget - fixed - rx_bytes - 16 * kSwMaxSlots) / per_slot;
   slots = slots < kSwMaxSlots ? slots : kSwMaxSlots;
   const int tmem_slots = (p.tmem_cols - kSwSfCol) / C::kSfSetCols;
   slots = slots < tmem_slots ? slots : tmem_slots;
@@ -465,13 +482,12 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   const int w_end = guard + slots * p.wrows * kSwStageKBytes + guard;
   p.x_off = (w_end + 1023) / 1024 * 1024;
   p.sf_off = p.x_off + slots * m * kSwStageKBytes;
-  p.bar_off = p.sf_off + slots * 2 * C::kSfBytes;
-  const int smem_bytes = p.bar_off + 8 * (2 * slots + 3) + 16;
-  // after the main loop the weight ring holds rank 0's received partials
-  // ([S - 1][m][128] FP32 at offset 0), then the four warps' output boxes
-  // (m x 32 each, at most FP32)
-  if (smem_bytes > smem_budget || (g.split_k - 1) * m * kSwRows * 4 + 4 * m * 32 * 4 > w_end)
-    return cudaErrorInvalidValue;
+  p.rx_off = p.sf_off + slots * 2 * C::kSfBytes;
+  p.bar_off = p.rx_off + rx_bytes;
+  const int smem_bytes = p.bar_off + 8 * (2 * slots + 2) + 16;
+  // after the main loop the weight ring holds the four lane quarters' parked
+  // partials or output boxes ([4][m][32] FP32 at offset 0)
+  if (smem_bytes > smem_budget || 4 * m * 32 * 4 > w_end) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -493,8 +509,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 }  // namespace
 
 // Shape of the swapped kernel for N weight rows: rows per CTA (128, 64 or 32)
-// and CTAs per cluster (1, 2 or 4; 4 only for M = 32, whose partials fit the
-// ring three times).  Preference order: whole 128-row slices first (measured
+// and CTAs per cluster (1, 2 or 4; 4 only for M = 32).  Preference order: whole 128-row slices first (measured
 // on GB300: a CTA streaming 128-row slices reaches about twice the HBM rate of
 // one streaming 64-row slices), split along K over a cluster before the slices
 // get thinner; the first shape whose CTAs fill at least three quarters of the
