@@ -8,16 +8,19 @@
 // change: they are indexed by (operand row, block along K) in either storage
 // order.
 //
-// One CTA of 256 threads per 128-row x 256-column tile (16 KB in, 16 KB out):
-// each thread issues four 16-byte loads of input rows before it stores any
-// into shared memory; after one barrier each thread builds four times 16
-// output bytes (the codes of one input column over 32 consecutive input
-// rows) and stores them with 16-byte stores.  Measured on the 8192 x 28672
-// weight: 47.3 us (4.96 TB/s); tiles of 64 rows gave 71.8 us, of 256 rows
-// 55.3 us (fewer CTAs per SM).
-// Rows and cols are multiples of 32, so every 16-byte piece is wholly inside
-// or outside the matrix and 16-byte aligned.  HBM bound: it moves each code
-// byte once in and once out.
+// One CTA of 256 threads per 128-row x 256-column tile (16 KB in, 16 KB out).
+// Each thread issues four 16-byte loads of input rows before it stores any
+// into shared memory; after one barrier each thread transposes two 8 x 8
+// blocks of codes in registers (eight 32-bit words, one per input row, become
+// eight words, one per input column: three rounds of masked swaps, of 4 x 4,
+// 2 x 2 and 1 x 1 sub-blocks) and writes each word straight to its output
+// row; the eight lanes that hold one output row's neighbouring blocks fill
+// whole 32-byte sectors.  (The previous version built every output byte from
+// two nibble reads of shared memory, about 25 instructions a byte, and was
+// bound by instruction issue: 47.3 us on the 8192 x 28672 weight.)
+// Rows and cols are multiples of 32, so every 16-byte load and every 8 x 8
+// block is wholly inside or outside the matrix.  HBM bound: it moves each
+// code byte once in and once out.
 #include <cstdint>
 
 #include "mx_device.cuh"
@@ -30,21 +33,45 @@ constexpr int kTrThreads = 256;
 constexpr int kTrRows = 128;          // input rows per tile (a multiple of 32)
 constexpr int kTrCols = 256;           // input columns (codes) per tile: 128 bytes a row
 constexpr int kTrWords = kTrCols / 8;  // 32-bit words of a tile row (8 codes each)
-constexpr int kTrIn = kTrRows * (kTrCols / 32) / kTrThreads;   // 16-byte loads per thread
-constexpr int kTrOut = kTrCols * (kTrRows / 32) / kTrThreads;  // 16-byte stores per thread
-static_assert(kTrIn >= 1 && kTrOut >= 1, "whole 16-byte pieces per thread");
+constexpr int kTrIn = kTrRows * (kTrCols / 32) / kTrThreads;            // 16-byte loads per thread
+constexpr int kTrBlocks = (kTrRows / 8) * kTrWords / kTrThreads;       // 8 x 8 blocks per thread
+static_assert(kTrIn >= 1 && kTrBlocks == 2 && kTrWords == 32, "thread mapping below");
 
-// Word w of tile row r sits at column (w + r / 32) % 32 of a 33-word row: the
-// threads of a warp read rows 32 apart, and the rotation puts them in
-// different banks.
-__device__ __forceinline__ int tr_slot(int r, int w) { return r * (kTrWords + 1) + ((w + (r >> 5)) & 31); }
+// Word w of tile row r sits at w ^ (4 * (r / 8 % 8)) of its 32-word row: the
+// XOR keeps each 16-byte group of a row together (the row loads store whole
+// groups), and the lanes of a warp that read one word column of eight
+// different 8-row blocks land in eight different groups of banks.
+__device__ __forceinline__ int tr_slot(int r, int w) { return r * kTrWords + (w ^ (4 * ((r >> 3) & 7))); }
+
+// a[i] holds codes (i, 0..7) of an 8 x 8 block (code k in nibble k); on
+// return a[k] holds codes (0..7, k) (code i in nibble i).
+__device__ __forceinline__ void transpose8x8_nibbles(uint32_t (&a)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // the 4 x 4 corner blocks: columns 4..7 of rows 0..3 <-> 0..3 of 4..7
+    const uint32_t t = ((a[i] >> 16) ^ a[i + 4]) & 0x0000FFFFu;
+    a[i] ^= t << 16;
+    a[i + 4] ^= t;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += (i & 1) ? 3 : 1) {  // i = 0, 1, 4, 5: 2 x 2 blocks in each quadrant
+    const uint32_t t = ((a[i] >> 8) ^ a[i + 2]) & 0x00FF00FFu;
+    a[i] ^= t << 8;
+    a[i + 2] ^= t;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {  // single codes in each 2 x 2 block
+    const uint32_t t = ((a[i] >> 4) ^ a[i + 1]) & 0x0F0F0F0Fu;
+    a[i] ^= t << 4;
+    a[i + 1] ^= t;
+  }
+}
 
 __global__ void __launch_bounds__(kTrThreads) fp4_transpose_kernel(
     const uint8_t *__restrict__ in, int64_t rows, int64_t cols, uint8_t *__restrict__ out,
     uint32_t *status) {
   griddep_launch_dependents();
   griddep_wait();
-  __shared__ uint32_t tile[kTrRows * (kTrWords + 1)];
+  __shared__ __align__(16) uint32_t tile[kTrRows * kTrWords];
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTrRows;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTrCols;
   const int64_t in_pitch = cols / 2, out_pitch = rows / 2;
@@ -64,37 +91,28 @@ __global__ void __launch_bounds__(kTrThreads) fp4_transpose_kernel(
   for (int j = 0; j < kTrIn; ++j) {
     const int id = threadIdx.x + j * kTrThreads;
     const int lr = id >> 3, q = id & 7;
-    tile[tr_slot(lr, 4 * q + 0)] = v[j].x;
-    tile[tr_slot(lr, 4 * q + 1)] = v[j].y;
-    tile[tr_slot(lr, 4 * q + 2)] = v[j].z;
-    tile[tr_slot(lr, 4 * q + 3)] = v[j].w;
+    *reinterpret_cast<uint4 *>(&tile[tr_slot(lr, 4 * q)]) = v[j];
   }
   __syncthreads();
-  // output row c0 + oc (an input column), bytes r0 / 2 + 16 h .. + 15: byte b
-  // holds the codes of input rows 2b and 2b + 1 (low, high nibble); the
-  // neighbouring threads of a warp complete the row's bytes of this tile
+  // warp wp, lane (b = lane % 8, g = lane / 8): word column w = 4 wp + g,
+  // 8-row blocks b and b + 8
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int w = 4 * wp + (lane >> 3);
 #pragma unroll
-  for (int j = 0; j < kTrOut; ++j) {
-    const int id = threadIdx.x + j * kTrThreads;
-    const int oc = id / (kTrRows / 32), h = id % (kTrRows / 32);
-    if (c0 + oc >= cols || r0 + 32 * h >= rows) continue;
-    const int word = oc >> 3, shift = 4 * (oc & 7);
-    uint32_t o[4];
+  for (int j = 0; j < kTrBlocks; ++j) {
+    const int rb = (lane & 7) + 8 * j;  // 8-row block of the tile
+    uint32_t a[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t packed = 0;
+    for (int i = 0; i < 8; ++i) a[i] = tile[tr_slot(8 * rb + i, w)];
+    transpose8x8_nibbles(a);
+    // a[k]: output row c0 + 8 w + k (an input column), its codes of input
+    // rows r0 + 8 rb .. + 7 = output bytes r0 / 2 + 4 rb .. + 3
+    if (c0 + 8 * w >= cols || r0 + 8 * rb >= rows) continue;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int r = 32 * h + 8 * i + 2 * b;  // input rows r, r + 1 of the tile
-        const uint32_t lo = (tile[tr_slot(r, word)] >> shift) & 0xFu;
-        const uint32_t hi = (tile[tr_slot(r + 1, word)] >> shift) & 0xFu;
-        packed |= (lo | (hi << 4)) << (8 * b);
-      }
-      o[i] = packed;
+    for (int k = 0; k < 8; ++k) {
+      const int64_t off = (c0 + 8 * w + k) * out_pitch + r0 / 2 + 4 * rb;
+      if (in_bounds(off, 4, cols * out_pitch, status)) *reinterpret_cast<uint32_t *>(out + off) = a[k];
     }
-    const int64_t off = (c0 + oc) * out_pitch + r0 / 2 + 16 * h;
-    if (in_bounds(off, 16, cols * out_pitch, status))
-      *reinterpret_cast<uint4 *>(out + off) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
