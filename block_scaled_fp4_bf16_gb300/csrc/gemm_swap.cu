@@ -509,23 +509,28 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 }  // namespace
 
 // Shape of the swapped kernel for N weight rows: rows per CTA (128, 64 or 32)
-// and CTAs per cluster (1, 2 or 4; 4 only for M = 32).  Preference order: whole 128-row slices first (measured
-// on GB300: a CTA streaming 128-row slices reaches about twice the HBM rate of
-// one streaming 64-row slices), split along K over a cluster before the slices
-// get thinner; the first shape whose CTAs fill at least three quarters of the
-// SMs and fit on them at one per SM (each split keeping >= 4 stages of K),
-// else the one with the most CTAs that fit; when none fits (more 128-row
-// slices than SMs), 128-row slices with no split, which launch_gemm_swap then
-// runs at two CTAs per SM.
+// and CTAs per cluster (1, 2 or 4).  Preference order: whole 128-row slices
+// first (measured on GB300: a CTA streaming 128-row slices reaches about
+// twice the HBM rate of one streaming 64-row slices), split along K over a
+// cluster before the slices get thinner; the first shape whose CTAs fill at
+// least three quarters of the SMs and fit on them at one per SM (each split
+// keeping >= 4 stages of K, 8 for M = 64 in four), else the one with the
+// most CTAs that fit; when none fits (more 128-row slices than SMs), 128-row
+// slices with no split, which launch_gemm_swap then runs at two CTAs per SM.
 void gemm_swap_shape(int64_t m, int64_t n, int64_t k, int num_sms, int *wrows, int *splits) {
   const int64_t stages = k / 256;
   const int64_t want = num_sms - num_sms / 4;
-  const int smax = m <= 32 ? 4 : 2;
+  const int smax = 4;
   int best_r = 128, best_s = 1;
   int64_t best_ctas = 0;
   for (int r = 128; r >= 32; r /= 2) {
     for (int sp = 1; sp <= smax; sp *= 2) {
-      if (sp > 1 && stages < 4 * sp) break;
+      // >= 4 stages of K per split; >= 8 when 64-row accumulators are
+      // exchanged four ways (measured: 64 x 4096 x 4096 at 128 rows x 4
+      // splits of 4 stages 8.97 us, at 64 rows x 2 splits 8.48 us; with 8
+      // stages a split the four-way split gains, 64 x 2048 x 8192 10.51 ->
+      // 9.63 us)
+      if (sp > 1 && stages < (m > 32 && sp == 4 ? 8 : 4) * sp) break;
       const int64_t ctas = (n + r - 1) / r * sp;
       if (ctas > num_sms) break;
       if (ctas >= want) {
@@ -546,7 +551,7 @@ void gemm_swap_shape(int64_t m, int64_t n, int64_t k, int num_sms, int *wrows, i
 
 cudaError_t launch_gemm_swap(const GemmArgs &g, cudaStream_t s) {
   if (g.m > kSwMaxM || g.m % 32 != 0 || (g.split_k != 1 && g.split_k != 2 && g.split_k != 4) ||
-      (g.m > 32 && g.split_k > 2) || (g.bn != 128 && g.bn != 64 && g.bn != 32))
+      (g.bn != 128 && g.bn != 64 && g.bn != 32))
     return cudaErrorInvalidValue;
   if (g.m == 32) {
     if (g.fmt == 0) return g.out_fp32 ? launch_typed<0, 1, 1>(g, s) : launch_typed<0, 0, 1>(g, s);

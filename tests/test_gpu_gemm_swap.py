@@ -34,10 +34,11 @@ def _check(d, ref, s_abs, out_fp32, what):
 
 # (m, n, k): cluster of 1 (one stage; one block with 96 rows past N), of 2, of 4,
 # ragged N, M = 64, and more 128-row blocks than SMs (two CTAs per SM, also
-# with a ragged last block and with more blocks than two per SM hold)
+# with a ragged last block and with more blocks than two per SM hold); M = 64
+# in clusters of 4 (128- and 64-row slices, the latter with a ragged last one)
 SHAPES = [(32, 32, 256), (32, 8192, 8192), (32, 4096, 4096), (64, 4224, 2048),
           (32, 1056, 1024), (64, 640, 1024), (32, 28672, 512), (64, 28672, 1024),
-          (32, 24608, 2048), (32, 45056, 512)]
+          (32, 24608, 2048), (32, 45056, 512), (64, 4096, 8192), (64, 2080, 8192)]
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
@@ -51,7 +52,7 @@ def test_swap_mxfp4_matches_oracle(m, n, k, out_fp32):
 
 
 @pytest.mark.parametrize("m,n,k", [(32, 4096, 4096), (64, 1152, 2048), (32, 96, 512),
-                                   (32, 28672, 1024), (64, 20480, 512)])
+                                   (32, 28672, 1024), (64, 20480, 512), (64, 4096, 8192)])
 @pytest.mark.parametrize("out_fp32", [True, False])
 def test_swap_nvfp4_matches_oracle(m, n, k, out_fp32):
     xa = synth.bf16_normal(m, k, 1.0, seed=m * 3 + k)
