@@ -509,28 +509,57 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 }  // namespace
 
 // Shape of the swapped kernel for N weight rows: rows per CTA (128, 64 or 32)
-// and CTAs per cluster (1, 2 or 4).  Preference order: whole 128-row slices
-// first (measured on GB300: a CTA streaming 128-row slices reaches about
-// twice the HBM rate of one streaming 64-row slices), split along K over a
-// cluster before the slices get thinner; the first shape whose CTAs fill at
-// least three quarters of the SMs and fit on them at one per SM (each split
-// keeping >= 4 stages of K, 8 for M = 64 in four), else the one with the
-// most CTAs that fit; when none fits (more 128-row slices than SMs), 128-row
-// slices with no split, which launch_gemm_swap then runs at two CTAs per SM.
+// and CTAs per cluster (1, 2 or 4).
+//
+// From 8 128-row slices up (N > 896): 128-row slices (a sweep of every
+// slice height and split count on GB300 never found thinner slices more than
+// 1 % faster), and the split count S that minimises a call-time model fitted
+// to that sweep (us):
+//   T(S) = F(S) + 0.01 * CTAs + max(0.26 * stages per split, bytes / 7 TB/s)
+// with F = 3.0, 3.8, 4.8 for S = 1, 2, 4 (the fixed cost, which grows with
+// the exchange of partials), 0.26 us the time a CTA takes per stage of its
+// stream (about 87 GB/s for a 128-row stage with its activations and
+// scales), and 7 TB/s the weight stream of the whole GPU.  Its choices were
+// the fastest measured (or within 2.5 %) on 32 and 64 x 1024..16384 x
+// 2048..8192; e.g. 32 x 4096 x 4096: S = 2, 6.05 us, against 6.71 for the
+// previous rule's S = 4; 32 x 2048 x 8192: S = 4, 6.87 against 7.5 us with
+// 64-row slices.  Only splits whose CTAs fit on the SMs at one each are
+// considered; with more slices than SMs, S = 1 and launch_gemm_swap runs two
+// CTAs per SM.
+//
+// Below 8 slices: the first shape (128-row slices first, split along K
+// before the slices get thinner) whose CTAs fill at least three quarters of
+// the SMs at one per SM with >= 4 stages of K per split, else the one with
+// the most CTAs that fit.
 void gemm_swap_shape(int64_t m, int64_t n, int64_t k, int num_sms, int *wrows, int *splits) {
   const int64_t stages = k / 256;
+  const int64_t slices = (n + kSwRows - 1) / kSwRows;
+  if (slices >= 8) {
+    constexpr double kFixedUs[3] = {3.0, 3.8, 4.8};  // S = 1, 2, 4
+    const double stream_us = static_cast<double>(m + n) * static_cast<double>(k) * 0.53125 / 7.0e6;
+    double best_t = 0.0;
+    int best_s = 1;
+    for (int sp = 1, i = 0; sp <= 4; sp *= 2, ++i) {
+      const int64_t ctas = slices * sp;
+      if (sp > 1 && (sp > stages || ctas > num_sms)) break;
+      const double cta_us = 0.26 * static_cast<double>((stages + sp - 1) / sp);
+      const double t = kFixedUs[i] + 0.01 * static_cast<double>(ctas) +
+                       (cta_us > stream_us ? cta_us : stream_us);
+      if (sp == 1 || t < best_t) {
+        best_t = t;
+        best_s = sp;
+      }
+    }
+    *wrows = kSwRows;
+    *splits = best_s;
+    return;
+  }
   const int64_t want = num_sms - num_sms / 4;
-  const int smax = 4;
   int best_r = 128, best_s = 1;
   int64_t best_ctas = 0;
   for (int r = 128; r >= 32; r /= 2) {
-    for (int sp = 1; sp <= smax; sp *= 2) {
-      // >= 4 stages of K per split; >= 8 when 64-row accumulators are
-      // exchanged four ways (measured: 64 x 4096 x 4096 at 128 rows x 4
-      // splits of 4 stages 8.97 us, at 64 rows x 2 splits 8.48 us; with 8
-      // stages a split the four-way split gains, 64 x 2048 x 8192 10.51 ->
-      // 9.63 us)
-      if (sp > 1 && stages < (m > 32 && sp == 4 ? 8 : 4) * sp) break;
+    for (int sp = 1; sp <= 4; sp *= 2) {
+      if (sp > 1 && stages < 4 * sp) break;
       const int64_t ctas = (n + r - 1) / r * sp;
       if (ctas > num_sms) break;
       if (ctas >= want) {
