@@ -418,10 +418,14 @@ __global__ void __launch_bounds__(kSwThreads, 2)
 
   tc_fence_before();
   __syncthreads();
-  if (S > 1) cluster_sync();  // no CTA leaves while another may still write to it
   // After an abort a copy into this CTA may still be in flight (its sender
-  // did not know): wait (bounded) for the bytes before shared memory goes.
-  if (S > 1 && threadIdx.x == 64 && *abort) mbar_drain(smem_u32(partials), 0u);
+  // did not know): wait (bounded) for its bytes before the cluster barrier,
+  // which holds every sender, and so the source of every copy, until then.
+  // (Every role has passed the barrier above: the abort flag no longer
+  // changes, and the whole warp takes the same branch.)
+  if (S > 1 && warp == 2 && *abort) mbar_drain(smem_u32(partials), 0u);
+  __syncwarp();
+  if (S > 1) cluster_sync();  // no CTA leaves while another may still write to it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
