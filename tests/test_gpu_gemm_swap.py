@@ -36,11 +36,12 @@ def _check(d, ref, s_abs, out_fp32, what):
 # ragged N, M = 64, and more 128-row blocks than SMs (two CTAs per SM, also
 # with a ragged last block and with more blocks than two per SM hold); M = 64
 # in clusters of 4 (a ragged last 128-row slice); 32-row slices in clusters of
-# 4 and of 2 (the latter with a ragged last 128-row atom)
+# 4 and of 2 (the latter with a ragged last 128-row atom), and for M = 64 in
+# clusters of 4 (one lane quarter of real output per CTA)
 SHAPES = [(32, 32, 256), (32, 8192, 8192), (32, 4096, 4096), (64, 4224, 2048),
           (32, 1056, 1024), (64, 640, 1024), (32, 28672, 512), (64, 28672, 1024),
           (32, 24608, 2048), (32, 45056, 512), (64, 4096, 8192), (64, 2080, 8192),
-          (32, 768, 4096), (64, 864, 2048)]
+          (32, 768, 4096), (64, 864, 2048), (64, 512, 8192)]
 
 
 @pytest.mark.parametrize("m,n,k", SHAPES)
