@@ -400,3 +400,28 @@ def test_calibrate_argument_validation(lib):
         mx.MX_ERR_INVALID_ARG
     assert lib.mx_calibrate_mma(0, 1, 16, None, 0, None, u, None) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_calibrate_mma(0, 1, 16, FAKE + 4, 152, f, u, None) == mx.MX_ERR_ALIGNMENT
+
+
+def test_maximum_sizes_are_rejected_before_any_launch(lib):
+    """The largest shapes the kernels' index arithmetic covers: beyond them
+    every entry point answers MX_ERR_UNSUPPORTED_SHAPE (GEMM dimensions and
+    quantize rows / cols below 2^31, fewer than 2^31 scale blocks, transpose
+    rows below 64 * 65536), and the limit itself is accepted as far as the
+    shape checks go (the fake pointers then fail the alignment check)."""
+    big = 1 << 31
+    assert _gemm(lib, m=big) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, n=big) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, k=big) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert _gemm(lib, m=big - 32, a=FAKE_ODD) == mx.MX_ERR_ALIGNMENT
+    q = lib.mx_quantize_bf16
+    # rows x (cols / 32) scale blocks reach 2^31 (cols = 2^16: 2^11 blocks a row)
+    assert q(FAKE, 1 << 20, 1 << 16, 1 << 16, 0, 0, FAKE, FAKE, None, None, 0, None) == \
+        mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert q(FAKE_ODD, (1 << 20) - 128, 1 << 16, 1 << 16, 0, 0, FAKE, FAKE, None, None, 0,
+             None) == mx.MX_ERR_ALIGNMENT
+    assert q(FAKE, big, 32, 32, 0, 0, FAKE, FAKE, None, None, 0, None) == \
+        mx.MX_ERR_UNSUPPORTED_SHAPE
+    t = lib.mx_fp4_transpose
+    assert t(FAKE, 64 * 65536, 32, FAKE + (1 << 40), None) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert t(FAKE, 32, big, FAKE + (1 << 40), None) == mx.MX_ERR_UNSUPPORTED_SHAPE
+    assert t(FAKE_ODD, 64 * 65535, 32, FAKE + (1 << 40), None) == mx.MX_ERR_ALIGNMENT
