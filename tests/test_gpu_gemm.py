@@ -362,3 +362,18 @@ def test_workspace_too_small_is_rejected():
 
 def test_device_is_available():
     assert mx.mx_available()
+
+
+def test_pair_gemm_very_tall_a():
+    """M = 2^17 rows of A (512 256-row tiles, 6.7 waves of pair tiles), N = 256,
+    K = 256: the tile walk and the output offsets at a size where 32-bit products
+    of them would overflow; every output against the oracle."""
+    m, n, k = 1 << 17, 256, 256
+    a = synth.fp4_codes(m, k, 91)
+    sa = synth.scale_bytes(m, k // 32, 120, 134, 92)
+    b = synth.fp4_codes(n, k, 93)
+    sb = synth.scale_bytes(n, k // 32, 120, 134, 94)
+    d = gpu_gemm(MX, a, oracle.scale_tile(sa), b, oracle.scale_tile(sb), m, n, k, out_fp32=False)
+    ref, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
+    stats = check_bf16(d, ref, s_abs, "pair 2^17 x 256 x 256")
+    assert stats["exact"] > 0.9 * stats["total"]

@@ -106,3 +106,15 @@ def test_swap_skinny_workload_full_size():
     ref, s_abs = oracle.mx_gemm(w["a_codes"], w["a_scales"], w["b_codes"], w["b_scales"], m, n, k)
     stats = check_bf16(d, ref, s_abs, "skinny 32x8192x8192 (swapped kernel)")
     assert stats["exact"] > 0.9 * stats["total"]
+
+
+def test_swap_very_wide_weight():
+    """N = 2^20 weight rows (8192 slices of 128, far more than two per SM hold),
+    K = 256: the grid, the slice offsets and the output indices at a size where
+    32-bit products of them would overflow; every output against the oracle."""
+    m, n, k = 32, 1 << 20, 256
+    a, sa, b, sb = _mx_case(m, n, k, seed=77)
+    d = gpu_gemm(MX, a, oracle.scale_tile(sa), b, oracle.scale_tile(sb), m, n, k, out_fp32=False)
+    ref, s_abs = oracle.mx_gemm(a, sa, b, sb, m, n, k)
+    stats = check_bf16(d, ref, s_abs, "swap 32 x 2^20 x 256")
+    assert stats["exact"] > 0.9 * stats["total"]
