@@ -234,10 +234,11 @@ def _gpu_transpose(codes, rows, cols):
 
 
 @pytest.mark.parametrize("rows,cols", [(32, 32), (64, 128), (96, 4128), (160, 96), (4096, 1056),
-                                       (8192, 8192)])
+                                       (8192, 8192), (1 << 21, 64), (32, 1 << 22)])
 def test_fp4_transpose_matches_oracle(rows, cols):
-    """Bit-exact against the oracle: one and several 64 x 128 tiles, ragged
-    tails in both directions, and a full 8192 x 8192 weight."""
+    """Bit-exact against the oracle: one and several 128 x 256 tiles, ragged
+    tails in both directions, a full 8192 x 8192 weight, and tile grids 16384
+    tiles tall or 16384 tiles wide."""
     codes = synth.fp4_codes(rows, cols, seed=rows * 7 + cols)
     assert np.array_equal(_gpu_transpose(codes, rows, cols),
                           oracle.fp4_transpose(codes, rows, cols))
