@@ -17,7 +17,9 @@
 // One CTA per SM, with a stage ring as deep as shared memory allows; or, when
 // the CTAs outnumber the SMs (more than num_sms 128-row weight slices), two
 // CTAs per SM, each with half the shared and tensor memory, so that all of
-// them stream in one wave.
+// them stream in one wave; for M = 32, three (a third each) when two per SM
+// would still take two waves, or (MXFP4) when each CTA streams at most 8
+// stages of K and the shallower ring costs nothing.
 //
 // Roles (192 threads):
 //   warp 0      TMA producer: before waiting for the previous kernel, the
@@ -59,12 +61,12 @@ constexpr int kSwRows = 128;        // rows of the MMA's weight tile (its M)
 constexpr int kSwStageKBytes = 128; // 256 FP4 codes of K per stage
 constexpr int kSwMaxSlots = 32;
 constexpr int kSwSmemBytes = 232448;
-// Two CTAs per SM (when the CTAs outnumber the SMs): each takes half of an
-// SM's shared memory (less the 1 KB the runtime reserves per CTA) and half of
-// its tensor memory.
-constexpr int kSwSmemBytesDense = 233472 / 2 - 1024;
+// Two or three CTAs per SM (when the CTAs outnumber the SMs): each takes that
+// share of an SM's shared memory (less the 1 KB the runtime reserves per CTA)
+// and of its tensor memory.
+constexpr int kSwSmemPerSm = 233472;
 constexpr int kSwSfCol = kSwMaxM;   // tensor memory: accumulator (<= 64 columns), then scales
-constexpr int kSwTmemCols = 512;  // one CTA per SM; 256 with two
+constexpr int kSwTmemCols = 512;  // one CTA per SM; 256 with two, 128 with three
 
 // Shared memory of a CTA, laid out by the host for (format, M, weight rows R):
 //   weights     a ring of `slots` slices of R rows x 128 bytes, with
@@ -101,7 +103,7 @@ struct SwapParams {
   int wrows;            // weight rows per CTA: 128, 64 or 32 (a part of a 128-row atom)
   int splits;           // CTAs per cluster (1, 2 or 4), one K range each
   int slots;            // stages in flight
-  int tmem_cols;        // tensor-memory columns allocated (512, or 256 with two CTAs an SM)
+  int tmem_cols;        // tensor-memory columns allocated (512; 256 or 128 with two or three CTAs an SM)
   int w_off, x_off, sf_off, rx_off, bar_off;  // shared-memory layout (bytes; w_off: slot 0's slice)
   EpiParams epi;        // bias / beta / GELU (applied by rank 0 after the sum)
 };
@@ -114,7 +116,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // MT: M / 32 (1 or 2), so that the accumulator rows of a thread are
 // registers indexed by compile-time constants.
 template <int FMT, int OUT_F32, int MT>
-__global__ void __launch_bounds__(kSwThreads, 2)
+__global__ void __launch_bounds__(kSwThreads, MT == 1 ? 3 : 2)
     gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_x, const SwapParams p) {
   using C = SwapCfg<FMT>;
@@ -462,11 +464,25 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
   // CTAs per SM, each with half the ring, so that all of them stream at once
   // instead of in two waves (measured, 32 x 28672 x 8192: 27.8 -> 21.3 us;
   // the grids that fit one CTA per SM keep the deeper ring, which is faster
-  // for them).
+  // for them).  Three for M = 32 (the M = 64 instance needs more registers
+  // than three CTAs of an SM leave) when two per SM would take two waves
+  // (32 x 45056 x 512: MXFP4 7.74 -> 4.60 us, NVFP4 7.67 -> 4.71 us) or, for
+  // MXFP4, each CTA streams at most 8 stages (32 x 24608 x 2048: 7.88 -> 7.54
+  // us; NVFP4, whose scale sets leave a third of the tensor memory room for
+  // a ring of two, 32 x 28672 x 1024: 5.44 -> 5.85 us); with longer streams
+  // the third CTA's shallower rings are slower (32 x 28672 x 8192: 22.0 ->
+  // 23.5 us).
   const int64_t blocks = (g.n + g.bn - 1) / g.bn;
-  const bool dense = blocks * g.split_k > g.num_sms;
-  const int smem_budget = dense ? kSwSmemBytesDense : kSwSmemBytes;
-  p.tmem_cols = dense ? kSwTmemCols / 2 : kSwTmemCols;
+  const int64_t ctas = blocks * g.split_k;
+  int per_sm = 1;
+  if (ctas > g.num_sms) {
+    per_sm = 2;
+    if (MT == 1 && (ctas > 2 * static_cast<int64_t>(g.num_sms) ||
+                    (FMT == 0 && p.stages_per_split <= 8)))
+      per_sm = 3;
+  }
+  const int smem_budget = per_sm == 1 ? kSwSmemBytes : kSwSmemPerSm / per_sm - 1024;
+  p.tmem_cols = per_sm == 1 ? kSwTmemCols : per_sm == 2 ? kSwTmemCols / 2 : kSwTmemCols / 4;
   // shared-memory layout (see SwapCfg): as many slots as shared and tensor
   // memory hold
   const int m = 32 * MT;
@@ -529,7 +545,7 @@ cudaError_t launch_typed(const GemmArgs &g, cudaStream_t s) {
 // previous rule's S = 4; 32 x 2048 x 8192: S = 4, 6.87 against 7.5 us with
 // 64-row slices.  Only splits whose CTAs fit on the SMs at one each are
 // considered; with more slices than SMs, S = 1 and launch_gemm_swap runs two
-// CTAs per SM.
+// or three CTAs per SM.
 //
 // Below 8 slices: the first shape (128-row slices first, split along K
 // before the slices get thinner) whose CTAs fill at least three quarters of
